@@ -1,0 +1,166 @@
+"""Seeded synthetic inputs for the NVFP4 paged-KV append + causal prefill path.
+
+This module only draws inputs (normal K/V/Q, outliers, slot mappings, page
+tables, sequence lengths, global decode scales).  It holds none of the method's
+arithmetic, and both the CUDA path and the CPU oracle take their inputs from it.
+
+Workloads (shapes follow the pages' workloads; data is synthetic):
+  tiny        1 x 64 tokens, H_kv=2, H_q=4, D=64, ps=16, 4 pages in shuffled order
+  append      8192 tokens, H_kv=8, D=128, ps=16, 512 pages; 0.1% outliers x20;
+              slots through a random page permutation, 5% (410) slots = -1
+  single      1 x 2048 tokens, H_q=32, H_kv=8, D=128, ps=16, random page table
+  uniform     1024 x 1024 tokens, H_q=32, H_kv=8, D=128, ps=16, random page table
+  ragged      256 sequences, L = round(exp(U[ln 128, ln 16384])), qo_len = kv_len,
+              H_q=32, H_kv=8, D=128, ps=16, random page table
+plus small ragged cases used by the parity tests.
+
+K, V, Q ~ N(0, 1) in fp32, rounded to bf16.  The global decode scales are
+k_scale = amax|K| / (6 * 448) and likewise v_scale (fp32, host).  The seed of
+workload index c is 1000 * c.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+E4M3_MAX = 448.0
+E2M1_MAX = 6.0
+
+
+@dataclass
+class Spec:
+    name: str
+    seed: int
+    num_kv_heads: int
+    head_dim: int
+    page_size: int
+    num_qo_heads: int = 0          # 0: append-only workload
+    seq_lens: list = field(default_factory=list)   # qo_len == kv_len per sequence
+    append_tokens: int = 0         # append-only workloads
+    num_pages: int = 0             # append-only workloads
+    skip_fraction: float = 0.0     # fraction of slots set to -1 (append-only)
+    outlier_p: float = 0.0
+    outlier_scale: float = 20.0
+
+    @property
+    def batch(self) -> int:
+        return len(self.seq_lens)
+
+    @property
+    def group(self) -> int:
+        return self.num_qo_heads // self.num_kv_heads
+
+
+def ragged_lengths(batch: int, lo: int, hi: int, seed: int) -> list:
+    g = torch.Generator().manual_seed(seed + 1)
+    u = torch.rand(batch, generator=g, dtype=torch.float64)
+    lens = torch.exp(math.log(lo) + u * (math.log(hi) - math.log(lo)))
+    return [int(round(x)) for x in lens.tolist()]
+
+
+def spec(name: str) -> Spec:
+    if name == "tiny":
+        return Spec("tiny", 0, num_kv_heads=2, head_dim=64, page_size=16, num_qo_heads=4,
+                    seq_lens=[64])
+    if name == "append":
+        return Spec("append", 1000, num_kv_heads=8, head_dim=128, page_size=16,
+                    append_tokens=8192, num_pages=512, skip_fraction=0.05, outlier_p=0.001)
+    if name == "single":
+        return Spec("single", 2000, num_kv_heads=8, head_dim=128, page_size=16,
+                    num_qo_heads=32, seq_lens=[2048])
+    if name == "uniform":
+        return Spec("uniform", 3000, num_kv_heads=8, head_dim=128, page_size=16,
+                    num_qo_heads=32, seq_lens=[1024] * 1024)
+    if name == "ragged":
+        return Spec("ragged", 4000, num_kv_heads=8, head_dim=128, page_size=16,
+                    num_qo_heads=32, seq_lens=ragged_lengths(256, 128, 16384, 4000))
+    # Small cases for the parity tests: several tiles and ragged tails.
+    if name == "ragged_small":
+        return Spec("ragged_small", 5000, num_kv_heads=2, head_dim=128, page_size=16,
+                    num_qo_heads=8, seq_lens=[1, 17, 128, 129, 300, 520])
+    if name == "ragged_small_d64":
+        return Spec("ragged_small_d64", 6000, num_kv_heads=2, head_dim=64, page_size=32,
+                    num_qo_heads=4, seq_lens=[5, 130, 257, 64])
+    if name == "uniform_small":
+        return Spec("uniform_small", 7000, num_kv_heads=2, head_dim=128, page_size=16,
+                    num_qo_heads=8, seq_lens=[384] * 6)
+    raise KeyError(name)
+
+
+def _bf16_normal(shape, gen, device, outlier_p=0.0, outlier_scale=20.0):
+    x = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    if outlier_p > 0:
+        mask = torch.rand(shape, generator=gen, device=device) < outlier_p
+        x = torch.where(mask, x * outlier_scale, x)
+    return x.to(torch.bfloat16)
+
+
+def global_scale(x: torch.Tensor) -> float:
+    """amax|x| / (6 * 448) in fp32 (the workloads' recipe for k_scale/v_scale)."""
+    amax = x.abs().max().float().item()
+    return float(torch.tensor(amax / (E2M1_MAX * E4M3_MAX), dtype=torch.float32).item())
+
+
+def make(sp: Spec, device="cpu") -> dict:
+    """Draw every input of workload `sp` on `device` (deterministic per device)."""
+    device = torch.device(device)
+    gen = torch.Generator(device=device).manual_seed(sp.seed)
+    hg = torch.Generator().manual_seed(sp.seed + 7)     # host-side permutations
+    H, D, ps = sp.num_kv_heads, sp.head_dim, sp.page_size
+    out = {"spec": sp}
+    if sp.append_tokens:
+        n = sp.append_tokens
+        k = _bf16_normal((n, H, D), gen, device, sp.outlier_p, sp.outlier_scale)
+        v = _bf16_normal((n, H, D), gen, device, sp.outlier_p, sp.outlier_scale)
+        perm = torch.randperm(sp.num_pages, generator=hg)
+        tok = torch.arange(n)
+        slots = perm[tok // ps] * ps + tok % ps
+        n_skip = int(round(sp.skip_fraction * n))
+        skip = torch.randperm(n, generator=hg)[:n_skip]
+        slots[skip] = -1
+        out.update(k=k, v=v, slot_mapping=slots.to(torch.int64), num_pages=sp.num_pages,
+                   k_scale=global_scale(k), v_scale=global_scale(v))
+        return out
+    lens = torch.tensor(sp.seq_lens, dtype=torch.int64)
+    indptr = torch.zeros(sp.batch + 1, dtype=torch.int64)
+    indptr[1:] = torch.cumsum(lens, 0)
+    total = int(indptr[-1])
+    pages_per_seq = (lens + ps - 1) // ps
+    num_pages = int(pages_per_seq.sum())
+    max_pages = int(pages_per_seq.max()) if sp.batch else 0
+    perm = torch.randperm(num_pages, generator=hg)
+    page_table = torch.zeros((sp.batch, max(max_pages, 1)), dtype=torch.int32)
+    slot_mapping = torch.empty(total, dtype=torch.int64)
+    off = 0
+    for b in range(sp.batch):
+        npg = int(pages_per_seq[b])
+        page_table[b, :npg] = perm[off:off + npg].to(torch.int32)
+        off += npg
+        L = int(lens[b])
+        pos = torch.arange(L)
+        slot_mapping[int(indptr[b]):int(indptr[b]) + L] = (
+            page_table[b, pos // ps].to(torch.int64) * ps + pos % ps)
+    k = _bf16_normal((total, H, D), gen, device)
+    v = _bf16_normal((total, H, D), gen, device)
+    q = _bf16_normal((total, sp.num_qo_heads, D), gen, device)
+    out.update(k=k, v=v, q=q, slot_mapping=slot_mapping, page_table=page_table,
+               qo_indptr=indptr.to(torch.int32), kv_indptr=indptr.to(torch.int32),
+               num_pages=num_pages, k_scale=global_scale(k), v_scale=global_scale(v),
+               sm_scale=1.0 / math.sqrt(D))
+    return out
+
+
+def causal_flops(qo_lens, kv_lens, num_qo_heads: int, head_dim: int) -> int:
+    """Algorithmic causal FLOPs: 4 * D * H_q * sum_b sum_i (i + kv - qo + 1)."""
+    total = 0
+    for qo, kv in zip(qo_lens, kv_lens):
+        d = kv - qo
+        total += qo * (qo + 1) // 2 + qo * d
+    return 4 * head_dim * num_qo_heads * total
+
+
+def bits(x: torch.Tensor):
+    """bf16 tensor -> numpy uint16 bit patterns (host)."""
+    return x.detach().cpu().contiguous().view(torch.int16).numpy().view("uint16")
