@@ -1,0 +1,56 @@
+/*
+ * fi_nvfp4_diag.h — diagnostic probes of libfi_nvfp4_diag.so.  They run the
+ * exact device code of libfi_nvfp4.so (the same headers) on small inputs so
+ * that tests can pin each building block separately:
+ *   - the native NVFP4 / FP8 conversions against the CPU codec over all 2^32
+ *     fp32 bit patterns,
+ *   - the per-16 block quantizer (the append's arithmetic),
+ *   - the tile repack (FP4 codes + E4M3 scales -> exact 16-bit staging tile),
+ *   - the tcgen05 operand layouts and descriptors used by the prefill.
+ * The pages have no counterpart of these probes; they exist to test the
+ * library.  All pointers are device pointers; `stream` is a cudaStream_t.
+ * Every call returns 0 on success, 1 on a bad argument, 4 on a CUDA error.
+ */
+#ifndef FI_NVFP4_DIAG_H
+#define FI_NVFP4_DIAG_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* For the `count` fp32 bit patterns first_bits, first_bits+1, ... (mod 2^32):
+ * e4m3_out[i] = E4M3 code (cvt.rn.satfinite.e4m3x2.f32),
+ * e2m1_out[i] = E2M1 code (cvt.rn.satfinite.e2m1x2.f32) in the low nibble. */
+int32_t fi_diag_codec_span(uint32_t first_bits, uint64_t count, uint8_t* e4m3_out,
+                           uint8_t* e2m1_out, void* stream);
+
+/* Quantizes n_blocks blocks of 16 bf16 values (x: [n_blocks][16]) with global
+ * decode scale g, exactly as the append kernel does: packed_out [n_blocks][8]
+ * code bytes, s8_out [n_blocks] scale bytes. */
+int32_t fi_diag_quantize_blocks(const void* x, int64_t n_blocks, float g, uint8_t* packed_out,
+                                uint8_t* s8_out, void* stream);
+
+/* Repacks one raw tile (raw: 128*(D/2) code bytes then 128*(D/16) scale bytes)
+ * as the prefill does (is_v = 0: bf16, 1: fp16; rows >= valid become 0) and
+ * writes the unswizzled 16-bit values to out [128][D] (uint16 bit patterns). */
+int32_t fi_diag_repack_tile(const uint8_t* raw, int32_t head_dim, int32_t is_v, int32_t valid,
+                            uint16_t* out, void* stream);
+
+/* One 128x128x128 tcgen05 MMA product, fp32 result c [128][128]:
+ *   mode 0: c = A * B^T, A bf16 [128][128] loaded by TMA (128B swizzle,
+ *           K-major), B bf16 [128][128] staged K-major by threads (as K tiles);
+ *   mode 1: c = A * B, A fp16 [128][128] stored into tensor memory (as P),
+ *           B fp16 [128 k][128 n] staged MN-major (as V tiles), leading byte
+ *           offset 16384 / stride byte offset 1024 (the prefill's choice);
+ *   mode 2: as mode 1 with the two offsets exchanged;
+ *   mode 3: as mode 1 with A fp16 staged K-major in shared memory.
+ * `status` (device int32) gets bit 16 if a wait ran out of time. */
+int32_t fi_diag_umma(int32_t mode, const void* a, const void* b, float* c, int32_t* status,
+                     void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,267 @@
+// diag.cu — probes that run the library's device code on small inputs
+// (declared in include/fi_nvfp4_diag.h).
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "fi_nvfp4_diag.h"
+#include "nvfp4.cuh"
+
+namespace fi {
+namespace {
+
+constexpr uint64_t kProbeTimeoutNs = 1000000000ull;
+
+__global__ void codec_span_kernel(uint32_t first, uint64_t count, uint8_t* e4, uint8_t* e2) {
+  const uint64_t i = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= count) return;
+  const float x = __uint_as_float(first + static_cast<uint32_t>(i));
+  e4[i] = static_cast<uint8_t>(e4m3_from_f32(x));
+  e2[i] = static_cast<uint8_t>(e2m1x4_from_f32(x, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f) & 0xFu);
+}
+
+__global__ void quantize_blocks_kernel(const __nv_bfloat16* x, int64_t n, float g, uint8_t* packed,
+                                       uint8_t* s8) {
+  const int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (b >= n) return;
+  float lo[8], hi[8];
+  float amax = 0.0f;
+  for (int j = 0; j < 8; ++j) {
+    lo[j] = __bfloat162float(x[b * 16 + j]);
+    hi[j] = __bfloat162float(x[b * 16 + 8 + j]);
+    amax = fmaxf(amax, fmaxf(fabsf(lo[j]), fabsf(hi[j])));
+  }
+  const Quant8 a = quantize8(lo, amax, g);
+  const Quant8 c = quantize8(hi, amax, g);
+  reinterpret_cast<uint32_t*>(packed + b * 8)[0] = a.codes;
+  reinterpret_cast<uint32_t*>(packed + b * 8)[1] = c.codes;
+  s8[b] = static_cast<uint8_t>(a.s8);
+}
+
+template <int D, bool IS_V>
+__global__ void repack_probe_kernel(const uint8_t* raw, int valid, uint16_t* out) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* rs = smem;                    // raw tile
+  uint8_t* st = smem + 16384;            // staging tile (1 KB aligned)
+  constexpr int kRaw = 128 * (D / 2 + D / 16);
+  for (int i = threadIdx.x; i < kRaw; i += blockDim.x) rs[i] = raw[i];
+  __syncthreads();
+  repack_tile<D, IS_V>(rs, st, valid, threadIdx.x, blockDim.x);
+  __syncthreads();
+  for (int i = threadIdx.x; i < 128 * (D / 8); i += blockDim.x) {
+    const int row = i / (D / 8), c = i % (D / 8);
+    const uint4 v = *reinterpret_cast<const uint4*>(st + sw128_offset(row, c));
+    *reinterpret_cast<uint4*>(out + row * D + c * 8) = v;
+  }
+}
+
+struct UmmaProbeParams {
+  CUtensorMap tmap_a;
+  const uint16_t* a;
+  const uint16_t* b;
+  float* c;
+  int32_t* status;
+  int mode;
+};
+
+__global__ void __launch_bounds__(128, 1) umma_probe_kernel(const __grid_constant__ UmmaProbeParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sa = smem;
+  uint8_t* sb = smem + 32768;
+  uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + 65536);
+  uint64_t* bar_mma = bar_tma + 1;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_mma + 1);
+  int* abort_flag = reinterpret_cast<int*>(tslot + 1);
+  const int tid = threadIdx.x;
+  const int warp = tid / 32;
+  if (tid == 0) {
+    mbar_init(bar_tma, 1);
+    mbar_init(bar_mma, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tslot, 256);
+    tmem_relinquish();
+  }
+  // thread tid stages row tid of B (and of A in mode 3) in the swizzled layout
+  for (int c = 0; c < 16; ++c)
+    *reinterpret_cast<uint4*>(sb + sw128_offset(tid, c)) =
+        *reinterpret_cast<const uint4*>(p.b + tid * 128 + c * 8);
+  if (p.mode == 3)
+    for (int c = 0; c < 16; ++c)
+      *reinterpret_cast<uint4*>(sa + sw128_offset(tid, c)) =
+          *reinterpret_cast<const uint4*>(p.a + tid * 128 + c * 8);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+  const uint32_t lane_base = tbase + ((static_cast<uint32_t>(warp) * 32) << 16);
+  if (p.mode == 1 || p.mode == 2) {
+    // row tid of A into columns 128..191: column c holds elements 2c (low
+    // half) and 2c+1 (high half)
+    const uint32_t* arow = reinterpret_cast<const uint32_t*>(p.a + tid * 128);
+    uint32_t v[32];
+    for (int k = 0; k < 32; ++k) v[k] = arow[k];
+    tmem_st32(lane_base + 128, v);
+    for (int k = 0; k < 32; ++k) v[k] = arow[32 + k];
+    tmem_st32(lane_base + 160, v);
+    tmem_st_wait();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const AbortState ab{abort_flag, p.status, kProbeTimeoutNs, 1 << 16};
+  if (tid == 0) {
+    bool ok = true;
+    if (p.mode == 0) {
+      mbar_arrive_expect_tx(bar_tma, 32768);
+      tma_load_3d(sa, &p.tmap_a, bar_tma, 0, 0, 0);
+      tma_load_3d(sa + 16384, &p.tmap_a, bar_tma, 64, 0, 0);
+      ok = mbar_wait(bar_tma, 0, ab);
+    }
+    if (ok) {
+      const uint32_t a_addr = smem_u32(sa), b_addr = smem_u32(sb);
+      if (p.mode == 0) {
+        constexpr uint32_t idesc = idesc_f16(1, 0, 0, 128, 128);
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tbase, smem_desc_sw128(a_addr + off, 16, 1024),
+                 smem_desc_sw128(b_addr + off, 16, 1024), idesc, kk > 0);
+        }
+      } else {
+        constexpr uint32_t idesc = idesc_f16(0, 0, 1, 128, 128);
+        const uint32_t lbo = p.mode == 2 ? 1024 : 16384;
+        const uint32_t sbo = p.mode == 2 ? 16384 : 1024;
+        for (int s = 0; s < 8; ++s) {
+          const uint64_t bd = smem_desc_sw128(b_addr + s * 2048, lbo, sbo);
+          if (p.mode == 3) {
+            const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
+            mma_ss(tbase, smem_desc_sw128(a_addr + off, 16, 1024), bd, idesc, s > 0);
+          } else {
+            mma_ts(tbase, tbase + 128 + s * 8, bd, idesc, s > 0);
+          }
+        }
+      }
+    }
+    mma_commit(bar_mma);
+  }
+  __syncwarp();
+  mbar_wait(bar_mma, 0, ab);
+  tc_fence_after();
+  for (int c = 0; c < 4; ++c) {
+    uint32_t v[32];
+    tmem_ld32(lane_base + c * 32, v);
+    for (int k = 0; k < 32; ++k) p.c[tid * 128 + c * 32 + k] = __uint_as_float(v[k]);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tbase, 256);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_once;
+
+void load_encode() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace fi
+
+extern "C" {
+
+int32_t fi_diag_codec_span(uint32_t first_bits, uint64_t count, uint8_t* e4m3_out,
+                           uint8_t* e2m1_out, void* stream) {
+  if (!e4m3_out || !e2m1_out || count > (1ull << 32)) return 1;
+  if (count == 0) return 0;
+  const unsigned blocks = static_cast<unsigned>((count + 255) / 256);
+  fi::codec_span_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      first_bits, count, e4m3_out, e2m1_out);
+  return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}
+
+int32_t fi_diag_quantize_blocks(const void* x, int64_t n_blocks, float g, uint8_t* packed_out,
+                                uint8_t* s8_out, void* stream) {
+  if (!x || !packed_out || !s8_out || n_blocks < 0 || !fi::a16(packed_out)) return 1;
+  if (n_blocks == 0) return 0;
+  const unsigned blocks = static_cast<unsigned>((n_blocks + 127) / 128);
+  fi::quantize_blocks_kernel<<<blocks, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __nv_bfloat16*>(x), n_blocks, g, packed_out, s8_out);
+  return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}
+
+int32_t fi_diag_repack_tile(const uint8_t* raw, int32_t head_dim, int32_t is_v, int32_t valid,
+                            uint16_t* out, void* stream) {
+  if (!raw || !out || !fi::a16(out) || (head_dim != 64 && head_dim != 128)) return 1;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int smem = 16384 + 32768 + 1024;
+  if (head_dim == 128) {
+    if (is_v) {
+      cudaFuncSetAttribute(fi::repack_probe_kernel<128, true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      fi::repack_probe_kernel<128, true><<<1, 128, smem, s>>>(raw, valid, out);
+    } else {
+      cudaFuncSetAttribute(fi::repack_probe_kernel<128, false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      fi::repack_probe_kernel<128, false><<<1, 128, smem, s>>>(raw, valid, out);
+    }
+  } else {
+    if (is_v) {
+      cudaFuncSetAttribute(fi::repack_probe_kernel<64, true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      fi::repack_probe_kernel<64, true><<<1, 128, smem, s>>>(raw, valid, out);
+    } else {
+      cudaFuncSetAttribute(fi::repack_probe_kernel<64, false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      fi::repack_probe_kernel<64, false><<<1, 128, smem, s>>>(raw, valid, out);
+    }
+  }
+  return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}
+
+int32_t fi_diag_umma(int32_t mode, const void* a, const void* b, float* c, int32_t* status,
+                     void* stream) {
+  if (mode < 0 || mode > 3 || !a || !b || !c || !status || !fi::a16(a) || !fi::a16(b)) return 1;
+  fi::UmmaProbeParams p;
+  memset(&p, 0, sizeof(p));
+  if (mode == 0) {
+    std::call_once(fi::g_once, fi::load_encode);
+    if (!fi::g_encode) return 4;
+    cuuint64_t dims[3] = {128, 1, 128};
+    cuuint64_t strides[2] = {256, 256};
+    cuuint32_t box[3] = {64, 1, 128};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (fi::g_encode(&p.tmap_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return 4;
+  }
+  p.a = static_cast<const uint16_t*>(a);
+  p.b = static_cast<const uint16_t*>(b);
+  p.c = c;
+  p.status = status;
+  p.mode = mode;
+  const int smem = 65536 + 64 + 1024;
+  if (cudaFuncSetAttribute(fi::umma_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem) != cudaSuccess)
+    return 4;
+  fi::umma_probe_kernel<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(p);
+  return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}
+
+}  // extern "C"

@@ -1,0 +1,79 @@
+// internal.h — declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "fi_nvfp4.h"
+
+struct fi_context {
+  int device = 0;
+  int32_t* status_dev = nullptr;  // device status word (FI_DEV_* bits)
+  int num_sms = 0;
+  int64_t l2_bytes = 0;
+};
+
+namespace fi {
+
+constexpr int kTileQ = 128;   // query rows per tile (MMA M)
+constexpr int kTileKV = 128;  // keys per KV tile (MMA N of QK^T, K of PV)
+
+// ---- append ----------------------------------------------------------------
+struct AppendArgs {
+  const void* k;
+  const void* v;
+  int64_t num_tokens;
+  int64_t k_tok_stride;
+  int64_t v_tok_stride;
+  const float* k_scale_dev;  // null: use the host values below
+  const float* v_scale_dev;
+  float k_scale_host;
+  float v_scale_host;
+  const int64_t* slot_mapping;
+  fi_nvfp4_cache cache;
+  int32_t* status;
+};
+fi_status launch_append(const AppendArgs& a, cudaStream_t stream);
+
+// ---- planner ---------------------------------------------------------------
+struct HostPlan {
+  fi_plan_info info{};
+  int32_t num_qo_heads = 0, num_kv_heads = 0, head_dim = 0, page_size = 0;
+  int32_t group = 0;              // num_qo_heads / num_kv_heads
+  int32_t units_per_kv_head = 0;  // group / heads_per_cta
+  int32_t uniform_qo_len = 0, uniform_kv_len = 0;
+  float sm_scale = 0.0f;
+  std::vector<int32_t> work;      // 4 int32 per unit (ragged batches only)
+};
+
+// Validates the arguments and plans on the host only (no CUDA calls).
+// `want_list`: also fill the ordered work list for uniform batches.
+fi_status plan_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t batch,
+                    int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                    int32_t page_size, float sm_scale, int64_t l2_bytes, int32_t default_ctas,
+                    const fi_plan_options* opts, bool want_list, HostPlan* out);
+
+// ---- prefill -----------------------------------------------------------------
+struct PrefillArgs {
+  const HostPlan* plan;
+  const int32_t* qo_indptr_dev;
+  const int32_t* kv_indptr_dev;
+  const int32_t* work_dev;       // null for uniform batches
+  const int32_t* page_table;
+  int32_t page_table_stride;
+  const void* q;
+  fi_nvfp4_cache cache;
+  void* out;
+  float* lse;
+  int32_t* status;
+};
+fi_status launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point.
+bool encode_tensor_map_3d_bf16(void* map_out, const void* base, uint64_t dim0, uint64_t dim1,
+                               uint64_t dim2, uint64_t stride1_bytes, uint64_t stride2_bytes,
+                               uint32_t box0, uint32_t box1, uint32_t box2);
+
+}  // namespace fi

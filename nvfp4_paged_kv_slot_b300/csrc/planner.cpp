@@ -1,0 +1,192 @@
+// planner.cpp — host planning of the causal batched prefill.
+//
+// Follows two analysis pages:
+//  * FlashInfer PR #5043, "FlashInfer의 plan() 함수 최적화: Python max()에서
+//    Tensor.max()로의 전환": max_qo_len / max_kv_len come from one reduction over
+//    the int32 length arrays (no per-element Python loop, lengths as int32).
+//  * FlashInfer PR #3575, "FlashInfer FP8 Causal Attention 최적화: O(1) 디코딩과
+//    글로벌 스케줄링의 힘": §1 the uniform-length flag (checked cheaply as
+//    total == batch * max, as in the page's reviewer section) that lets the
+//    kernel decode tile -> (batch, head, q-tile) arithmetically; §2 global
+//    reverse-Q-tile order (the heaviest causal q-tiles of every sequence and
+//    head first); §3 the L2 gate (global order only if 2 * KV bytes fit in L2).
+// Ragged batches get an explicit work list in the same spirit: heaviest first.
+#include <algorithm>
+#include <cstring>
+#include <numeric>
+
+#include "internal.h"
+
+namespace fi {
+
+namespace {
+
+inline int32_t n_kv_tiles(int32_t qt, int32_t qo_len, int32_t kv_len) {
+  // last query row of the tile, and the last key it may see
+  const int32_t last_row = std::min(qo_len, (qt + 1) * kTileQ) - 1;
+  const int32_t last_key = last_row + (kv_len - qo_len);
+  return last_key / kTileKV + 1;
+}
+
+}  // namespace
+
+fi_status plan_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t batch,
+                    int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                    int32_t page_size, float sm_scale, int64_t l2_bytes, int32_t default_ctas,
+                    const fi_plan_options* opts, bool want_list, HostPlan* out) {
+  if (!out || batch < 0 || (batch > 0 && (!qo_indptr || !kv_indptr)))
+    return FI_ERR_INVALID_ARGUMENT;
+  if (num_kv_heads <= 0 || num_qo_heads <= 0 || num_qo_heads % num_kv_heads != 0)
+    return FI_ERR_INVALID_ARGUMENT;
+  if (head_dim != 64 && head_dim != 128) return FI_ERR_UNSUPPORTED;
+  if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128)
+    return FI_ERR_UNSUPPORTED;
+  const int32_t schedule = opts ? opts->schedule : 0;
+  if (schedule < 0 || schedule > 2) return FI_ERR_INVALID_ARGUMENT;
+  if (opts && opts->num_ctas < 0) return FI_ERR_INVALID_ARGUMENT;
+  if (batch > 0 && (qo_indptr[0] != 0 || kv_indptr[0] != 0)) return FI_ERR_INVALID_ARGUMENT;
+
+  HostPlan& P = *out;
+  P = HostPlan{};
+  P.num_qo_heads = num_qo_heads;
+  P.num_kv_heads = num_kv_heads;
+  P.head_dim = head_dim;
+  P.page_size = page_size;
+  P.group = num_qo_heads / num_kv_heads;
+  P.sm_scale = sm_scale;
+
+  // One pass: the maxima, and the validity of every length.
+  int32_t max_qo = 0, max_kv = 0;
+  for (int32_t b = 0; b < batch; ++b) {
+    const int32_t qo = qo_indptr[b + 1] - qo_indptr[b];
+    const int32_t kv = kv_indptr[b + 1] - kv_indptr[b];
+    if (qo < 0 || kv < 0 || qo > kv) return FI_ERR_INVALID_ARGUMENT;
+    max_qo = std::max(max_qo, qo);
+    max_kv = std::max(max_kv, kv);
+  }
+  fi_plan_info& I = P.info;
+  I.batch = batch;
+  I.max_qo_len = max_qo;
+  I.max_kv_len = max_kv;
+  I.total_qo_len = batch > 0 ? qo_indptr[batch] : 0;
+  I.total_kv_len = batch > 0 ? kv_indptr[batch] : 0;
+  // every length equals the maximum iff the totals are batch * maximum
+  I.is_uniform = (I.total_qo_len == static_cast<int64_t>(batch) * max_qo &&
+                  I.total_kv_len == static_cast<int64_t>(batch) * max_kv)
+                     ? 1
+                     : 0;
+  I.heads_per_cta = (P.group % 2 == 0) ? 2 : 1;
+  P.units_per_kv_head = P.group / I.heads_per_cta;
+  I.head_units = num_kv_heads * P.units_per_kv_head;
+  I.q_tiles = (max_qo + kTileQ - 1) / kTileQ;
+  I.kv_bytes = I.total_kv_len * num_kv_heads * 2 * (head_dim / 2 + head_dim / 16);
+  if (schedule == 1) {
+    I.global_reverse = 1;
+  } else if (schedule == 2) {
+    I.global_reverse = 0;
+  } else {
+    I.global_reverse = (2 * I.kv_bytes <= l2_bytes) ? 1 : 0;
+  }
+
+  const int32_t HU = I.head_units;
+  if (I.is_uniform) {
+    P.uniform_qo_len = max_qo;
+    P.uniform_kv_len = max_kv;
+    I.num_units = static_cast<int64_t>(batch) * HU * I.q_tiles;
+    if (want_list) {
+      P.work.resize(static_cast<size_t>(I.num_units) * 4);
+      const int64_t BH = static_cast<int64_t>(batch) * HU;
+      for (int64_t t = 0; t < I.num_units; ++t) {
+        int64_t b, hu, qt;
+        if (I.global_reverse) {
+          qt = I.q_tiles - 1 - t / BH;
+          const int64_t r = t % BH;
+          hu = r / batch;
+          b = r % batch;
+        } else {
+          b = t / (static_cast<int64_t>(HU) * I.q_tiles);
+          const int64_t r = t % (static_cast<int64_t>(HU) * I.q_tiles);
+          hu = r / I.q_tiles;
+          qt = I.q_tiles - 1 - r % I.q_tiles;
+        }
+        P.work[4 * t + 0] = static_cast<int32_t>(b);
+        P.work[4 * t + 1] = static_cast<int32_t>(hu);
+        P.work[4 * t + 2] = static_cast<int32_t>(qt);
+        P.work[4 * t + 3] = 0;
+      }
+    }
+  } else {
+    // Ragged: enumerate (sequence, head unit, q-tile) with its cost in KV tiles.
+    struct Item {
+      int32_t b, hu, qt, cost;
+    };
+    std::vector<Item> items;
+    int64_t n = 0;
+    for (int32_t b = 0; b < batch; ++b)
+      n += static_cast<int64_t>((qo_indptr[b + 1] - qo_indptr[b] + kTileQ - 1) / kTileQ) * HU;
+    items.reserve(static_cast<size_t>(n));
+    if (I.global_reverse) {
+      for (int32_t b = 0; b < batch; ++b) {
+        const int32_t qo = qo_indptr[b + 1] - qo_indptr[b];
+        const int32_t kv = kv_indptr[b + 1] - kv_indptr[b];
+        const int32_t tiles = (qo + kTileQ - 1) / kTileQ;
+        for (int32_t hu = 0; hu < HU; ++hu)
+          for (int32_t qt = 0; qt < tiles; ++qt)
+            items.push_back({b, hu, qt, n_kv_tiles(qt, qo, kv)});
+      }
+      // heaviest tiles of all sequences and heads first (stable: ties keep the
+      // head-then-sequence order of the page's global mapping)
+      std::stable_sort(items.begin(), items.end(),
+                       [](const Item& x, const Item& y) { return x.cost > y.cost; });
+    } else {
+      // per (sequence, head unit) groups, reversed q-tiles inside each group;
+      // groups ordered longest first so the longest chains start early
+      std::vector<int32_t> order(batch);
+      std::iota(order.begin(), order.end(), 0);
+      std::stable_sort(order.begin(), order.end(), [&](int32_t x, int32_t y) {
+        return (kv_indptr[x + 1] - kv_indptr[x]) > (kv_indptr[y + 1] - kv_indptr[y]);
+      });
+      for (int32_t b : order) {
+        const int32_t qo = qo_indptr[b + 1] - qo_indptr[b];
+        const int32_t kv = kv_indptr[b + 1] - kv_indptr[b];
+        const int32_t tiles = (qo + kTileQ - 1) / kTileQ;
+        for (int32_t hu = 0; hu < HU; ++hu)
+          for (int32_t qt = tiles - 1; qt >= 0; --qt)
+            items.push_back({b, hu, qt, n_kv_tiles(qt, qo, kv)});
+      }
+    }
+    I.num_units = static_cast<int64_t>(items.size());
+    P.work.resize(items.size() * 4);
+    for (size_t t = 0; t < items.size(); ++t) {
+      P.work[4 * t + 0] = items[t].b;
+      P.work[4 * t + 1] = items[t].hu;
+      P.work[4 * t + 2] = items[t].qt;
+      P.work[4 * t + 3] = items[t].cost;
+    }
+  }
+  const int32_t ctas = (opts && opts->num_ctas > 0) ? opts->num_ctas : default_ctas;
+  I.num_ctas = static_cast<int32_t>(std::min<int64_t>(I.num_units, std::max(ctas, 1)));
+  return FI_OK;
+}
+
+}  // namespace fi
+
+extern "C" fi_status fi_prefill_plan_host(const int32_t* qo_indptr_host,
+                                          const int32_t* kv_indptr_host, int32_t batch,
+                                          int32_t num_qo_heads, int32_t num_kv_heads,
+                                          int32_t head_dim, int32_t page_size, int64_t l2_bytes,
+                                          const fi_plan_options* opts, fi_plan_info* info,
+                                          int32_t* work_out, int64_t work_capacity) {
+  if (!info || (work_out && work_capacity < 0)) return FI_ERR_INVALID_ARGUMENT;
+  fi::HostPlan P;
+  const fi_status st = fi::plan_host(qo_indptr_host, kv_indptr_host, batch, num_qo_heads,
+                                     num_kv_heads, head_dim, page_size, 0.0f, l2_bytes, 148,
+                                     opts, work_out != nullptr, &P);
+  if (st != FI_OK) return st;
+  *info = P.info;
+  if (work_out) {
+    const int64_t n = std::min<int64_t>(work_capacity, P.info.num_units);
+    std::memcpy(work_out, P.work.data(), static_cast<size_t>(n) * 4 * sizeof(int32_t));
+  }
+  return FI_OK;
+}

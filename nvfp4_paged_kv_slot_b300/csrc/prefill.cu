@@ -1,0 +1,554 @@
+// prefill.cu — causal batched prefill over the NVFP4 paged KV cache, sm_103a.
+//
+// What it computes follows the analysis pages of FlashInfer PRs:
+//  * #4769 "FlashInfer NVFP4 KV 타일 리팩(Repack)을 통한 성능 최적화": every NVFP4
+//    KV tile is dequantized once into a 16-bit staging tile outside the MMA loop
+//    (there: repack_fp4_tile_to_16b feeding ldmatrix on SM80).
+//  * #3575 "FlashInfer FP8 Causal Attention 최적화: O(1) 디코딩과 글로벌 스케줄링의
+//    힘": causal attention with GQA; §1 O(1) tile decoding for uniform lengths;
+//    §2 global reverse-Q-tile order, heaviest tiles first; §3 the L2 gate.
+//
+// B300 design (one persistent CTA per SM, warp-specialized):
+//   warp 0        load: TMA of the Q tiles (128B swizzle), bulk copies of the
+//                 FP4 pages and E4M3 scales of each KV tile into a raw ring
+//   warp 1        MMA: one thread issues tcgen05.mma (QK^T: bf16 SS; PV: fp16
+//                 TS with P in tensor memory) and tcgen05.commit
+//   warps 2-3     idle
+//   WG 1..NQ      softmax, one warpgroup per Q tile, one thread per query row:
+//                 online softmax in fp32 (base 2), P written back to tensor
+//                 memory over S, lazy O rescale, epilogue
+//   last WG       repack: raw FP4 tile -> exact 16-bit tile in the swizzled
+//                 layout the tensor cores read (K as bf16, V as fp16)
+// The NQ Q tiles of a CTA are NQ query heads of one GQA group at the same
+// positions, so every staged KV tile is repacked once and used NQ times.
+// Tensor memory: S_i at column 128 i, O_i after all S.  All waits are bounded.
+#include <cmath>
+
+#include "internal.h"
+#include "nvfp4.cuh"
+
+namespace fi {
+
+namespace {
+
+constexpr int kRawStages = 4;
+constexpr int kStgStages = 3;
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
+constexpr uint64_t kDrainNs = 100000000ull;     // 0.1 s per wait while aborting
+
+struct PrefillParams {
+  CUtensorMap tmap_q;  // 3-D view of q: (head_dim, num_qo_heads, total_qo)
+  const uint8_t* k_data;
+  const uint8_t* v_data;
+  const uint8_t* k_sf;
+  const uint8_t* v_sf;
+  const float* k_scale;
+  const float* v_scale;
+  __nv_bfloat16* out;
+  float* lse;
+  const int32_t* qo_indptr;
+  const int32_t* kv_indptr;
+  const int4* work;
+  const int32_t* page_table;
+  int32_t* status;
+  int64_t pt_stride;
+  int32_t batch, num_qo_heads, num_kv_heads, num_pages, page_size;
+  int32_t group, units_per_kv_head, head_units;
+  int32_t uniform, global_reverse, uni_qo_len, uni_kv_len, q_tiles;
+  int64_t num_units;
+  float sm_scale;
+};
+
+template <int D, int NQ>
+struct Layout {
+  static constexpr int kQTile = kTileQ * D * 2;
+  static constexpr int kStg = kTileKV * D * 2;
+  static constexpr int kRawData = kTileKV * D / 2;
+  static constexpr int kRawSf = kTileKV * D / 16;
+  static constexpr int kRaw = kRawData + kRawSf;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffStg = kOffQ + NQ * kQTile;
+  static constexpr int kOffRaw = kOffStg + kStgStages * kStg;
+  static constexpr int kOffBar = kOffRaw + kRawStages * kRaw;
+  // q_full, q_empty, raw_full[], raw_empty[], stg_full[], stg_empty[],
+  // s_full[NQ], p_full[NQ], o_full[NQ], drain
+  static constexpr int kNumBars = 2 + 2 * kRawStages + 2 * kStgStages + 3 * NQ + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kBytes = kOffMisc + 16;
+  static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
+  static constexpr int kTmemCols = (NQ * 128 + NQ * D) <= 256 ? 256 : 512;
+  static constexpr int kThreads = 128 * (NQ + 2);
+  static_assert(kOffStg % 1024 == 0 && kStg % 1024 == 0, "swizzled tiles need 1 KB alignment");
+  static_assert(kRaw % 16 == 0 && kOffRaw % 16 == 0, "bulk copies need 16 B alignment");
+};
+
+struct Unit {
+  int b, hk, hq0, qt, qo_start, qo_len, kv_len, n_kv;
+};
+
+// tile id -> (sequence, head unit, q-tile): arithmetic for uniform batches
+// (#3575 §1, §2), the planner's list otherwise.
+__device__ __forceinline__ Unit decode_unit(const PrefillParams& p, int64_t u, int nq) {
+  Unit w;
+  int hu;
+  if (p.uniform) {
+    const int64_t BH = static_cast<int64_t>(p.batch) * p.head_units;
+    if (p.global_reverse) {
+      w.qt = p.q_tiles - 1 - static_cast<int>(u / BH);
+      const int64_t r = u % BH;
+      hu = static_cast<int>(r / p.batch);
+      w.b = static_cast<int>(r % p.batch);
+    } else {
+      const int64_t per_b = static_cast<int64_t>(p.head_units) * p.q_tiles;
+      w.b = static_cast<int>(u / per_b);
+      const int r = static_cast<int>(u % per_b);
+      hu = r / p.q_tiles;
+      w.qt = p.q_tiles - 1 - r % p.q_tiles;
+    }
+    w.qo_len = p.uni_qo_len;
+    w.kv_len = p.uni_kv_len;
+    w.qo_start = w.b * p.uni_qo_len;
+  } else {
+    const int4 it = __ldg(p.work + u);
+    w.b = it.x;
+    hu = it.y;
+    w.qt = it.z;
+    w.qo_start = __ldg(p.qo_indptr + w.b);
+    w.qo_len = __ldg(p.qo_indptr + w.b + 1) - w.qo_start;
+    w.kv_len = __ldg(p.kv_indptr + w.b + 1) - __ldg(p.kv_indptr + w.b);
+  }
+  w.hk = hu / p.units_per_kv_head;
+  w.hq0 = w.hk * p.group + (hu % p.units_per_kv_head) * nq;
+  const int last_row = min(w.qo_len, (w.qt + 1) * kTileQ) - 1;
+  w.n_kv = (last_row + w.kv_len - w.qo_len) / kTileKV + 1;
+  return w;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+template <int D, int NQ>
+__global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
+    nvfp4_prefill_kernel(const __grid_constant__ PrefillParams p) {
+  using L = Layout<D, NQ>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* q_smem = smem + L::kOffQ;
+  uint8_t* stg_smem = smem + L::kOffStg;
+  uint8_t* raw_smem = smem + L::kOffRaw;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
+  uint64_t* q_full = bars + 0;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* raw_full = bars + 2;
+  uint64_t* raw_empty = raw_full + kRawStages;
+  uint64_t* stg_full = raw_empty + kRawStages;
+  uint64_t* stg_empty = stg_full + kStgStages;
+  uint64_t* s_full = stg_empty + kStgStages;
+  uint64_t* p_full = s_full + NQ;
+  uint64_t* o_full = p_full + NQ;
+  uint64_t* drain = o_full + NQ;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
+  int* abort_flag = reinterpret_cast<int*>(smem + L::kOffMisc + 4);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int s = 0; s < kRawStages; ++s) {
+      mbar_init(raw_full + s, 1);
+      mbar_init(raw_empty + s, 128);
+    }
+    for (int s = 0; s < kStgStages; ++s) {
+      mbar_init(stg_full + s, 128);
+      mbar_init(stg_empty + s, 1);
+    }
+    for (int i = 0; i < NQ; ++i) {
+      mbar_init(s_full + i, 1);
+      mbar_init(p_full + i, 128);
+      mbar_init(o_full + i, 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const AbortState ab{abort_flag, p.status, kTimeoutNs, FI_DEV_WAIT_TIMEOUT};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------- load warp
+    if (lane == 0) prefetch_tensormap(&p.tmap_q);
+    uint32_t raw_k = 0;
+    int it = 0;
+    bool ok = true;
+    int q_issued = -1;  // iteration of the last Q load issued
+    const uint32_t pg_data = static_cast<uint32_t>(p.page_size) * (D / 2);
+    const uint32_t pg_sf = static_cast<uint32_t>(p.page_size) * (D / 16);
+    const int pages_per_tile = kTileKV / p.page_size;
+    for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
+      const Unit w = decode_unit(p, u, NQ);
+      if (!mbar_wait(q_empty, (it & 1) ^ 1, ab)) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(q_full, NQ * L::kQTile);
+        for (int i = 0; i < NQ; ++i)
+          for (int h = 0; h < D / 64; ++h)
+            tma_load_3d(q_smem + i * L::kQTile + h * 16384, &p.tmap_q, q_full, h * 64,
+                        w.hq0 + i, w.qo_start + w.qt * kTileQ);
+      }
+      q_issued = it;
+      __syncwarp();
+      const int32_t* pt = p.page_table + static_cast<int64_t>(w.b) * p.pt_stride;
+      const int seq_pages = (w.kv_len + p.page_size - 1) / p.page_size;
+      for (int j = 0; ok && j < w.n_kv; ++j) {
+        for (int t = 0; t < 2; ++t, ++raw_k) {
+          const int slot = raw_k % kRawStages;
+          if (!mbar_wait(raw_empty + slot, ((raw_k / kRawStages) & 1) ^ 1, ab)) {
+            ok = false;
+            break;
+          }
+          const int first = j * pages_per_tile;
+          const int npg = min(pages_per_tile, seq_pages - first);
+          if (lane == 0) mbar_arrive_expect_tx(raw_full + slot, npg * (pg_data + pg_sf));
+          __syncwarp();
+          if (lane < npg) {
+            int page = __ldg(pt + first + lane);
+            if (page < 0 || page >= p.num_pages) {
+              atomicOr(p.status, FI_DEV_PAGE_OOB);
+              page = 0;
+            }
+            const int64_t blk = static_cast<int64_t>(page) * p.num_kv_heads + w.hk;
+            const uint8_t* gd = (t ? p.v_data : p.k_data) + blk * pg_data;
+            const uint8_t* gs = (t ? p.v_sf : p.k_sf) + blk * pg_sf;
+            uint8_t* sd = raw_smem + slot * L::kRaw;
+            bulk_g2s(sd + lane * pg_data, gd, pg_data, raw_full + slot);
+            bulk_g2s(sd + L::kRawData + lane * pg_sf, gs, pg_sf, raw_full + slot);
+          }
+          __syncwarp();
+        }
+      }
+    }
+    if (!ok) {
+      // Aborting: wait (briefly) for the copies this warp may still have in
+      // flight so that no copy lands in shared memory after the CTA exits.
+      volatile int drain_flag = 0;
+      const AbortState drain_ab{&drain_flag, nullptr, kDrainNs, 0};
+      const uint32_t n = raw_k < kRawStages ? raw_k : kRawStages;
+      for (uint32_t f = raw_k - n; f < raw_k; ++f)
+        mbar_wait(raw_full + (f % kRawStages), (f / kRawStages) & 1, drain_ab);
+      if (q_issued >= 0) mbar_wait(q_full, q_issued & 1, drain_ab);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA warp
+    if (lane == 0) {
+      constexpr uint32_t kIdescQK = idesc_f16(1, 0, 0, kTileQ, kTileKV);
+      constexpr uint32_t kIdescPV = idesc_f16(0, 0, 1, kTileQ, D);
+      const uint32_t q_addr = smem_u32(q_smem);
+      const uint32_t stg_addr = smem_u32(stg_smem);
+      uint32_t stg_k = 0;
+      uint32_t pk[NQ];
+      for (int i = 0; i < NQ; ++i) pk[i] = 0;
+      int it = 0;
+      bool ok = true;
+      auto issue_qk = [&](int i, uint32_t ss) {
+        const uint32_t d_tmem = tmem_base + i * 128;
+        const uint32_t qa = q_addr + i * L::kQTile;
+        const uint32_t kb = stg_addr + ss * L::kStg;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(d_tmem, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
+                 kIdescQK, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int i, uint32_t ss, bool acc) {
+        const uint32_t d_tmem = tmem_base + NQ * 128 + i * D;
+        const uint32_t a_tmem = tmem_base + i * 128;
+        const uint32_t vb = stg_addr + ss * L::kStg;
+#pragma unroll
+        for (int s = 0; s < kTileKV / 16; ++s)
+          mma_ts(d_tmem, a_tmem + s * 8, smem_desc_sw128(vb + s * 2048, 16384, 1024), kIdescPV,
+                 (acc || s > 0) ? 1u : 0u);
+      };
+      for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
+        const Unit w = decode_unit(p, u, NQ);
+        if (!mbar_wait(q_full, it & 1, ab)) { ok = false; break; }
+        // K tile 0
+        uint32_t ss_k = stg_k % kStgStages;
+        if (!mbar_wait(stg_full + ss_k, (stg_k / kStgStages) & 1, ab)) { ok = false; break; }
+        ++stg_k;
+        tc_fence_after();
+        for (int i = 0; i < NQ; ++i) {
+          issue_qk(i, ss_k);
+          mma_commit(s_full + i);
+        }
+        if (w.n_kv == 1) mma_commit(q_empty);
+        mma_commit(stg_empty + ss_k);
+        for (int j = 0; ok && j < w.n_kv; ++j) {
+          const uint32_t ss_v = stg_k % kStgStages;
+          if (!mbar_wait(stg_full + ss_v, (stg_k / kStgStages) & 1, ab)) { ok = false; break; }
+          ++stg_k;
+          const bool more = j + 1 < w.n_kv;
+          for (int i = 0; i < NQ; ++i) {
+            if (!mbar_wait(p_full + i, pk[i] & 1, ab)) { ok = false; break; }
+            ++pk[i];
+            tc_fence_after();
+            issue_pv(i, ss_v, j > 0);
+            if (i == NQ - 1) mma_commit(stg_empty + ss_v);
+            if (more) {
+              if (i == 0) {
+                ss_k = stg_k % kStgStages;
+                if (!mbar_wait(stg_full + ss_k, (stg_k / kStgStages) & 1, ab)) { ok = false; break; }
+                ++stg_k;
+                tc_fence_after();
+              }
+              issue_qk(i, ss_k);
+              mma_commit(s_full + i);
+              if (i == NQ - 1) {
+                mma_commit(stg_empty + ss_k);
+                if (j + 2 == w.n_kv) mma_commit(q_empty);
+              }
+            }
+          }
+        }
+        if (!ok) break;
+        for (int i = 0; i < NQ; ++i) mma_commit(o_full + i);
+      }
+      // Every MMA this thread issued has completed once `drain` arrives.
+      mma_commit(drain);
+      volatile int drain_flag = 0;
+      const AbortState drain_ab{&drain_flag, nullptr, ok ? kTimeoutNs : kDrainNs, 0};
+      mbar_wait(drain, 0, drain_ab);
+    }
+  } else if (warp >= 4 && warp < 4 * (NQ + 1)) {
+    // ------------------------------------------------------------- softmax
+    const int i = warp / 4 - 1;
+    const int r = threadIdx.x - 128 * (i + 1);  // query row within the tile
+    const uint32_t lane_base = tmem_base + ((static_cast<uint32_t>(r / 32) * 32) << 16);
+    const uint32_t s_col = lane_base + i * 128;
+    const uint32_t o_col = lane_base + NQ * 128 + i * D;
+    const float ks = __ldg(p.k_scale);
+    const float vs = __ldg(p.v_scale);
+    if (blockIdx.x == 0 && threadIdx.x == 128) {
+      int bad = 0;
+      if (!(isfinite(ks) && ks > 0.0f)) bad |= FI_DEV_BAD_K_SCALE;
+      if (!(isfinite(vs) && vs > 0.0f)) bad |= FI_DEV_BAD_V_SCALE;
+      if (bad) atomicOr(p.status, bad);
+    }
+    const float scale_log2 = p.sm_scale * ks * 1.4426950408889634f;
+    uint32_t sk = 0;
+    int it = 0;
+    bool ok = true;
+    for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
+      const Unit w = decode_unit(p, u, NQ);
+      const int row_q = w.qt * kTileQ + r;
+      const int delta = w.kv_len - w.qo_len;
+      const int limit = row_q + delta;                 // last key this row sees
+      const int tile_first_limit = w.qt * kTileQ + delta;
+      float m_ref = -INFINITY;
+      float l = 0.0f;
+      for (int j = 0; j < w.n_kv; ++j) {
+        if (!mbar_wait(s_full + i, sk & 1, ab)) { ok = false; break; }
+        ++sk;
+        tc_fence_after();
+        const int key0 = j * kTileKV;
+        const bool masked = key0 + kTileKV - 1 > tile_first_limit;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(s_col + c * 32, v);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const float s = __uint_as_float(v[k]);
+            if (!masked || key0 + c * 32 + k <= limit) mx = fmaxf(mx, s);
+          }
+        }
+        const float m_new = fmaxf(m_ref, mx * scale_log2);
+        if (m_new > m_ref + 8.0f) {
+          // lazy rescale: only when the running max grows by more than 2^8
+          const float alpha = ex2(m_ref - m_new);
+          l *= alpha;
+          if (j > 0) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(o_col + c * 32, o);
+#pragma unroll
+              for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+              tmem_st32(o_col + c * 32, o);
+            }
+          }
+          m_ref = m_new;
+        }
+        float rs = 0.0f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(s_col + c * 32, v);
+          uint32_t pp[16];
+#pragma unroll
+          for (int k = 0; k < 32; k += 2) {
+            const bool vis0 = !masked || key0 + c * 32 + k <= limit;
+            const bool vis1 = !masked || key0 + c * 32 + k + 1 <= limit;
+            const float p0 = vis0 ? ex2(fmaf(__uint_as_float(v[k]), scale_log2, -m_ref)) : 0.0f;
+            const float p1 = vis1 ? ex2(fmaf(__uint_as_float(v[k + 1]), scale_log2, -m_ref)) : 0.0f;
+            rs += p0 + p1;
+            pp[k / 2] = pack_f16x2(p0, p1);
+          }
+          tmem_st16(s_col + c * 16, pp);
+        }
+        l += rs;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(p_full + i);
+      }
+      if (!ok) break;
+      if (!mbar_wait(o_full + i, it & 1, ab)) { ok = false; break; }
+      tc_fence_after();
+      const bool valid = row_q < w.qo_len;
+      const float inv = vs / l;
+      __nv_bfloat16* dst =
+          p.out + (static_cast<int64_t>(w.qo_start + row_q) * p.num_qo_heads + w.hq0 + i) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(o_col + c * 32, o);
+        if (valid) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint4 v4;
+            v4.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv, __uint_as_float(o[8 * k + 1]) * inv);
+            v4.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv);
+            v4.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv);
+            v4.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv);
+            d4[k] = v4;
+          }
+        }
+      }
+      if (valid && p.lse)
+        p.lse[static_cast<int64_t>(w.qo_start + row_q) * p.num_qo_heads + w.hq0 + i] =
+            (m_ref + log2f(l)) * 0.6931471805599453f;
+      // the next unit's first PV may overwrite O_i only after these loads
+      tc_fence_before();
+    }
+  } else if (warp >= 4 * (NQ + 1)) {
+    // ------------------------------------------------------------- repack
+    const int rt = threadIdx.x - 128 * (NQ + 1);
+    uint32_t raw_k = 0, stg_k = 0;
+    bool ok = true;
+    for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+      const Unit w = decode_unit(p, u, NQ);
+      for (int j = 0; ok && j < w.n_kv; ++j) {
+        const int valid = min(kTileKV, w.kv_len - j * kTileKV);
+        for (int t = 0; t < 2; ++t, ++raw_k, ++stg_k) {
+          const int rs = raw_k % kRawStages;
+          const int ss = stg_k % kStgStages;
+          if (!mbar_wait(raw_full + rs, (raw_k / kRawStages) & 1, ab)) { ok = false; break; }
+          if (!mbar_wait(stg_empty + ss, ((stg_k / kStgStages) & 1) ^ 1, ab)) { ok = false; break; }
+          if (t)
+            repack_tile<D, true>(raw_smem + rs * L::kRaw, stg_smem + ss * L::kStg, valid, rt, 128);
+          else
+            repack_tile<D, false>(raw_smem + rs * L::kRaw, stg_smem + ss * L::kStg, valid, rt, 128);
+          fence_proxy_async_smem();
+          mbar_arrive(stg_full + ss);
+          mbar_arrive(raw_empty + rs);
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, L::kTmemCols);
+}
+
+template <int D, int NQ>
+fi_status launch_impl(const PrefillParams& p, int grid, cudaStream_t stream) {
+  using L = Layout<D, NQ>;
+  auto kern = nvfp4_prefill_kernel<D, NQ>;
+  // at least ~116 KB so that a single CTA (and its 256-512 TMEM columns)
+  // occupies each SM
+  const int smem = L::kAlloc > 118784 ? L::kAlloc : 118784;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+      cudaSuccess)
+    return FI_ERR_CUDA;
+  kern<<<grid, L::kThreads, smem, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? FI_OK : FI_ERR_CUDA;
+}
+
+}  // namespace
+
+fi_status launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
+  const HostPlan& P = *a.plan;
+  if (P.info.num_units == 0) return FI_OK;
+  PrefillParams p;
+  memset(&p, 0, sizeof(p));
+  const int D = P.head_dim;
+  if (!encode_tensor_map_3d_bf16(&p.tmap_q, a.q, D, P.num_qo_heads, P.info.total_qo_len,
+                                 static_cast<uint64_t>(D) * 2,
+                                 static_cast<uint64_t>(P.num_qo_heads) * D * 2, 64, 1, kTileQ))
+    return FI_ERR_CUDA;
+  p.k_data = a.cache.k_data;
+  p.v_data = a.cache.v_data;
+  p.k_sf = a.cache.k_sf;
+  p.v_sf = a.cache.v_sf;
+  p.k_scale = a.cache.k_scale;
+  p.v_scale = a.cache.v_scale;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.lse = a.lse;
+  p.qo_indptr = a.qo_indptr_dev;
+  p.kv_indptr = a.kv_indptr_dev;
+  p.work = reinterpret_cast<const int4*>(a.work_dev);
+  p.page_table = a.page_table;
+  p.status = a.status;
+  p.pt_stride = a.page_table_stride;
+  p.batch = P.info.batch;
+  p.num_qo_heads = P.num_qo_heads;
+  p.num_kv_heads = P.num_kv_heads;
+  p.num_pages = a.cache.num_pages;
+  p.page_size = P.page_size;
+  p.group = P.group;
+  p.units_per_kv_head = P.units_per_kv_head;
+  p.head_units = P.info.head_units;
+  p.uniform = P.info.is_uniform;
+  p.global_reverse = P.info.global_reverse;
+  p.uni_qo_len = P.uniform_qo_len;
+  p.uni_kv_len = P.uniform_kv_len;
+  p.q_tiles = P.info.q_tiles;
+  p.num_units = P.info.num_units;
+  p.sm_scale = P.sm_scale;
+  const int grid = P.info.num_ctas;
+  const int nq = P.info.heads_per_cta;
+  if (D == 128) return nq == 2 ? launch_impl<128, 2>(p, grid, stream) : launch_impl<128, 1>(p, grid, stream);
+  return nq == 2 ? launch_impl<64, 2>(p, grid, stream) : launch_impl<64, 1>(p, grid, stream);
+}
+
+}  // namespace fi

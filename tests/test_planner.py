@@ -1,0 +1,152 @@
+"""Host planner (no GPU): max lengths, uniform flag, L2 gate and tile order.
+
+Mirrors the pages' plan tests: FlashInfer PR #5043 analysis page ("plan() 함수
+최적화"), test_batch_prefill_plan_max_lens over seq_lens of dtypes None / int32 /
+uint32 and several batch and page sizes; and the scheduling rules of the PR
+#3575 page (O(1) uniform decode, global reverse-Q-tile order, L2 gate).
+"""
+import numpy as np
+import pytest
+
+import nvfp4_paged_kv_slot_b300 as fi
+
+L2 = 126 * 2**20
+
+
+def _lens(batch, seed, lo=1, hi=3000):
+    rng = np.random.default_rng(seed)
+    return rng.integers(lo, hi, size=batch)
+
+
+@pytest.mark.parametrize("dtype", [None, np.int32, np.uint32, np.int64])
+@pytest.mark.parametrize("batch", [1, 7, 64, 256, 1024])
+@pytest.mark.parametrize("page_size", [16, 64])
+def test_plan_max_lens(dtype, batch, page_size):
+    kv = _lens(batch, batch)
+    qo = np.minimum(kv, _lens(batch, batch + 1))
+    if dtype is None:          # lengths given directly as indptr (no seq_lens)
+        kv_ind = np.concatenate([[0], np.cumsum(kv)]).astype(np.int32)
+    else:
+        kv_ind = fi.indptr_from_lens(kv.astype(dtype))
+    qo_ind = fi.indptr_from_lens(qo)
+    info, _ = fi.fi_prefill_plan_host(qo_ind, kv_ind, 32, 8, 128, page_size, with_list=False)
+    assert info["max_qo_len"] == int(qo.max())
+    assert info["max_kv_len"] == int(kv.max())
+    assert info["total_qo_len"] == int(qo.sum())
+    assert info["total_kv_len"] == int(kv.sum())
+    assert info["batch"] == batch
+
+
+def test_uniform_flag_and_o1_decode_orders():
+    B, L = 6, 300
+    ind = fi.indptr_from_lens([L] * B)
+    for schedule, global_rev in ((1, 1), (2, 0)):
+        info, work = fi.fi_prefill_plan_host(ind, ind, 8, 2, 128, 16, schedule=schedule)
+        assert info["is_uniform"] == 1 and info["global_reverse"] == global_rev
+        q_tiles = (L + 127) // 128
+        HU = info["head_units"]
+        assert info["heads_per_cta"] == 2 and HU == 2 * 2
+        assert info["num_units"] == B * HU * q_tiles == work.shape[0]
+        # every (b, hu, qt) exactly once
+        assert len({tuple(w[:3]) for w in work}) == work.shape[0]
+        for t, (b, hu, qt, _) in enumerate(work):
+            if global_rev:   # page formula: q-step from the end, head-major, batch fastest
+                assert qt == q_tiles - 1 - t // (B * HU)
+                assert hu == (t % (B * HU)) // B and b == (t % (B * HU)) % B
+            else:
+                assert b == t // (HU * q_tiles)
+                assert qt == q_tiles - 1 - (t % (HU * q_tiles)) % q_tiles
+
+
+def test_uniform_check_is_totals_based():
+    # lengths that are not all equal are never "uniform"
+    qo = fi.indptr_from_lens([128, 128, 127])
+    info, _ = fi.fi_prefill_plan_host(qo, qo, 4, 4, 64, 16, with_list=False)
+    assert info["is_uniform"] == 0
+    # equal qo but different kv -> not uniform either
+    kv = fi.indptr_from_lens([128, 129, 128])
+    qo = fi.indptr_from_lens([128, 128, 128])
+    info, _ = fi.fi_prefill_plan_host(qo, kv, 4, 4, 64, 16, with_list=False)
+    assert info["is_uniform"] == 0
+
+
+def test_l2_gate():
+    H_kv, D = 8, 128
+    per_token = H_kv * 2 * (D // 2 + D // 16)        # NVFP4 K and V bytes per token
+    fits = (L2 // 2) // per_token                    # 2 * kv_bytes <= L2
+    ind = fi.indptr_from_lens([fits])
+    info, _ = fi.fi_prefill_plan_host(ind, ind, 32, H_kv, D, 16, l2_bytes=L2, with_list=False)
+    assert info["kv_bytes"] == fits * per_token and info["global_reverse"] == 1
+    ind = fi.indptr_from_lens([fits + 1])
+    info, _ = fi.fi_prefill_plan_host(ind, ind, 32, H_kv, D, 16, l2_bytes=L2, with_list=False)
+    assert info["global_reverse"] == 0
+
+
+def _n_kv(qt, qo, kv):
+    last_row = min(qo, (qt + 1) * 128) - 1
+    return (last_row + kv - qo) // 128 + 1
+
+
+@pytest.mark.parametrize("schedule", [1, 2])
+def test_ragged_work_list(schedule):
+    qo = [1, 17, 128, 129, 300, 520, 0, 2000]
+    kv = [1, 40, 128, 300, 300, 600, 5, 2100]
+    qi, ki = fi.indptr_from_lens(qo), fi.indptr_from_lens(kv)
+    info, work = fi.fi_prefill_plan_host(qi, ki, 8, 2, 128, 16, schedule=schedule)
+    assert info["is_uniform"] == 0
+    HU = info["head_units"]
+    want = {(b, hu, qt) for b in range(len(qo)) for hu in range(HU)
+            for qt in range((qo[b] + 127) // 128)}
+    got = [tuple(w[:3]) for w in work]
+    assert sorted(got) == sorted(want) and len(got) == len(want)
+    for b, hu, qt, cost in work:
+        assert cost == _n_kv(qt, qo[b], kv[b])
+    if schedule == 1:   # global: heaviest first
+        assert all(work[i, 3] >= work[i + 1, 3] for i in range(len(work) - 1))
+    else:               # per (sequence, head unit): contiguous, q-tiles reversed
+        seen = []
+        for b, hu, qt, _ in work:
+            if not seen or seen[-1][:2] != (b, hu):
+                seen.append((b, hu, qt))
+            else:
+                assert qt == seen[-1][2] - 1
+                seen[-1] = (b, hu, qt)
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(qo=[0, 5], kv=[0, 4]), fi.FI_ERR_INVALID_ARGUMENT),        # qo_len > kv_len
+    (dict(qo=[0, 5, 3], kv=[0, 5, 9]), fi.FI_ERR_INVALID_ARGUMENT),  # decreasing indptr
+    (dict(qo=[1, 5], kv=[1, 5]), fi.FI_ERR_INVALID_ARGUMENT),        # indptr not from 0
+    (dict(hq=6, hk=4), fi.FI_ERR_INVALID_ARGUMENT),                  # H_q % H_kv != 0
+    (dict(d=96), fi.FI_ERR_UNSUPPORTED),
+    (dict(ps=8), fi.FI_ERR_UNSUPPORTED),
+])
+def test_plan_rejects(args, code):
+    qo = args.get("qo", [0, 4])
+    kv = args.get("kv", [0, 4])
+    with pytest.raises(fi.FiError) as e:
+        fi.fi_prefill_plan_host(qo, kv, args.get("hq", 4), args.get("hk", 2), args.get("d", 64),
+                                args.get("ps", 16))
+    assert e.value.status == code
+
+
+def test_uint32_lengths_converted():
+    lens = np.array([5, 4000, 17], dtype=np.uint32)
+    ind = fi.indptr_from_lens(lens)
+    assert ind.dtype == np.int32 and list(ind) == [0, 5, 4005, 4022]
+    with pytest.raises(ValueError):
+        fi.indptr_from_lens(np.array([2**31], dtype=np.uint32))
+
+
+def test_workload_shapes():
+    import workloads as W
+    info, _ = fi.fi_prefill_plan_host(*([fi.indptr_from_lens(W.spec("uniform").seq_lens)] * 2),
+                                      32, 8, 128, 16, with_list=False)
+    assert info["is_uniform"] == 1 and info["global_reverse"] == 0   # 1.2 GB KV > L2
+    assert info["num_units"] == 1024 * 16 * 8
+    sp = W.spec("single")
+    ind = fi.indptr_from_lens(sp.seq_lens)
+    info, _ = fi.fi_prefill_plan_host(ind, ind, 32, 8, 128, 16, with_list=False)
+    assert info["global_reverse"] == 1                                 # 2.4 MB KV fits in L2
+    sp = W.spec("ragged")
+    assert len(sp.seq_lens) == 256 and min(sp.seq_lens) >= 128 and max(sp.seq_lens) <= 16384
