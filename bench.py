@@ -1,0 +1,501 @@
+"""Benchmark of the NVFP4 paged-KV hot path on B300: quantize-append -> plan ->
+causal prefill, through the C ABI of libfi_nvfp4.so.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload uniform|single|ragged] [--no-e2e] [--no-cpu-baseline]
+
+One step is one pass of the whole path over one batch: fi_nvfp4_append of every
+token's K/V into the cache, fi_prefill_plan of the batch, fi_prefill_run.  The
+default workload is the uniform batch: 1024 sequences of qo_len = kv_len = 1024,
+H_q = 32, H_kv = 8, head_dim = 128, page_size = 16 (synthetic N(0,1) bf16
+inputs, random page table).  `value` is the causal prefill FLOPs of a step
+divided by the measured step time (TFLOP/s); the append bandwidth of the
+8192-token append workload (cold L2: 24 rotating buffer sets captured in one
+CUDA graph) is reported beside it.
+
+Under torchrun (N > 1) every rank runs its own independent copy of the
+workload on its own GPU (the path has no exchange step): scaling is weak and
+`value` is the FLOPs of all ranks over the slowest rank's time.
+
+--impl reference times the CPU oracle (the slow, plain C++ definition of the
+method) on a bounded sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "causal prefill TFLOP/s over NVFP4 paged KV; append GB/s; % of roofline"
+UNIT = "TFLOP/s"
+
+WORKLOAD_DESC = {
+    "uniform": "uniform batch: 1024 x (qo_len=kv_len=1024), H_q=32, H_kv=8, head_dim=128, "
+               "page_size=16, NVFP4 paged KV, append + plan + causal prefill",
+    "single": "single sequence 2048x2048, H_q=32, H_kv=8, head_dim=128, page_size=16, "
+              "append + plan + causal prefill",
+    "ragged": "ragged batch: 256 sequences, qo_len=kv_len log-uniform in [128,16384], H_q=32, "
+              "H_kv=8, head_dim=128, page_size=16, append + plan + causal prefill",
+}
+
+
+# ----------------------------------------------------------------- helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+            "source": "fallback"}
+
+
+def append_bytes(num_tokens_written, num_tokens_skipped, num_kv_heads, head_dim):
+    """Algorithmic bytes of one append: per written token read K and V bf16
+    rows, write K and V NVFP4 rows (codes + scales) and read its 8-byte slot;
+    per skipped token read its slot; plus the two 4-byte scales."""
+    per_tok = num_kv_heads * (2 * head_dim * 2) + num_kv_heads * 2 * (head_dim // 2 +
+                                                                        head_dim // 16) + 8
+    return num_tokens_written * per_tok + num_tokens_skipped * 8 + 8
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- our arm
+class PathRunner:
+    """Device-resident inputs and outputs of one workload, and one step of the
+    path (append -> plan -> run) through the C ABI."""
+
+    def __init__(self, fi, name, device):
+        self.fi = fi
+        sp = W.spec(name)
+        self.sp = sp
+        d = W.make(sp, device=device)
+        self.d = d
+        self.device = device
+        self.k, self.v, self.q = d["k"], d["v"], d["q"]
+        self.slots = d["slot_mapping"].to(device)
+        self.page_table = d["page_table"].to(device)
+        self.qo_indptr = d["qo_indptr"].numpy()
+        self.kv_indptr = d["kv_indptr"].numpy()
+        ks = torch.tensor([d["k_scale"]], dtype=torch.float32, device=device)
+        vs = torch.tensor([d["v_scale"]], dtype=torch.float32, device=device)
+        self.cache = fi.NVFP4Cache(d["num_pages"], sp.num_kv_heads, sp.page_size, sp.head_dim,
+                                   device=device, k_scale=ks, v_scale=vs, fill=0)
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty(self.q.shape[:2], dtype=torch.float32, device=device)
+        self.ctx = fi.fi_context_create()
+        self.plan = fi.fi_plan_create(self.ctx)
+        lens = np.diff(self.qo_indptr).tolist()
+        self.flops = W.causal_flops(lens, lens, sp.num_qo_heads, sp.head_dim)
+        self.tokens = int(self.qo_indptr[-1])
+        self.append_bytes = append_bytes(self.tokens, 0, sp.num_kv_heads, sp.head_dim)
+
+    def step(self, stream, ev=None):
+        fi, sp = self.fi, self.sp
+        if ev is not None:
+            ev[0].record(stream)
+        fi.fi_nvfp4_append(self.ctx, self.k, self.v, self.cache.k_scale, self.cache.v_scale,
+                           self.slots, self.cache, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        fi.fi_prefill_plan(self.plan, self.qo_indptr, self.kv_indptr, self.page_table,
+                           sp.num_qo_heads, sp.num_kv_heads, sp.head_dim, sp.page_size,
+                           sm_scale=self.d["sm_scale"], stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        fi.fi_prefill_run(self.plan, self.q, self.cache, self.out, self.lse, stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    def status(self):
+        return self.fi.fi_device_status(self.ctx)
+
+    def close(self):
+        self.fi.fi_plan_destroy(self.plan)
+        self.fi.fi_context_destroy(self.ctx)
+
+
+def barrier(dist_on):
+    if dist_on:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, dist_on, device):
+    if not dist_on:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_device_steps(runner, stream, steps, warmup, dist_on, device):
+    for _ in range(warmup):
+        runner.step(stream)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier(dist_on)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(steps):
+        runner.step(stream, evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist_on)
+    total_ms = start.elapsed_time(end)
+    append_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    prefill_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    return total_ms, append_ms, prefill_ms
+
+
+def time_e2e(runner, stream, steps, warmup):
+    """Same step through the public API with host inputs: pinned host K/V/Q,
+    slot_mapping and page_table are copied to the device inside the timed
+    region, and the attention output (and LSE) are read back to pinned host
+    memory at the end of every step."""
+    hk = runner.k.cpu().pin_memory()
+    hv = runner.v.cpu().pin_memory()
+    hq = runner.q.cpu().pin_memory()
+    hs = runner.slots.cpu().pin_memory()
+    hpt = runner.page_table.cpu().pin_memory()
+    ho = torch.empty(runner.out.shape, dtype=runner.out.dtype, pin_memory=True)
+    hl = torch.empty(runner.lse.shape, dtype=runner.lse.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in (hk, hv, hq, hs, hpt))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+
+    def one():
+        with torch.cuda.stream(stream):
+            runner.k.copy_(hk, non_blocking=True)
+            runner.v.copy_(hv, non_blocking=True)
+            runner.q.copy_(hq, non_blocking=True)
+            runner.slots.copy_(hs, non_blocking=True)
+            runner.page_table.copy_(hpt, non_blocking=True)
+            runner.step(stream)
+            ho.copy_(runner.out, non_blocking=True)
+            hl.copy_(runner.lse, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    stream.synchronize()
+    dt = time.perf_counter() - t0
+    return dt / steps, h2d, d2h
+
+
+def time_append_cold(fi, device, n_sets=24, reps=20):
+    """Append of the 8192-token workload: n_sets distinct input / slot / cache
+    buffer sets (together far larger than L2) appended back to back from one
+    CUDA graph, as a model's per-layer appends run.  Returns per-append ms
+    (cold L2) and the same append repeated on one set (warm L2)."""
+    sp = W.spec("append")
+    d = W.make(sp, device=device)
+    ctx = fi.fi_context_create()
+    ks = torch.tensor([d["k_scale"]], dtype=torch.float32, device=device)
+    vs = torch.tensor([d["v_scale"]], dtype=torch.float32, device=device)
+    sets = []
+    for _ in range(n_sets):
+        c = fi.NVFP4Cache(sp.num_pages, sp.num_kv_heads, sp.page_size, sp.head_dim,
+                          device=device, k_scale=ks, v_scale=vs, fill=0)
+        sets.append((d["k"].clone(), d["v"].clone(), d["slot_mapping"].to(device).clone(), c))
+    set_bytes = sum(t.numel() * t.element_size() for t in sets[0][:3]) + \
+        sum(t.numel() for t in (sets[0][3].k_data, sets[0][3].v_data, sets[0][3].k_sf,
+                                 sets[0][3].v_sf))
+    s = torch.cuda.Stream(device=device)
+    for k, v, sl, c in sets:
+        fi.fi_nvfp4_append(ctx, k, v, ks, vs, sl, c, stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for k, v, sl, c in sets:
+                fi.fi_nvfp4_append(ctx, k, v, ks, vs, sl, c, stream=s)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(reps):
+            g.replay()
+        e1.record(s)
+    torch.cuda.synchronize()
+    cold_ms = e0.elapsed_time(e1) / (reps * n_sets)
+    # warm: one set, back to back
+    k, v, sl, c = sets[0]
+    gw = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(gw, stream=s):
+            for _ in range(n_sets):
+                fi.fi_nvfp4_append(ctx, k, v, ks, vs, sl, c, stream=s)
+    gw.replay()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(reps):
+            gw.replay()
+        e1.record(s)
+    torch.cuda.synchronize()
+    warm_ms = e0.elapsed_time(e1) / (reps * n_sets)
+    status = fi.fi_device_status(ctx)
+    fi.fi_context_destroy(ctx)
+    n_skip = int((d["slot_mapping"] < 0).sum())
+    nbytes = append_bytes(sp.append_tokens - n_skip, n_skip, sp.num_kv_heads, sp.head_dim)
+    return {"cold_ms": cold_ms, "warm_ms": warm_ms, "bytes": nbytes, "status": status,
+            "sets": n_sets, "set_bytes": set_bytes, "launches": n_sets * reps}
+
+
+# ----------------------------------------------------------------- oracle legs
+def oracle_sample(name, budget_s, seed=0):
+    """Times the CPU oracle on a bounded sample of workload `name`: two of its
+    sequences (same per-sequence shape, freshly drawn seeded inputs) are
+    appended by the oracle into a host cache, then sampled attention rows of
+    those sequences are computed until `budget_s` seconds of attention time
+    are used.  Returns (flops, seconds, description, threads, append seconds)."""
+    import oracle as O
+    sp = W.sample_spec(name, 2, seed)
+    d = W.make(sp, device="cpu")
+    qo = d["qo_indptr"].numpy().astype(np.int64)
+    rng = np.random.default_rng(seed)
+    threads = O.max_threads()
+    host = O.new_cache(d["num_pages"], sp.num_kv_heads, sp.page_size, sp.head_dim, 0)
+    t0 = time.perf_counter()
+    st = O.append(W.bits(d["k"]), W.bits(d["v"]), d["k_scale"], d["v_scale"],
+                  d["slot_mapping"].numpy(), host)
+    t_append = time.perf_counter() - t0
+    assert st == 0
+    # rows: (token, head) pairs of the sample in random order, until the budget is used
+    all_rows = np.stack(np.meshgrid(np.arange(int(qo[-1])), np.arange(sp.num_qo_heads),
+                                    indexing="ij"), -1).reshape(-1, 2).astype(np.int64)
+    rng.shuffle(all_rows)
+    seq_of = np.searchsorted(qo, all_rows[:, 0], side="right") - 1
+    flops, t_attn, done, chunk = 0, 0.0, 0, 256
+    qb = W.bits(d["q"])
+    pt = d["page_table"].numpy()
+    while done < len(all_rows) and t_attn < budget_s:
+        rows = all_rows[done:done + chunk]
+        t0 = time.perf_counter()
+        O.prefill(qb, qo.astype(np.int32), qo.astype(np.int32), pt, host, sp.num_qo_heads,
+                  d["k_scale"], d["v_scale"], d["sm_scale"], rows=rows, threads=threads)
+        t_attn += time.perf_counter() - t0
+        i = rows[:, 0] - qo[seq_of[done:done + chunk]]
+        flops += int(4 * sp.head_dim * (i + 1).sum())
+        done += len(rows)
+        chunk = min(chunk * 2, 8192)
+    desc = (f"{len(sp.seq_lens)} sequences of the workload (lengths {sp.seq_lens}): oracle "
+            f"append ({t_append:.2f} s) + fp64 attention of {done} sampled (token, head) rows "
+            f"({t_attn:.2f} s); TFLOP/s over the sampled rows' causal FLOPs")
+    return flops, t_attn, desc, threads, t_append
+
+
+def run_reference(args):
+    """--impl reference: the oracle, timed on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample(args.workload, budget / 4, seed=1)
+    tot_f, tot_t, desc, threads = 0, 0.0, "", 1
+    for i in range(args.steps):
+        f, t, desc, threads, _ = oracle_sample(args.workload, budget, seed=2 + i)
+        tot_f += f
+        tot_t += t
+    value = tot_f / tot_t / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC[args.workload], "sampled": True},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_DESC), default="uniform")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-append-bench", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    dist_on = world > 1
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    if dist_on:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    import nvfp4_paged_kv_slot_b300 as fi
+    peaks = load_peaks()
+    runner = PathRunner(fi, args.workload, device)
+    stream = torch.cuda.Stream(device=device)
+    # correctness guard: the step must run clean before it is timed
+    runner.step(stream)
+    st = runner.status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the first step")
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    total_ms, append_ms, prefill_ms = time_device_steps(runner, stream, args.steps, args.warmup,
+                                                        dist_on, device)
+    clk = clocks.stop()
+    st = runner.status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the timed steps")
+    step_ms = max_over_ranks(total_ms / args.steps, dist_on, device)
+    value = world * runner.flops / (step_ms * 1e-3) / 1e12
+    pf_ms = statistics.mean(prefill_ms)
+    ap_ms = statistics.mean(append_ms)
+    pf_tflops = runner.flops / (pf_ms * 1e-3) / 1e12
+    peak_sus = peaks["bf16_tflops_sustained"]
+    peak_burst = peaks["bf16_tflops"]
+
+    e2e = None
+    if not args.no_e2e:
+        e2e_s, h2d, d2h = time_e2e(runner, stream, args.e2e_steps, 1)
+        e2e_s = max_over_ranks(e2e_s, dist_on, device)
+        e2e = {"value": world * runner.flops / e2e_s / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": args.e2e_steps, "ms_per_step": e2e_s * 1e3}
+
+    app = None
+    if not args.no_append_bench and rank == 0:
+        a = time_append_cold(fi, device)
+        app = {"workload": "append bandwidth: 8192 tokens, H_kv=8, head_dim=128, "
+                           "page_size=16, 5% slots=-1, random page permutation",
+               "gbs_cold_l2": a["bytes"] / (a["cold_ms"] * 1e-3) / 1e9,
+               "gbs_warm_l2": a["bytes"] / (a["warm_ms"] * 1e-3) / 1e9,
+               "us_cold_l2": a["cold_ms"] * 1e3, "us_warm_l2": a["warm_ms"] * 1e3,
+               "algorithmic_bytes": a["bytes"],
+               "frac_cold_l2": a["bytes"] / (a["cold_ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
+               "peak_gbs": peaks["hbm_gbs"],
+               "cold_l2_method": f"{a['sets']} rotating buffer sets "
+                                 f"({a['sets'] * a['set_bytes'] / 2**20:.0f} MiB) in one CUDA graph",
+               "status": a["status"]}
+
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        f, t, desc, threads, _ = oracle_sample(args.workload, args.cpu_budget)
+        cpu = {"value": f / t / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": desc}
+
+    runner_append_gbs = runner.append_bytes / (ap_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC[args.workload], "tokens": runner.tokens,
+                   "flops_per_step": runner.flops,
+                   "l2": "inputs larger than L2 (Q 8.6 GB, KV cache 1.2 GB per step)"
+                   if args.workload == "uniform" else "see workload",
+                   "parallelism": f"replicas x{world} (independent shards, no collective)"},
+        "roofline": {"bound": "tensor", "achieved": pf_tflops, "peak": peak_sus,
+                     "unit": "TFLOP/s", "frac": pf_tflops / peak_sus, "traffic": None,
+                     "kernel": "nvfp4_prefill_kernel", "peak_kind":
+                     f"bf16 dense sustained ({peaks['source']})",
+                     "frac_of_burst_peak": pf_tflops / peak_burst,
+                     "ms_per_launch": pf_ms},
+        "append_in_step": {"ms_per_launch": ap_ms, "gbs": runner_append_gbs,
+                           "frac": runner_append_gbs / peaks["hbm_gbs"]},
+        "append_bench": app,
+        "clocks": clk,
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "cpu_baseline": cpu,
+    }
+    runner.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist_on:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

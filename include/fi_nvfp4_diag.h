@@ -43,9 +43,10 @@ int32_t fi_diag_repack_tile(const uint8_t* raw, int32_t head_dim, int32_t is_v, 
  *           K-major), B bf16 [128][128] staged K-major by threads (as K tiles);
  *   mode 1: c = A * B, A fp16 [128][128] stored into tensor memory (as P),
  *           B fp16 [128 k][128 n] staged MN-major (as V tiles), leading byte
- *           offset 16384 / stride byte offset 1024 (the prefill's choice);
- *   mode 2: as mode 1 with the two offsets exchanged;
+ *           offset 16384 (between 64-column blocks) and stride byte offset
+ *           1024 (between groups of 8 k rows), the prefill's choice;
  *   mode 3: as mode 1 with A fp16 staged K-major in shared memory.
+ * Any other mode returns 1.
  * `status` (device int32) gets bit 16 if a wait ran out of time. */
 int32_t fi_diag_umma(int32_t mode, const void* a, const void* b, float* c, int32_t* status,
                      void* stream);

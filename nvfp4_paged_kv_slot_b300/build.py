@@ -1,6 +1,9 @@
 """Build libfi_nvfp4.so (and the diagnostic probe library) in-tree with nvcc.
 
-    python -m nvfp4_paged_kv_slot_b300.build [--force]
+    python nvfp4_paged_kv_slot_b300/build.py [--force] [-v]
+
+The script uses the standard library only, so it runs before the package (whose
+import needs the built library) can be imported.
 
 Targets sm_103a only.  No fast-math: the quantizer relies on IEEE division
 and separately rounded products (it uses explicit _rn intrinsics as well).

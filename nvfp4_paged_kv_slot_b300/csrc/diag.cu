@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(128, 1) umma_probe_kernel(const __grid_constan
   tc_fence_after();
   const uint32_t tbase = *tslot;
   const uint32_t lane_base = tbase + ((static_cast<uint32_t>(warp) * 32) << 16);
-  if (p.mode == 1 || p.mode == 2) {
+  if (p.mode == 1) {
     // row tid of A into columns 128..191: column c holds elements 2c (low
     // half) and 2c+1 (high half)
     const uint32_t* arow = reinterpret_cast<const uint32_t*>(p.a + tid * 128);
@@ -136,10 +136,8 @@ __global__ void __launch_bounds__(128, 1) umma_probe_kernel(const __grid_constan
         }
       } else {
         constexpr uint32_t idesc = idesc_f16(0, 0, 1, 128, 128);
-        const uint32_t lbo = p.mode == 2 ? 1024 : 16384;
-        const uint32_t sbo = p.mode == 2 ? 16384 : 1024;
         for (int s = 0; s < 8; ++s) {
-          const uint64_t bd = smem_desc_sw128(b_addr + s * 2048, lbo, sbo);
+          const uint64_t bd = smem_desc_sw128(b_addr + s * 2048, 16384, 1024);
           if (p.mode == 3) {
             const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32;
             mma_ss(tbase, smem_desc_sw128(a_addr + off, 16, 1024), bd, idesc, s > 0);
@@ -235,7 +233,7 @@ int32_t fi_diag_repack_tile(const uint8_t* raw, int32_t head_dim, int32_t is_v, 
 
 int32_t fi_diag_umma(int32_t mode, const void* a, const void* b, float* c, int32_t* status,
                      void* stream) {
-  if (mode < 0 || mode > 3 || !a || !b || !c || !status || !fi::a16(a) || !fi::a16(b)) return 1;
+  if ((mode != 0 && mode != 1 && mode != 3) || !a || !b || !c || !status || !fi::a16(a) || !fi::a16(b)) return 1;
   fi::UmmaProbeParams p;
   memset(&p, 0, sizeof(p));
   if (mode == 0) {

@@ -89,6 +89,17 @@ def spec(name: str) -> Spec:
     raise KeyError(name)
 
 
+def sample_spec(name: str, n_seqs: int, seed: int = 0) -> Spec:
+    """A bounded sample of workload `name`: n_seqs of its sequence lengths
+    (chosen with `seed`), same heads, head_dim and page size, its own seed."""
+    sp = spec(name)
+    g = torch.Generator().manual_seed(sp.seed + 100 + seed)
+    idx = torch.randperm(sp.batch, generator=g)[:min(n_seqs, sp.batch)].tolist()
+    return Spec(f"{name}_sample{seed}", sp.seed + 100 + seed, num_kv_heads=sp.num_kv_heads,
+                head_dim=sp.head_dim, page_size=sp.page_size, num_qo_heads=sp.num_qo_heads,
+                seq_lens=[sp.seq_lens[i] for i in sorted(idx)])
+
+
 def _bf16_normal(shape, gen, device, outlier_p=0.0, outlier_scale=20.0):
     x = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
     if outlier_p > 0:
