@@ -66,6 +66,24 @@ def load_peaks():
             "source": "fallback"}
 
 
+def recorded_traffic(key):
+    """DRAM bytes per launch recorded from an ncu capture (profiles/traffic.json),
+    or None when the kernel's sources changed since the capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(key)
+    if not rec:
+        return None
+    h = hashlib.sha256()
+    for src in rec["sources"]:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    return rec["dram_bytes_per_launch"] if h.hexdigest()[:16] == rec["source_sha256_16"] else None
+
+
 def append_bytes(num_tokens_written, num_tokens_skipped, num_kv_heads, head_dim):
     """Algorithmic bytes of one append: per written token read K and V bf16
     rows, write K and V NVFP4 rows (codes + scales) and read its 8-byte slot;
@@ -127,9 +145,11 @@ class PathRunner:
     """Device-resident inputs and outputs of one workload, and one step of the
     path (append -> plan -> run) through the C ABI."""
 
-    def __init__(self, fi, name, device):
+    def __init__(self, fi, name, device, seqs=0):
         self.fi = fi
         sp = W.spec(name)
+        if seqs:
+            sp.seq_lens = sp.seq_lens[:seqs]
         self.sp = sp
         d = W.make(sp, device=device)
         self.d = d
@@ -320,7 +340,9 @@ def oracle_sample(name, budget_s, seed=0):
     those sequences are computed until `budget_s` seconds of attention time
     are used.  Returns (flops, seconds, description, threads, append seconds)."""
     import oracle as O
-    sp = W.sample_spec(name, 2, seed)
+    full = W.spec(name)
+    n_seqs = max(1, min(full.batch, math.ceil(32768 * full.batch / sum(full.seq_lens))))
+    sp = W.sample_spec(name, n_seqs, seed)
     d = W.make(sp, device="cpu")
     qo = d["qo_indptr"].numpy().astype(np.int64)
     rng = np.random.default_rng(seed)
@@ -349,7 +371,9 @@ def oracle_sample(name, budget_s, seed=0):
         flops += int(4 * sp.head_dim * (i + 1).sum())
         done += len(rows)
         chunk = min(chunk * 2, 8192)
-    desc = (f"{len(sp.seq_lens)} sequences of the workload (lengths {sp.seq_lens}): oracle "
+    lens_txt = str(sp.seq_lens) if len(sp.seq_lens) <= 12 else f"{len(sp.seq_lens)} x {sp.seq_lens[0]}" \
+        if len(set(sp.seq_lens)) == 1 else f"{sum(sp.seq_lens)} tokens in total"
+    desc = (f"{len(sp.seq_lens)} sequences of the workload ({lens_txt}): oracle "
             f"append ({t_append:.2f} s) + fp64 attention of {done} sampled (token, head) rows "
             f"({t_attn:.2f} s); TFLOP/s over the sampled rows' causal FLOPs")
     return flops, t_attn, desc, threads, t_append
@@ -395,6 +419,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-append-bench", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--seqs", type=int, default=0,
+                    help="use only the first N sequences of the workload (profiling cases)")
+    ap.add_argument("--only", choices=["all", "append"], default="all",
+                    help="append: run only the cold-L2 append measurement")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -411,7 +439,14 @@ def main():
 
     import nvfp4_paged_kv_slot_b300 as fi
     peaks = load_peaks()
-    runner = PathRunner(fi, args.workload, device)
+    if args.only == "append":
+        a = time_append_cold(fi, device)
+        gbs = a["bytes"] / (a["cold_ms"] * 1e-3) / 1e9
+        print(json.dumps({"append_only": True, "gbs_cold_l2": gbs, "us_cold_l2": a["cold_ms"] * 1e3,
+                          "us_warm_l2": a["warm_ms"] * 1e3, "frac": gbs / peaks["hbm_gbs"],
+                          "status": a["status"]}), flush=True)
+        return 0 if a["status"] == 0 else 1
+    runner = PathRunner(fi, args.workload, device, args.seqs)
     stream = torch.cuda.Stream(device=device)
     # correctness guard: the step must run clean before it is timed
     runner.step(stream)
@@ -453,6 +488,7 @@ def main():
                "us_cold_l2": a["cold_ms"] * 1e3, "us_warm_l2": a["warm_ms"] * 1e3,
                "algorithmic_bytes": a["bytes"],
                "frac_cold_l2": a["bytes"] / (a["cold_ms"] * 1e-3) / 1e9 / peaks["hbm_gbs"],
+               "traffic": recorded_traffic("append_8192"),
                "peak_gbs": peaks["hbm_gbs"],
                "cold_l2_method": f"{a['sets']} rotating buffer sets "
                                  f"({a['sets'] * a['set_bytes'] / 2**20:.0f} MiB) in one CUDA graph",
@@ -469,13 +505,17 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD_DESC[args.workload], "tokens": runner.tokens,
+        "config": {"workload": WORKLOAD_DESC[args.workload] +
+                   (f" (first {args.seqs} sequences only)" if args.seqs else ""),
+                   "tokens": runner.tokens,
                    "flops_per_step": runner.flops,
                    "l2": "inputs larger than L2 (Q 8.6 GB, KV cache 1.2 GB per step)"
                    if args.workload == "uniform" else "see workload",
                    "parallelism": f"replicas x{world} (independent shards, no collective)"},
         "roofline": {"bound": "tensor", "achieved": pf_tflops, "peak": peak_sus,
-                     "unit": "TFLOP/s", "frac": pf_tflops / peak_sus, "traffic": None,
+                     "unit": "TFLOP/s", "frac": pf_tflops / peak_sus,
+                     "traffic": recorded_traffic("prefill_uniform")
+                     if args.workload == "uniform" and not args.seqs else None,
                      "kernel": "nvfp4_prefill_kernel", "peak_kind":
                      f"bf16 dense sustained ({peaks['source']})",
                      "frac_of_burst_peak": pf_tflops / peak_burst,
