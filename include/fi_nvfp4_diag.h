@@ -32,6 +32,18 @@ int32_t fi_diag_codec_span(uint32_t first_bits, uint64_t count, uint8_t* e4m3_ou
 int32_t fi_diag_quantize_blocks(const void* x, int64_t n_blocks, float g, uint8_t* packed_out,
                                 uint8_t* s8_out, void* stream);
 
+/* Checks the append's division by the block decode scale: for all 65536 bf16
+ * inputs x and each of the n_d fp32 divisors d_values[i] (device array), where
+ * the quantizer takes its Markstein path (d in [2^-98, 2^100], |x| <= 2^100 d),
+ * compares its quotient with the IEEE quotient x / d.  counts (device, 4 x
+ * uint64, zeroed by the caller): [0] checked pairs, [1] pairs whose E2M1 codes
+ * differ, [2] pairs with |x| >= 2^-100 and a normal IEEE quotient whose bits
+ * differ, [3] pairs with |x| < 2^-100 whose bits differ (the code is the same
+ * there by construction).  first_bad (device, 2 x uint32): x bits and divisor
+ * index of a pair counted in [1] or [2].  n_d <= 65535. */
+int32_t fi_diag_div_check(const float* d_values, int32_t n_d, unsigned long long* counts,
+                          uint32_t* first_bad, void* stream);
+
 /* Repacks one raw tile (raw: 128*(D/2) code bytes then 128*(D/16) scale bytes)
  * as the prefill does (is_v = 0: bf16, 1: fp16; rows >= valid become 0) and
  * writes the unswizzled 16-bit values to out [128][D] (uint16 bit patterns). */

@@ -3,11 +3,13 @@
 // 최적화로 인한 동기화 제거": the append kernel checks the device scales itself
 // instead of the host reading them back).
 //
-// One thread owns 8 consecutive head-dim elements of one (token, tensor, head)
-// row: a 128-bit bf16 load, the per-16 amax shared with the neighbouring lane
-// by one shuffle, native E4M3/E2M1 conversion, one 32-bit store of 8 codes and
-// (even lanes) one scale byte.  The kernel is HBM-bound: per written token it
-// reads 2*H*D*2 bytes and writes 2*H*(D/2 + D/16) bytes.
+// Grid: x = groups of kTokPerCta tokens, y = (tensor, kv head) = (K|V, h).
+// One thread owns one 16-element block of one (token, tensor, head) row: two
+// 128-bit bf16 loads, the block amax in registers, native E4M3/E2M1
+// conversion, one 64-bit store of 16 codes and one scale byte.  All index
+// arithmetic inside the kernel is 32-bit except the final byte offsets; the
+// page size is a power of two (shift and mask).  The kernel is HBM-bound: per
+// written token it reads 2*H*D*2 bytes and writes 2*H*(D/2 + D/16) bytes.
 #include "internal.h"
 #include "nvfp4.cuh"
 
@@ -29,9 +31,9 @@ struct AppendParams {
   uint8_t* v_data;
   uint8_t* k_sf;
   uint8_t* v_sf;
-  int64_t num_rows;   // num_tokens * 2 * num_kv_heads
+  int64_t num_tokens;
   int64_t num_slots;  // num_pages * page_size
-  int32_t num_kv_heads, page_size;
+  int32_t num_kv_heads, log2_page_size;
   int32_t* status;
 };
 
@@ -39,68 +41,55 @@ __device__ __forceinline__ bool scale_ok(float g) { return isfinite(g) && g > 0.
 
 template <int D>
 __global__ void __launch_bounds__(kAppendThreads) nvfp4_append_kernel(const AppendParams p) {
-  constexpr int kChunks = D / 8;                     // threads per row
-  constexpr int kRowsPerBlock = kAppendThreads / kChunks;
+  constexpr int kBlocks = D / 16;                    // threads per row
+  constexpr int kTokPerCta = kAppendThreads / kBlocks;
 
-  // Scale check, once per CTA before any store: a bad scale means no CTA writes.
+  // Scale check, once per CTA before any store: a bad scale means no CTA
+  // writes anything, for K and V alike.
   const float ks = p.k_scale_dev ? __ldg(p.k_scale_dev) : p.k_scale_host;
   const float vs = p.v_scale_dev ? __ldg(p.v_scale_dev) : p.v_scale_host;
   if (!scale_ok(ks) || !scale_ok(vs)) {
-    if (blockIdx.x == 0 && threadIdx.x == 0)
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
       atomicOr(p.status, (scale_ok(ks) ? 0 : FI_DEV_BAD_K_SCALE) |
                              (scale_ok(vs) ? 0 : FI_DEV_BAD_V_SCALE));
-    return;  // uniform across the CTA
+    return;  // uniform across the grid
   }
 
-  const int c = threadIdx.x % kChunks;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerBlock + threadIdx.x / kChunks;
   const int H = p.num_kv_heads;
-  bool active = row < p.num_rows;
-  int64_t tok = 0, slot = -1;
-  int t = 0, h = 0;
-  if (active) {
-    tok = row / (2 * H);
-    const int rem = static_cast<int>(row - tok * 2 * H);
-    t = rem / H;  // 0 = K, 1 = V
-    h = rem - t * H;
-    slot = __ldg(p.slot_mapping + tok);
-    if (slot < 0) {
-      active = false;
-    } else if (slot >= p.num_slots) {
-      if (t == 0 && h == 0 && c == 0) atomicOr(p.status, FI_DEV_SLOT_OOB);
-      active = false;
-    }
+  const int t = static_cast<int>(blockIdx.y) >= H ? 1 : 0;  // 0 = K, 1 = V
+  const int h = static_cast<int>(blockIdx.y) - t * H;
+  const int blk = threadIdx.x % kBlocks;
+  const int64_t tok = static_cast<int64_t>(blockIdx.x) * kTokPerCta + threadIdx.x / kBlocks;
+  if (tok >= p.num_tokens) return;
+  const int64_t slot = __ldg(p.slot_mapping + tok);
+  if (slot < 0) return;
+  if (slot >= p.num_slots) {
+    if (t == 0 && h == 0 && blk == 0) atomicOr(p.status, FI_DEV_SLOT_OOB);
+    return;
   }
-  float x[8];
-  float amax = 0.0f;
-  if (active) {
-    const __nv_bfloat16* src =
-        (t ? p.v + tok * p.v_tok_stride : p.k + tok * p.k_tok_stride) + h * D + c * 8;
-    const uint4 raw = __ldcs(reinterpret_cast<const uint4*>(src));
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      x[2 * j] = __uint_as_float(w[j] << 16);
-      x[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(x[j]));
-  } else {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) x[j] = 0.0f;
-  }
-  // lanes 2b and 2b+1 hold the two halves of 16-element block b
-  amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-  if (!active) return;
 
-  const Quant8 q = quantize8(x, amax, t ? vs : ks);
-  const int64_t page = slot / p.page_size;
-  const int64_t off = slot - page * p.page_size;
-  const int64_t cache_row = (page * H + h) * p.page_size + off;
+  const __nv_bfloat16* src =
+      (t ? p.v + tok * p.v_tok_stride : p.k + tok * p.k_tok_stride) + h * D + blk * 16;
+  const uint4 w0 = __ldcs(reinterpret_cast<const uint4*>(src));
+  const uint4 w1 = __ldcs(reinterpret_cast<const uint4*>(src) + 1);
+  float x[16];
+  bf16x8_to_f32(w0, x);
+  bf16x8_to_f32(w1, x + 8);
+  const Quant16 q = quantize16(x, t ? vs : ks);
+
+  const int64_t page = slot >> p.log2_page_size;
+  const int64_t off = slot & ((1 << p.log2_page_size) - 1);
+  const int64_t cache_row = ((page * H + h) << p.log2_page_size) + off;
   uint8_t* data = t ? p.v_data : p.k_data;
   uint8_t* sf = t ? p.v_sf : p.k_sf;
-  *reinterpret_cast<uint32_t*>(data + cache_row * (D / 2) + c * 4) = q.codes;
-  if ((c & 1) == 0) sf[cache_row * (D / 16) + c / 2] = static_cast<uint8_t>(q.s8);
+  *reinterpret_cast<uint2*>(data + cache_row * (D / 2) + blk * 8) = make_uint2(q.lo, q.hi);
+  sf[cache_row * kBlocks + blk] = static_cast<uint8_t>(q.s8);
+}
+
+int log2_exact(int v) {
+  int l = 0;
+  while ((1 << l) < v) ++l;
+  return l;
 }
 
 }  // namespace
@@ -121,18 +110,20 @@ fi_status launch_append(const AppendArgs& a, cudaStream_t stream) {
   p.k_sf = a.cache.k_sf;
   p.v_sf = a.cache.v_sf;
   p.num_kv_heads = a.cache.num_kv_heads;
-  p.page_size = a.cache.page_size;
-  p.num_rows = a.num_tokens * 2 * a.cache.num_kv_heads;
+  p.log2_page_size = log2_exact(a.cache.page_size);
+  p.num_tokens = a.num_tokens;
   p.num_slots = static_cast<int64_t>(a.cache.num_pages) * a.cache.page_size;
   p.status = a.status;
   const int D = a.cache.head_dim;
-  const int rows_per_block = kAppendThreads / (D / 8);
-  const int64_t blocks = (p.num_rows + rows_per_block - 1) / rows_per_block;
-  if (blocks > 0x7FFFFFFF) return FI_ERR_INVALID_ARGUMENT;
+  const int tok_per_cta = kAppendThreads / (D / 16);
+  const int64_t gx = (a.num_tokens + tok_per_cta - 1) / tok_per_cta;
+  const int64_t gy = 2 * static_cast<int64_t>(a.cache.num_kv_heads);
+  if (gx > 0x7FFFFFFF || gy > 65535) return FI_ERR_INVALID_ARGUMENT;
+  const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
   if (D == 128) {
-    nvfp4_append_kernel<128><<<static_cast<unsigned>(blocks), kAppendThreads, 0, stream>>>(p);
+    nvfp4_append_kernel<128><<<grid, kAppendThreads, 0, stream>>>(p);
   } else {
-    nvfp4_append_kernel<64><<<static_cast<unsigned>(blocks), kAppendThreads, 0, stream>>>(p);
+    nvfp4_append_kernel<64><<<grid, kAppendThreads, 0, stream>>>(p);
   }
   return cudaGetLastError() == cudaSuccess ? FI_OK : FI_ERR_CUDA;
 }

@@ -24,18 +24,52 @@ __global__ void quantize_blocks_kernel(const __nv_bfloat16* x, int64_t n, float 
                                        uint8_t* s8) {
   const int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (b >= n) return;
-  float lo[8], hi[8];
-  float amax = 0.0f;
-  for (int j = 0; j < 8; ++j) {
-    lo[j] = __bfloat162float(x[b * 16 + j]);
-    hi[j] = __bfloat162float(x[b * 16 + 8 + j]);
-    amax = fmaxf(amax, fmaxf(fabsf(lo[j]), fabsf(hi[j])));
+  float v[16];
+  for (int j = 0; j < 16; ++j) v[j] = __bfloat162float(x[b * 16 + j]);
+  const Quant16 q = quantize16(v, g);
+  reinterpret_cast<uint32_t*>(packed + b * 8)[0] = q.lo;
+  reinterpret_cast<uint32_t*>(packed + b * 8)[1] = q.hi;
+  s8[b] = static_cast<uint8_t>(q.s8);
+}
+
+// For every bf16 bit pattern x (blockIdx.x, threadIdx.x) and every divisor
+// d_values[blockIdx.y] that the quantizer would send through the Markstein
+// path (markstein_range_ok(d, |x|)), compares div_markstein_x2 (as the
+// quantizer calls it) with the IEEE quotient __fdiv_rn(x, d).
+// counts[0] += checked pairs; counts[1] += pairs whose E2M1 codes differ;
+// counts[2] += pairs with |x| >= 2^-100 and a normal IEEE quotient whose fp32
+// bits differ (the range where the residual is exact); counts[3] += pairs
+// with |x| < 2^-100 whose bits differ (allowed: the code is the same there).
+// first_bad gets the (x bits, d index) of one pair counted in [1] or [2].
+__global__ void div_check_kernel(const float* d_values, unsigned long long* counts,
+                                 uint32_t* first_bad) {
+  const uint32_t xb = blockIdx.x * blockDim.x + threadIdx.x;  // 0 .. 65535
+  const float x = __uint_as_float(xb << 16);
+  const float d = d_values[blockIdx.y];
+  unsigned long long c[4] = {0, 0, 0, 0};
+  if (isfinite(x) && markstein_range_ok(d, fabsf(x))) {
+    c[0] = 1;
+    const float r = __frcp_rn(d);
+    float a = x, a1 = x;
+    div_markstein_x2(a, a1, f2_pack(-d, -d), f2_pack(r, r));
+    const float b = __fdiv_rn(x, d);
+    const uint32_t ca = e2m1x4_from_f32(a, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f) & 0xFu;
+    const uint32_t cb = e2m1x4_from_f32(b, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f) & 0xFu;
+    const bool bits_differ = __float_as_uint(a) != __float_as_uint(b);
+    const bool exact_range = fabsf(x) >= 0x1p-100f && fabsf(b) >= 0x1p-126f;
+    if (ca != cb) c[1] = 1;
+    if (bits_differ && exact_range) c[2] = 1;
+    if (bits_differ && fabsf(x) < 0x1p-100f) c[3] = 1;
+    if (c[1] || c[2]) {
+      first_bad[0] = xb;
+      first_bad[1] = blockIdx.y;
+    }
   }
-  const Quant8 a = quantize8(lo, amax, g);
-  const Quant8 c = quantize8(hi, amax, g);
-  reinterpret_cast<uint32_t*>(packed + b * 8)[0] = a.codes;
-  reinterpret_cast<uint32_t*>(packed + b * 8)[1] = c.codes;
-  s8[b] = static_cast<uint8_t>(a.s8);
+  for (int k = 0; k < 4; ++k) {
+    unsigned long long v = c[k];
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    if ((threadIdx.x & 31) == 0 && v) atomicAdd(counts + k, v);
+  }
 }
 
 template <int D, bool IS_V>
@@ -199,6 +233,15 @@ int32_t fi_diag_quantize_blocks(const void* x, int64_t n_blocks, float g, uint8_
   const unsigned blocks = static_cast<unsigned>((n_blocks + 127) / 128);
   fi::quantize_blocks_kernel<<<blocks, 128, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const __nv_bfloat16*>(x), n_blocks, g, packed_out, s8_out);
+  return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}
+
+int32_t fi_diag_div_check(const float* d_values, int32_t n_d, unsigned long long* counts,
+                          uint32_t* first_bad, void* stream) {
+  if (!d_values || !counts || !first_bad || n_d <= 0 || n_d > 65535) return 1;
+  const dim3 grid(65536 / 256, static_cast<unsigned>(n_d));
+  fi::div_check_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(d_values, counts,
+                                                                           first_bad);
   return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }
 

@@ -17,31 +17,93 @@ __device__ __forceinline__ float e4m3_value(uint32_t code) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
 }
 
-struct Quant8 {
-  uint32_t codes;  // 8 E2M1 codes, element 2c in the low nibble of byte c
-  uint32_t s8;     // the block's E4M3 scale byte
+struct Quant16 {
+  uint32_t lo, hi;  // 16 E2M1 codes, element 2c in the low nibble of byte c
+  uint32_t s8;      // the block's E4M3 scale byte
 };
 
-// Quantizes 8 of the 16 elements of one NVFP4 block.  `amax` is the maximum
-// magnitude over all 16 elements of the block, `g` the global decode scale.
-// Each step is one fp32 IEEE operation (explicit _rn intrinsics: no fused
-// multiply-add, IEEE division):
-//   t = amax / (6 g), s8 = e4m3(t); d = e4m3(s8) g; code_j = e2m1(x_j / d);
-// a block with amax == 0 or with s8 == 0 stores s8 = 0 and all-zero codes.
-__device__ __forceinline__ Quant8 quantize8(const float (&x)[8], float amax, float g) {
-  Quant8 q{0u, 0u};
+// Division by the block's decode scale d, correctly rounded, without an IEEE
+// divide per element.  Markstein's theorem (P. W. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990): if r is 1/d rounded to nearest and q0 = RN(x r) (within
+// one ulp of x/d), the residual e = x - q0 d is exact when computed with one
+// fused multiply-add, and RN(q0 + e r) is x/d rounded to nearest.  The
+// hypotheses (no overflow, no underflow of q0 or e) hold for every element of
+// a block when d is in [2^-98, 2^100] and amax <= 2^100 d: an element with
+// |x| >= 2^-100 has an exact residual, and one with |x| < 2^-100 has
+// |x/d| < 1/4, where every value within a few ulps encodes to the same E2M1
+// code (0, or 8 for negative inputs).  The sign is restored for zero inputs
+// (-0 stays -0, as an IEEE division gives).  Callers outside that range use
+// the IEEE division itself.
+__device__ __forceinline__ bool markstein_range_ok(float d, float amax) {
+  return d >= 0x1p-98f && d <= 0x1p100f && amax <= d * 0x1p100f;
+}
+
+__device__ __forceinline__ float div_markstein(float x, float d, float r) {
+  const float q0 = __fmul_rn(x, r);
+  const float e = __fmaf_rn(-q0, d, x);
+  const float q1 = __fmaf_rn(e, r, q0);
+  return copysignf(q1, x);
+}
+
+// The same for a pair of elements with paired fp32 arithmetic (each lane one
+// IEEE operation, as above; fma(q0, -d, x) rounds x - q0 d exactly like
+// fma(-q0, d, x)).
+__device__ __forceinline__ void div_markstein_x2(float& x0, float& x1, uint64_t d2n,
+                                                 uint64_t r2) {
+  const uint64_t x2 = f2_pack(x0, x1);
+  const uint64_t q0 = f2_mul(x2, r2);
+  const uint64_t e = f2_fma(q0, d2n, x2);
+  float y0, y1;
+  f2_unpack(f2_fma(e, r2, q0), y0, y1);
+  x0 = copysignf(y0, x0);
+  x1 = copysignf(y1, x1);
+}
+
+// Quantizes one 16-element NVFP4 block with global decode scale g:
+//   amax = max |x_j|, t = amax / RN(6 g), s8 = e4m3(t), d = RN(e4m3(s8) g),
+//   code_j = e2m1(RN(x_j / d));
+// every step rounds like one IEEE fp32 operation (no contraction).  A block
+// with amax == 0, or whose s8 encodes 0, stores s8 = 0 and all-zero codes.
+__device__ __forceinline__ Quant16 quantize16(const float (&x)[16], float g) {
+  Quant16 q{0u, 0u, 0u};
+  // elements 0..14 in seven three-input steps, then element 15
+  float amax = fabsf(x[0]);
+#pragma unroll
+  for (int j = 1; j < 15; j += 2) amax = fmax3(amax, fabsf(x[j]), fabsf(x[j + 1]));
+  amax = fmaxf(amax, fabsf(x[15]));
   if (amax == 0.0f) return q;
   const float t = __fdiv_rn(amax, __fmul_rn(6.0f, g));
   const uint32_t s = e4m3_from_f32(t);
   const float sv = e4m3_value(s);
   if (sv == 0.0f) return q;
   const float d = __fmul_rn(sv, g);
-  float y[8];
+  float y[16];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) y[j] = __fdiv_rn(x[j], d);
-  q.codes = e2m1x4_from_f32(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
+  for (int j = 0; j < 16; ++j) y[j] = x[j];
+  if (markstein_range_ok(d, amax)) {
+    const float r = __frcp_rn(d);
+    const uint64_t r2 = f2_pack(r, r), d2n = f2_pack(-d, -d);
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) div_markstein_x2(y[j], y[j + 1], d2n, r2);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) y[j] = __fdiv_rn(x[j], d);
+  }
+  q.lo = e2m1x4_from_f32(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
+  q.hi = e2m1x4_from_f32(y[8], y[9], y[10], y[11], y[12], y[13], y[14], y[15]);
   q.s8 = s;
   return q;
+}
+
+// 8 bf16 values (one 128-bit word) -> fp32.
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 w, float* x) {
+  const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    x[2 * j] = __uint_as_float(v[j] << 16);
+    x[2 * j + 1] = __uint_as_float(v[j] & 0xFFFF0000u);
+  }
 }
 
 // --- 16-bit staging tile ------------------------------------------------------

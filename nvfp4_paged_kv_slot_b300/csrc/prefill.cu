@@ -15,13 +15,16 @@
 //                 TS with P in tensor memory) and tcgen05.commit
 //   warps 2-3     idle
 //   WG 1..NQ      softmax, one warpgroup per Q tile, one thread per query row:
-//                 online softmax in fp32 (base 2), P written back to tensor
-//                 memory over S, lazy O rescale, epilogue
+//                 the row of S in registers (one tensor-memory read), online
+//                 softmax in fp32 (base 2, paired fp32 arithmetic, exp2 split
+//                 between the MUFU unit and an FMA-pipe polynomial), P written
+//                 back to tensor memory over S as fp16, lazy O rescale, epilogue
 //   last WG       repack: raw FP4 tile -> exact 16-bit tile in the swizzled
 //                 layout the tensor cores read (K as bf16, V as fp16)
 // The NQ Q tiles of a CTA are NQ query heads of one GQA group at the same
 // positions, so every staged KV tile is repacked once and used NQ times.
-// Tensor memory: S_i at column 128 i, O_i after all S.  All waits are bounded.
+// Tensor memory: S_i at column 128 i, O_i after all S.  Registers are moved
+// to the softmax warpgroups with setmaxnreg.  All waits are bounded.
 #include <cmath>
 
 #include "internal.h"
@@ -35,6 +38,13 @@ constexpr int kRawStages = 4;
 constexpr int kStgStages = 3;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 constexpr uint64_t kDrainNs = 100000000ull;     // 0.1 s per wait while aborting
+// The running max is moved (and O rescaled) only when it grows by more than
+// 2^kLazyRescale, so P stays below 2^kLazyRescale (exact range for fp16 P).
+constexpr float kLazyRescale = 8.0f;
+// Outside the diagonal tiles, element pairs k with (k & kPolyMask) ==
+// kPolyMask take exp2 on the FMA pipe, the others on the MUFU unit (one pair
+// in four): the MUFU rate alone would match the tensor cores' time per tile.
+constexpr int kPolyMask = 3;
 
 struct PrefillParams {
   CUtensorMap tmap_q;  // 3-D view of q: (head_dim, num_qo_heads, total_qo)
@@ -55,7 +65,7 @@ struct PrefillParams {
   int32_t batch, num_qo_heads, num_kv_heads, num_pages, page_size;
   int32_t group, units_per_kv_head, head_units;
   int32_t uniform, global_reverse, uni_qo_len, uni_kv_len, q_tiles;
-  int64_t num_units;
+  int32_t num_units;
   float sm_scale;
 };
 
@@ -78,6 +88,12 @@ struct Layout {
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
   static constexpr int kTmemCols = (NQ * 128 + NQ * D) <= 256 ? 256 : 512;
   static constexpr int kThreads = 128 * (NQ + 2);
+  // Per-thread register counts after the warpgroup reallocation: the repack
+  // warpgroup gives registers up, each softmax warpgroup takes more, the
+  // load/MMA warpgroup keeps the launch's count.  The launcher checks that
+  // the sum fits in what the CTA is launched with.
+  static constexpr int kRegRepack = 64;
+  static constexpr int kRegSoftmax = NQ == 2 ? 160 : 232;
   static_assert(kOffStg % 1024 == 0 && kStg % 1024 == 0, "swizzled tiles need 1 KB alignment");
   static_assert(kRaw % 16 == 0 && kOffRaw % 16 == 0, "bulk copies need 16 B alignment");
 };
@@ -88,20 +104,20 @@ struct Unit {
 
 // tile id -> (sequence, head unit, q-tile): arithmetic for uniform batches
 // (#3575 §1, §2), the planner's list otherwise.
-__device__ __forceinline__ Unit decode_unit(const PrefillParams& p, int64_t u, int nq) {
+__device__ __forceinline__ Unit decode_unit(const PrefillParams& p, int u, int nq) {
   Unit w;
   int hu;
   if (p.uniform) {
-    const int64_t BH = static_cast<int64_t>(p.batch) * p.head_units;
+    const int BH = p.batch * p.head_units;
     if (p.global_reverse) {
-      w.qt = p.q_tiles - 1 - static_cast<int>(u / BH);
-      const int64_t r = u % BH;
-      hu = static_cast<int>(r / p.batch);
-      w.b = static_cast<int>(r % p.batch);
+      w.qt = p.q_tiles - 1 - u / BH;
+      const int r = u % BH;
+      hu = r / p.batch;
+      w.b = r % p.batch;
     } else {
-      const int64_t per_b = static_cast<int64_t>(p.head_units) * p.q_tiles;
-      w.b = static_cast<int>(u / per_b);
-      const int r = static_cast<int>(u % per_b);
+      const int per_b = p.head_units * p.q_tiles;
+      w.b = u / per_b;
+      const int r = u % per_b;
       hu = r / p.q_tiles;
       w.qt = p.q_tiles - 1 - r % p.q_tiles;
     }
@@ -128,6 +144,31 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// 2^x for a pair of fp32 arguments x <= 2^7, on the FMA and integer pipes
+// instead of the MUFU unit: x = n + f with n = round(x), read from the low
+// mantissa bits of x + 1.5 * 2^23, and f = x - n in [-1/2, 1/2]; 2^f by a
+// degree-3 polynomial fitted to the relative error on [-1/2, 1/2]
+// (coefficients derived by csrc/exp2_poly_fit.py; max relative error 7.5e-5,
+// below the 2^-11 rounding of the fp16 P it feeds); 2^n by adding n to the
+// exponent field.  Arguments are clamped at -120 (2^-120 is zero in fp16 P).
+__device__ __forceinline__ uint64_t exp2_fma_x2(uint64_t x2) {
+  float x0, x1;
+  f2_unpack(x2, x0, x1);
+  const uint64_t xc = f2_pack(fmaxf(x0, -120.0f), fmaxf(x1, -120.0f));
+  const uint64_t magic = f2_pack(12582912.0f, 12582912.0f);
+  const uint64_t t = f2_add(xc, magic);
+  const uint64_t f = f2_sub(xc, f2_sub(t, magic));
+  uint64_t q = f2_fma(f2_pack(0.055171623826026917f, 0.055171623826026917f), f,
+                      f2_pack(0.2426111251115799f, 0.2426111251115799f));
+  q = f2_fma(q, f, f2_pack(0.6932609677314758f, 0.6932609677314758f));
+  q = f2_fma(q, f, f2_pack(0.9999280571937561f, 0.9999280571937561f));
+  float q0, q1, t0, t1;
+  f2_unpack(q, q0, q1);
+  f2_unpack(t, t0, t1);
+  return f2_pack(__uint_as_float(__float_as_uint(q0) + (__float_as_uint(t0) << 23)),
+                 __uint_as_float(__float_as_uint(q1) + (__float_as_uint(t1) << 23)));
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
@@ -197,6 +238,7 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   const AbortState ab{abort_flag, p.status, kTimeoutNs, FI_DEV_WAIT_TIMEOUT};
 
+  const int wg = threadIdx.x / 128;
   if (warp == 0) {
     // ------------------------------------------------------------- load warp
     if (lane == 0) prefetch_tensormap(&p.tmap_q);
@@ -207,7 +249,7 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
     const uint32_t pg_data = static_cast<uint32_t>(p.page_size) * (D / 2);
     const uint32_t pg_sf = static_cast<uint32_t>(p.page_size) * (D / 16);
     const int pages_per_tile = kTileKV / p.page_size;
-    for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
+    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
       const Unit w = decode_unit(p, u, NQ);
       if (!mbar_wait(q_empty, (it & 1) ^ 1, ab)) {
         ok = false;
@@ -274,27 +316,32 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
       for (int i = 0; i < NQ; ++i) pk[i] = 0;
       int it = 0;
       bool ok = true;
+      // Descriptors are built once; a start address inside the region is
+      // reached by adding (byte offset >> 4) to the low 14-bit address field
+      // (shared-memory offsets stay below 2^18 bytes, so nothing carries out).
+      const uint64_t q_desc0 = smem_desc_sw128(q_addr, 16, 1024);
+      const uint64_t k_desc0 = smem_desc_sw128(stg_addr, 16, 1024);
+      const uint64_t v_desc0 = smem_desc_sw128(stg_addr, 16384, 1024);
       auto issue_qk = [&](int i, uint32_t ss) {
         const uint32_t d_tmem = tmem_base + i * 128;
-        const uint32_t qa = q_addr + i * L::kQTile;
-        const uint32_t kb = stg_addr + ss * L::kStg;
+        const uint64_t qd = q_desc0 + ((i * L::kQTile) >> 4);
+        const uint64_t kd = k_desc0 + ((ss * L::kStg) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(d_tmem, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
-                 kIdescQK, kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          mma_ss(d_tmem, qd + off, kd + off, kIdescQK, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int i, uint32_t ss, bool acc) {
         const uint32_t d_tmem = tmem_base + NQ * 128 + i * D;
         const uint32_t a_tmem = tmem_base + i * 128;
-        const uint32_t vb = stg_addr + ss * L::kStg;
+        const uint64_t vd = v_desc0 + ((ss * L::kStg) >> 4);
 #pragma unroll
         for (int s = 0; s < kTileKV / 16; ++s)
-          mma_ts(d_tmem, a_tmem + s * 8, smem_desc_sw128(vb + s * 2048, 16384, 1024), kIdescPV,
+          mma_ts(d_tmem, a_tmem + s * 8, vd + ((s * 2048) >> 4), kIdescPV,
                  (acc || s > 0) ? 1u : 0u);
       };
-      for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
+      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
         const Unit w = decode_unit(p, u, NQ);
         if (!mbar_wait(q_full, it & 1, ab)) { ok = false; break; }
         // K tile 0
@@ -344,10 +391,13 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
       const AbortState drain_ab{&drain_flag, nullptr, ok ? kTimeoutNs : kDrainNs, 0};
       mbar_wait(drain, 0, drain_ab);
     }
-  } else if (warp >= 4 && warp < 4 * (NQ + 1)) {
+  } else if (wg == 0) {
+    // warps 2-3: no role
+  } else if (wg <= NQ) {
     // ------------------------------------------------------------- softmax
-    const int i = warp / 4 - 1;
-    const int r = threadIdx.x - 128 * (i + 1);  // query row within the tile
+    setmaxnreg_inc<L::kRegSoftmax>();
+    const int i = wg - 1;
+    const int r = threadIdx.x - 128 * wg;  // query row within the tile
     const uint32_t lane_base = tmem_base + ((static_cast<uint32_t>(r / 32) * 32) << 16);
     const uint32_t s_col = lane_base + i * 128;
     const uint32_t o_col = lane_base + NQ * 128 + i * D;
@@ -360,69 +410,119 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
       if (bad) atomicOr(p.status, bad);
     }
     const float scale_log2 = p.sm_scale * ks * 1.4426950408889634f;
+    const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
     uint32_t sk = 0;
     int it = 0;
     bool ok = true;
-    for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
+    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
       const Unit w = decode_unit(p, u, NQ);
       const int row_q = w.qt * kTileQ + r;
       const int delta = w.kv_len - w.qo_len;
       const int limit = row_q + delta;                 // last key this row sees
       const int tile_first_limit = w.qt * kTileQ + delta;
-      float m_ref = -INFINITY;
-      float l = 0.0f;
+      float m_ref = -INFINITY;                         // running max (log2 units)
+      float l = 0.0f;                                  // running sum of p
       for (int j = 0; j < w.n_kv; ++j) {
         if (!mbar_wait(s_full + i, sk & 1, ab)) { ok = false; break; }
         ++sk;
         tc_fence_after();
         const int key0 = j * kTileKV;
+        // keys beyond this row's causal limit exist only in tiles that reach
+        // past the first row's limit (the diagonal tiles)
         const bool masked = key0 + kTileKV - 1 > tile_first_limit;
-        float mx = -INFINITY;
+        float mx;
+        {
+          uint32_t sv[128];
+          tmem_ld128(s_col, sv);
+          if (masked) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(s_col + c * 32, v);
-#pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const float s = __uint_as_float(v[k]);
-            if (!masked || key0 + c * 32 + k <= limit) mx = fmaxf(mx, s);
+            for (int k = 0; k < 128; ++k)
+              if (key0 + k > limit) sv[k] = 0xFF800000u;  // -inf
           }
+          // four independent chains over columns 32c .. 32c+31: element 32c,
+          // fifteen three-input steps over 32c+1 .. 32c+30, then 32c+31
+          float mc[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            mc[c] = __uint_as_float(sv[32 * c]);
+#pragma unroll
+            for (int k = 1; k < 31; k += 2)
+              mc[c] = fmax3(mc[c], __uint_as_float(sv[32 * c + k]),
+                            __uint_as_float(sv[32 * c + k + 1]));
+            mc[c] = fmaxf(mc[c], __uint_as_float(sv[32 * c + 31]));
+          }
+          mx = fmaxf(fmax3(mc[0], mc[1], mc[2]), mc[3]);
         }
         const float m_new = fmaxf(m_ref, mx * scale_log2);
-        if (m_new > m_ref + 8.0f) {
-          // lazy rescale: only when the running max grows by more than 2^8
-          const float alpha = ex2(m_ref - m_new);
+        // lazy rescale: the running max moves only when it grows by more than
+        // 2^kLazyRescale (P stays below that power of two otherwise); O is
+        // rescaled below, after P is stored.
+        float alpha = 1.0f;
+        if (m_new > m_ref + kLazyRescale) {
+          alpha = ex2(m_ref - m_new);
           l *= alpha;
-          if (j > 0) {
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t o[32];
-              tmem_ld32(o_col + c * 32, o);
-#pragma unroll
-              for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-              tmem_st32(o_col + c * 32, o);
-            }
-          }
           m_ref = m_new;
         }
-        float rs = 0.0f;
+        const uint64_t negm2 = f2_pack(-m_ref, -m_ref);
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+        // Exponentials in two halves of 64 columns, S read again from tensor
+        // memory: P (fp16 pairs) of columns 64h..64h+63 goes to columns
+        // 32h..32h+31, over S values already read, and is built in place in
+        // the registers of the consumed S pairs.
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(s_col + c * 32, v);
-          uint32_t pp[16];
+        for (int h = 0; h < 2; ++h) {
+          uint32_t sv[64];
+          tmem_ld64(s_col + 64 * h, sv);
+          if (masked) {
 #pragma unroll
-          for (int k = 0; k < 32; k += 2) {
-            const bool vis0 = !masked || key0 + c * 32 + k <= limit;
-            const bool vis1 = !masked || key0 + c * 32 + k + 1 <= limit;
-            const float p0 = vis0 ? ex2(fmaf(__uint_as_float(v[k]), scale_log2, -m_ref)) : 0.0f;
-            const float p1 = vis1 ? ex2(fmaf(__uint_as_float(v[k + 1]), scale_log2, -m_ref)) : 0.0f;
-            rs += p0 + p1;
-            pp[k / 2] = pack_f16x2(p0, p1);
+            for (int k = 0; k < 32; ++k) {
+              const int c = key0 + 64 * h + 2 * k;
+              const float s0 = c <= limit ? __uint_as_float(sv[2 * k]) : -INFINITY;
+              const float s1 = c + 1 <= limit ? __uint_as_float(sv[2 * k + 1]) : -INFINITY;
+              float x0, x1;
+              f2_unpack(f2_fma(f2_pack(s0, s1), scale2, negm2), x0, x1);
+              const float p0 = ex2(x0), p1 = ex2(x1);
+              acc[k & 3] = f2_add(acc[k & 3], f2_pack(p0, p1));
+              sv[k] = pack_f16x2(p0, p1);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const uint64_t x2 =
+                  f2_fma(f2_pack(__uint_as_float(sv[2 * k]), __uint_as_float(sv[2 * k + 1])),
+                         scale2, negm2);
+              uint64_t p2;
+              if ((k & kPolyMask) == kPolyMask) {
+                p2 = exp2_fma_x2(x2);
+              } else {
+                float x0, x1;
+                f2_unpack(x2, x0, x1);
+                p2 = f2_pack(ex2(x0), ex2(x1));
+              }
+              acc[k & 3] = f2_add(acc[k & 3], p2);
+              float p0, p1;
+              f2_unpack(p2, p0, p1);
+              sv[k] = pack_f16x2(p0, p1);
+            }
           }
-          tmem_st16(s_col + c * 16, pp);
+          tmem_st32(s_col + 32 * h, *reinterpret_cast<uint32_t(*)[32]>(sv));
         }
-        l += rs;
+        acc[0] = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+        float a0, a1;
+        f2_unpack(acc[0], a0, a1);
+        l += a0 + a1;
+        if (alpha != 1.0f && j > 0) {
+          // O holds the PV products of tiles < j, all complete: the commit
+          // behind this tile's s_full follows them.
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(o_col + c * 32, o);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+            tmem_st32(o_col + c * 32, o);
+          }
+        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(p_full + i);
@@ -457,12 +557,13 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
       // the next unit's first PV may overwrite O_i only after these loads
       tc_fence_before();
     }
-  } else if (warp >= 4 * (NQ + 1)) {
+  } else {
     // ------------------------------------------------------------- repack
+    setmaxnreg_dec<L::kRegRepack>();
     const int rt = threadIdx.x - 128 * (NQ + 1);
     uint32_t raw_k = 0, stg_k = 0;
     bool ok = true;
-    for (int64_t u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
       const Unit w = decode_unit(p, u, NQ);
       for (int j = 0; ok && j < w.n_kv; ++j) {
         const int valid = min(kTileKV, w.kv_len - j * kTileKV);
@@ -500,6 +601,12 @@ fi_status launch_impl(const PrefillParams& p, int grid, cudaStream_t stream) {
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
     return FI_ERR_CUDA;
+  // The warpgroup register reallocation must fit in what the launch gives the
+  // CTA, or a warpgroup's increase would never be granted.
+  cudaFuncAttributes attr;
+  if (cudaFuncGetAttributes(&attr, kern) != cudaSuccess) return FI_ERR_CUDA;
+  if (128 * (attr.numRegs + L::kRegRepack + NQ * L::kRegSoftmax) > attr.numRegs * L::kThreads)
+    return FI_ERR_UNSUPPORTED;
   kern<<<grid, L::kThreads, smem, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? FI_OK : FI_ERR_CUDA;
 }
@@ -543,7 +650,8 @@ fi_status launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.uni_qo_len = P.uniform_qo_len;
   p.uni_kv_len = P.uniform_kv_len;
   p.q_tiles = P.info.q_tiles;
-  p.num_units = P.info.num_units;
+  if (P.info.num_units > 0x7FFFFFFF) return FI_ERR_UNSUPPORTED;
+  p.num_units = static_cast<int32_t>(P.info.num_units);
   p.sm_scale = P.sm_scale;
   const int grid = P.info.num_ctas;
   const int nq = P.info.heads_per_cta;

@@ -14,12 +14,13 @@ if not LIB_PATH.exists():
     raise ImportError(f"{LIB_PATH} is not built: run `python -m nvfp4_paged_kv_slot_b300.build`")
 lib = C.CDLL(str(LIB_PATH))
 
-EXPORTED = ("fi_diag_codec_span", "fi_diag_quantize_blocks", "fi_diag_repack_tile",
-            "fi_diag_umma")
+EXPORTED = ("fi_diag_codec_span", "fi_diag_quantize_blocks", "fi_diag_div_check",
+            "fi_diag_repack_tile", "fi_diag_umma")
 
 _vp = C.c_void_p
 lib.fi_diag_codec_span.argtypes = [C.c_uint32, C.c_uint64, _vp, _vp, _vp]
 lib.fi_diag_quantize_blocks.argtypes = [_vp, C.c_int64, C.c_float, _vp, _vp, _vp]
+lib.fi_diag_div_check.argtypes = [_vp, C.c_int32, _vp, _vp, _vp]
 lib.fi_diag_repack_tile.argtypes = [_vp, C.c_int32, C.c_int32, C.c_int32, _vp, _vp]
 lib.fi_diag_umma.argtypes = [C.c_int32, _vp, _vp, _vp, _vp, _vp]
 for _n in EXPORTED:
@@ -45,6 +46,11 @@ def quantize_blocks(x, g: float, packed_out, s8_out):
     _ok(lib.fi_diag_quantize_blocks(x.data_ptr(), x.numel() // 16, float(g),
                                     packed_out.data_ptr(), s8_out.data_ptr(), _s()),
         "fi_diag_quantize_blocks")
+
+
+def div_check(d_values, counts, first_bad):
+    _ok(lib.fi_diag_div_check(d_values.data_ptr(), d_values.numel(), counts.data_ptr(),
+                              first_bad.data_ptr(), _s()), "fi_diag_div_check")
 
 
 def repack_tile(raw, head_dim: int, is_v: bool, valid: int, out):

@@ -87,6 +87,41 @@ def test_block_quantizer_bit_exact_vs_oracle(diag, oracle, g):
         assert gs[i] == rs and np.array_equal(gp[i], rp), (i, x[i], g)
 
 
+def test_markstein_division_matches_ieee_division(diag, oracle):
+    """The append divides each element by its block's decode scale d with one
+    rounded reciprocal and a fused-multiply-add correction (Markstein).  Over
+    every bf16 input and divisors d = RN(e4m3(s8) * g) for all positive E4M3
+    scales and many global scales g, plus log-uniform and edge divisors, the
+    quotient must give the IEEE quotient's E2M1 code wherever the quantizer
+    uses that path, and its exact bits wherever Markstein's theorem applies
+    (|x| >= 2^-100, normal quotient)."""
+    e4 = np.array([oracle.e4m3_value(c) for c in range(1, 127)], np.float32)
+    rng = np.random.default_rng(11)
+    gs = np.concatenate([[1.0, 0.0021, 3.7e-5, 1 / 2688.0, 1e-20, 7.5e30, 2.0 ** -60],
+                         np.exp2(rng.uniform(-80, 80, 40))]).astype(np.float32)
+    ds = (e4[None, :] * gs[:, None]).astype(np.float32).reshape(-1)   # RN(sv * g) in fp32
+    extra = np.exp2(rng.uniform(-98, 100, 4000)).astype(np.float32)
+    edges = np.array([2.0 ** -98, 2.0 ** 100, np.nextafter(np.float32(2.0 ** -98), np.float32(1)),
+                      np.nextafter(np.float32(2.0 ** 100), np.float32(0)), 1.0, 3.0, 448.0],
+                     np.float32)
+    d = np.concatenate([ds, extra, edges]).astype(np.float32)
+    dv = torch.from_numpy(d).cuda()
+    counts = torch.zeros(4, dtype=torch.int64, device="cuda")
+    first = torch.zeros(2, dtype=torch.int32, device="cuda")
+    diag.div_check(dv, counts, first)
+    checked, bad_code, bad_bits, small_bits = counts.cpu().tolist()
+    print(f"checked {checked}; bit differences with |x| < 2^-100 (same code): {small_bits}")
+    # expected number of (x, d) pairs on the Markstein path, counted on the host
+    xs = (np.arange(65536, dtype=np.uint32) << 16).view(np.float32)
+    ax = np.sort(np.abs(xs[np.isfinite(xs)]))
+    with np.errstate(over="ignore"):
+        lim = (d * np.float32(2.0 ** 100)).astype(np.float32)
+    ok = (d >= np.float32(2.0 ** -98)) & (d <= np.float32(2.0 ** 100))
+    want = int(np.searchsorted(ax, lim[ok], side="right").sum())
+    assert checked == want, (checked, want)
+    assert bad_code == 0 and bad_bits == 0, (bad_code, bad_bits, first.cpu().tolist())
+
+
 @pytest.mark.parametrize("head_dim", [64, 128])
 @pytest.mark.parametrize("is_v", [False, True])
 @pytest.mark.parametrize("valid", [128, 77])
