@@ -56,6 +56,7 @@ typedef int32_t fi_status;
 #define FI_ERR_UNSUPPORTED 3      /* head_dim / page_size / device not supported */
 #define FI_ERR_CUDA 4             /* a CUDA runtime call failed             */
 #define FI_ERR_OUT_OF_MEMORY 5    /* plan or context allocation failed      */
+#define FI_ERR_SCRATCH_TOO_SMALL 6 /* batch too large for fi_prefill_noalloc's fixed scratch */
 
 /* Bits of the device status word (fi_device_status). */
 #define FI_DEV_BAD_K_SCALE 1   /* device k_scale not positive finite: nothing written */
@@ -196,6 +197,33 @@ fi_status fi_prefill_plan_host(const int32_t* qo_indptr_host, const int32_t* kv_
                                int32_t head_dim, int32_t page_size, int64_t l2_bytes,
                                const fi_plan_options* opts, fi_plan_info* info,
                                int32_t* work_out, int64_t work_capacity);
+
+/* Plans and runs the causal prefill in one call without allocating memory
+ * (no cudaMalloc, no host heap), for callers that cannot allocate while they
+ * run — a serving engine that reserves all device memory for its KV cache up
+ * front, or a plugin whose enqueue callback must not allocate.  The pages have
+ * no counterpart of this entry point.
+ *   Arguments as in fi_prefill_plan and fi_prefill_run (no context, no plan).
+ *   status_dev: caller-owned device int32 that receives FI_DEV_* bits with
+ *       atomicOr (not cleared by the call), or NULL to discard them.
+ * Scratch: the indptr copies and, for ragged batches, the work-unit list are
+ * kept in one fixed device array of 2 MiB (524288 int32 words) inside the
+ * library, held by every GPU that loads it until the process exits.  A call
+ * needs 4 + 2 (batch + 1) words, plus 4 per work unit for ragged batches
+ * (units = sum over sequences of ceil(qo_len / 128) times the head units);
+ * larger calls return FI_ERR_SCRATCH_TOO_SMALL and enqueue nothing.  Every
+ * call shares the array: calls that overlap on the GPU (on different streams)
+ * race.  The host arrays are copied with cudaMemcpyAsync from pageable memory,
+ * which waits for the stream's earlier work, so calls on one stream are
+ * ordered.  The first call on a device looks up the array's device address;
+ * make that first call before any stream capture.  Ragged work units are taken
+ * in sequence order with the heaviest q-tile of each sequence first. */
+fi_status fi_prefill_noalloc(const int32_t* qo_indptr_host, const int32_t* kv_indptr_host,
+                             int32_t batch, const int32_t* page_table_dev,
+                             int32_t page_table_stride, int32_t num_qo_heads,
+                             int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                             float sm_scale, const void* q_dev, const fi_nvfp4_cache* cache,
+                             void* out_dev, float* lse_dev, int32_t* status_dev, void* stream);
 
 /* Reads the context's device status word after synchronizing `stream`; if
  * `reset` is non-zero the word is cleared afterwards.  The only call that

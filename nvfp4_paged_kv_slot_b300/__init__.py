@@ -27,6 +27,7 @@ FI_ERR_BAD_SCALE = 2
 FI_ERR_UNSUPPORTED = 3
 FI_ERR_CUDA = 4
 FI_ERR_OUT_OF_MEMORY = 5
+FI_ERR_SCRATCH_TOO_SMALL = 6
 
 FI_DEV_BAD_K_SCALE = 1
 FI_DEV_BAD_V_SCALE = 2
@@ -37,7 +38,7 @@ FI_DEV_WAIT_TIMEOUT = 16
 EXPORTED = ("fi_context_create", "fi_context_destroy", "fi_nvfp4_append",
             "fi_nvfp4_append_host_scale", "fi_plan_create", "fi_plan_destroy",
             "fi_prefill_plan", "fi_plan_get_info", "fi_prefill_run", "fi_prefill_plan_host",
-            "fi_device_status", "fi_status_string", "fi_version")
+            "fi_device_status", "fi_status_string", "fi_version", "fi_prefill_noalloc")
 
 
 class fi_nvfp4_cache(C.Structure):
@@ -80,6 +81,8 @@ _sigs = {
     "fi_prefill_plan_host": [_vp, _vp, _i32, _i32, _i32, _i32, _i32, _i64,
                              C.POINTER(fi_plan_options), C.POINTER(fi_plan_info), _vp, _i64],
     "fi_device_status": [_vp, _vp, C.POINTER(_i32), _i32],
+    "fi_prefill_noalloc": [_vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _vp,
+                           C.POINTER(fi_nvfp4_cache), _vp, _vp, _vp, _vp],
     "fi_status_string": [_i32],
     "fi_version": [],
 }

@@ -320,6 +320,8 @@ const char* fi_status_string(fi_status status) {
     case FI_ERR_UNSUPPORTED: return "unsupported head_dim, page_size or device";
     case FI_ERR_CUDA: return "CUDA runtime error";
     case FI_ERR_OUT_OF_MEMORY: return "out of memory";
+    case FI_ERR_SCRATCH_TOO_SMALL:
+      return "batch too large for the no-allocation prefill's fixed scratch";
     default: return "unknown status";
   }
 }
