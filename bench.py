@@ -212,6 +212,13 @@ def max_over_ranks(x, dist_on, device):
     return float(t.item())
 
 
+def aggregate_value(flops_per_rank, step_ms_max, world):
+    """Whole-job throughput in TFLOP/s: every rank runs its own copy of the
+    workload (weak scaling), so the FLOPs of all ranks over the slowest
+    rank's step time."""
+    return world * flops_per_rank / (step_ms_max * 1e-3) / 1e12
+
+
 def time_device_steps(runner, stream, steps, warmup, dist_on, device):
     for _ in range(warmup):
         runner.step(stream)
@@ -463,7 +470,7 @@ def main():
     if st != 0:
         raise RuntimeError(f"device status {st} after the timed steps")
     step_ms = max_over_ranks(total_ms / args.steps, dist_on, device)
-    value = world * runner.flops / (step_ms * 1e-3) / 1e12
+    value = aggregate_value(runner.flops, step_ms, world)
     pf_ms = statistics.mean(prefill_ms)
     ap_ms = statistics.mean(append_ms)
     pf_tflops = runner.flops / (pf_ms * 1e-3) / 1e12
@@ -474,7 +481,7 @@ def main():
     if not args.no_e2e:
         e2e_s, h2d, d2h = time_e2e(runner, stream, args.e2e_steps, 1)
         e2e_s = max_over_ranks(e2e_s, dist_on, device)
-        e2e = {"value": world * runner.flops / e2e_s / 1e12, "unit": UNIT,
+        e2e = {"value": aggregate_value(runner.flops, e2e_s * 1e3, world), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": args.e2e_steps, "ms_per_step": e2e_s * 1e3}
 
