@@ -41,10 +41,14 @@ constexpr uint64_t kDrainNs = 100000000ull;     // 0.1 s per wait while aborting
 // The running max is moved (and O rescaled) only when it grows by more than
 // 2^kLazyRescale, so P stays below 2^kLazyRescale (exact range for fp16 P).
 constexpr float kLazyRescale = 8.0f;
-// Outside the diagonal tiles, element pairs k with (k & kPolyMask) ==
-// kPolyMask take exp2 on the FMA pipe, the others on the MUFU unit (one pair
-// in four): the MUFU rate alone would match the tensor cores' time per tile.
-constexpr int kPolyMask = 3;
+// Outside the diagonal tiles, element pairs k (0..31 per half row) with
+// (k & kPolyMask) == kPolyMask take exp2 on the FMA pipe, the others on the
+// MUFU unit.  On B300 the MUFU unit keeps up (measured: every pair on MUFU is
+// 4% faster than one pair in four on the FMA pipe), so the mask selects none.
+constexpr int kPolyMask = 64;
+// Threads of the repack role: the last warpgroup.  (Adding warps 2-3 was
+// measured slower: they share the schedulers of two softmax warps.)
+constexpr int kRepackThreads = 128;
 
 struct PrefillParams {
   CUtensorMap tmap_q;  // 3-D view of q: (head_dim, num_qo_heads, total_qo)
@@ -81,8 +85,9 @@ struct Layout {
   static constexpr int kOffRaw = kOffStg + kStgStages * kStg;
   static constexpr int kOffBar = kOffRaw + kRawStages * kRaw;
   // q_full, q_empty, raw_full[], raw_empty[], stg_full[], stg_empty[],
-  // s_full[NQ], p_full[NQ], o_full[NQ], drain
-  static constexpr int kNumBars = 2 + 2 * kRawStages + 2 * kStgStages + 3 * NQ + 1;
+  // s_full[NQ], p_full[2 NQ] (P columns of keys 0-63 / 64-127 of head i at
+  // 2i / 2i+1), o_full[NQ], drain
+  static constexpr int kNumBars = 2 + 2 * kRawStages + 2 * kStgStages + 4 * NQ + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
@@ -200,7 +205,7 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
   uint64_t* stg_empty = stg_full + kStgStages;
   uint64_t* s_full = stg_empty + kStgStages;
   uint64_t* p_full = s_full + NQ;
-  uint64_t* o_full = p_full + NQ;
+  uint64_t* o_full = p_full + 2 * NQ;
   uint64_t* drain = o_full + NQ;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + L::kOffMisc + 4);
@@ -213,15 +218,16 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
     mbar_init(q_empty, 1);
     for (int s = 0; s < kRawStages; ++s) {
       mbar_init(raw_full + s, 1);
-      mbar_init(raw_empty + s, 128);
+      mbar_init(raw_empty + s, kRepackThreads);
     }
     for (int s = 0; s < kStgStages; ++s) {
-      mbar_init(stg_full + s, 128);
+      mbar_init(stg_full + s, kRepackThreads);
       mbar_init(stg_empty + s, 1);
     }
     for (int i = 0; i < NQ; ++i) {
       mbar_init(s_full + i, 1);
-      mbar_init(p_full + i, 128);
+      mbar_init(p_full + 2 * i, 128);
+      mbar_init(p_full + 2 * i + 1, 128);
       mbar_init(o_full + i, 1);
     }
     mbar_init(drain, 1);
@@ -239,6 +245,33 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
   const AbortState ab{abort_flag, p.status, kTimeoutNs, FI_DEV_WAIT_TIMEOUT};
 
   const int wg = threadIdx.x / 128;
+  // Repack: raw FP4 tiles -> 16-bit staging tiles, by kRepackThreads threads
+  // (rt = 0 .. kRepackThreads-1).
+  auto repack_role = [&](int rt) {
+    uint32_t raw_k = 0, stg_k = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
+      const Unit w = decode_unit(p, u, NQ);
+      for (int j = 0; ok && j < w.n_kv; ++j) {
+        const int valid = min(kTileKV, w.kv_len - j * kTileKV);
+        for (int t = 0; t < 2; ++t, ++raw_k, ++stg_k) {
+          const int rs = raw_k % kRawStages;
+          const int ss = stg_k % kStgStages;
+          if (!mbar_wait(raw_full + rs, (raw_k / kRawStages) & 1, ab)) { ok = false; break; }
+          if (!mbar_wait(stg_empty + ss, ((stg_k / kStgStages) & 1) ^ 1, ab)) { ok = false; break; }
+          if (t)
+            repack_tile<D, true>(raw_smem + rs * L::kRaw, stg_smem + ss * L::kStg, valid, rt,
+                                 kRepackThreads);
+          else
+            repack_tile<D, false>(raw_smem + rs * L::kRaw, stg_smem + ss * L::kStg, valid, rt,
+                                  kRepackThreads);
+          fence_proxy_async_smem();
+          mbar_arrive(stg_full + ss);
+          mbar_arrive(raw_empty + rs);
+        }
+      }
+    }
+  };
   if (warp == 0) {
     // ------------------------------------------------------------- load warp
     if (lane == 0) prefetch_tensormap(&p.tmap_q);
@@ -332,12 +365,13 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
           mma_ss(d_tmem, qd + off, kd + off, kIdescQK, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int i, uint32_t ss, bool acc) {
+      // PV over keys 64h .. 64h+63 (P columns 32h .. 32h+31)
+      auto issue_pv_half = [&](int i, uint32_t ss, int h, bool acc) {
         const uint32_t d_tmem = tmem_base + NQ * 128 + i * D;
         const uint32_t a_tmem = tmem_base + i * 128;
         const uint64_t vd = v_desc0 + ((ss * L::kStg) >> 4);
 #pragma unroll
-        for (int s = 0; s < kTileKV / 16; ++s)
+        for (int s = 4 * h; s < 4 * h + 4; ++s)
           mma_ts(d_tmem, a_tmem + s * 8, vd + ((s * 2048) >> 4), kIdescPV,
                  (acc || s > 0) ? 1u : 0u);
       };
@@ -361,10 +395,15 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
           ++stg_k;
           const bool more = j + 1 < w.n_kv;
           for (int i = 0; i < NQ; ++i) {
-            if (!mbar_wait(p_full + i, pk[i] & 1, ab)) { ok = false; break; }
+            // the first half of P may be multiplied while the softmax still
+            // computes the second
+            if (!mbar_wait(p_full + 2 * i, pk[i] & 1, ab)) { ok = false; break; }
+            tc_fence_after();
+            issue_pv_half(i, ss_v, 0, j > 0);
+            if (!mbar_wait(p_full + 2 * i + 1, pk[i] & 1, ab)) { ok = false; break; }
             ++pk[i];
             tc_fence_after();
-            issue_pv(i, ss_v, j > 0);
+            issue_pv_half(i, ss_v, 1, true);
             if (i == NQ - 1) mma_commit(stg_empty + ss_v);
             if (more) {
               if (i == 0) {
@@ -430,15 +469,15 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
         // keys beyond this row's causal limit exist only in tiles that reach
         // past the first row's limit (the diagonal tiles)
         const bool masked = key0 + kTileKV - 1 > tile_first_limit;
+        uint32_t sv[128];
+        tmem_ld128(s_col, sv);
+        if (masked) {
+#pragma unroll
+          for (int k = 0; k < 128; ++k)
+            if (key0 + k > limit) sv[k] = 0xFF800000u;  // -inf
+        }
         float mx;
         {
-          uint32_t sv[128];
-          tmem_ld128(s_col, sv);
-          if (masked) {
-#pragma unroll
-            for (int k = 0; k < 128; ++k)
-              if (key0 + k > limit) sv[k] = 0xFF800000u;  // -inf
-          }
           // four independent chains over columns 32c .. 32c+31: element 32c,
           // fifteen three-input steps over 32c+1 .. 32c+30, then 32c+31
           float mc[4];
@@ -455,77 +494,72 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
         }
         const float m_new = fmaxf(m_ref, mx * scale_log2);
         // lazy rescale: the running max moves only when it grows by more than
-        // 2^kLazyRescale (P stays below that power of two otherwise); O is
-        // rescaled below, after P is stored.
-        float alpha = 1.0f;
+        // 2^kLazyRescale (P stays below that power of two otherwise).  O holds
+        // the PV products of tiles < j, all complete (the commit behind this
+        // tile's s_full follows them); it is rescaled before any P of this
+        // tile is released.
         if (m_new > m_ref + kLazyRescale) {
-          alpha = ex2(m_ref - m_new);
+          const float alpha = ex2(m_ref - m_new);
           l *= alpha;
           m_ref = m_new;
+          if (j > 0) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld32(o_col + c * 32, o);
+#pragma unroll
+              for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+              tmem_st32(o_col + c * 32, o);
+            }
+          }
         }
         const uint64_t negm2 = f2_pack(-m_ref, -m_ref);
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-        // Exponentials in two halves of 64 columns, S read again from tensor
-        // memory: P (fp16 pairs) of columns 64h..64h+63 goes to columns
-        // 32h..32h+31, over S values already read, and is built in place in
-        // the registers of the consumed S pairs.
+        // Exponentials in two halves of 64 columns.  Half 0 uses the S values
+        // still in registers; half 1 reads its columns again (its registers are
+        // given up after the maximum).  P (fp16 pairs) of columns 64h..64h+63
+        // goes to columns 32h..32h+31, over S values already read, and each
+        // half is released to the MMA as soon as it is stored.
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          uint32_t sv[64];
-          tmem_ld64(s_col + 64 * h, sv);
-          if (masked) {
+          uint32_t* sh = sv;
+          uint32_t sv1[64];
+          if (h == 1) {
+            tmem_ld64(s_col + 64, sv1);
+            if (masked) {
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-              const int c = key0 + 64 * h + 2 * k;
-              const float s0 = c <= limit ? __uint_as_float(sv[2 * k]) : -INFINITY;
-              const float s1 = c + 1 <= limit ? __uint_as_float(sv[2 * k + 1]) : -INFINITY;
-              float x0, x1;
-              f2_unpack(f2_fma(f2_pack(s0, s1), scale2, negm2), x0, x1);
-              const float p0 = ex2(x0), p1 = ex2(x1);
-              acc[k & 3] = f2_add(acc[k & 3], f2_pack(p0, p1));
-              sv[k] = pack_f16x2(p0, p1);
+              for (int k = 0; k < 64; ++k)
+                if (key0 + 64 + k > limit) sv1[k] = 0xFF800000u;
             }
-          } else {
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-              const uint64_t x2 =
-                  f2_fma(f2_pack(__uint_as_float(sv[2 * k]), __uint_as_float(sv[2 * k + 1])),
-                         scale2, negm2);
-              uint64_t p2;
-              if ((k & kPolyMask) == kPolyMask) {
-                p2 = exp2_fma_x2(x2);
-              } else {
-                float x0, x1;
-                f2_unpack(x2, x0, x1);
-                p2 = f2_pack(ex2(x0), ex2(x1));
-              }
-              acc[k & 3] = f2_add(acc[k & 3], p2);
-              float p0, p1;
-              f2_unpack(p2, p0, p1);
-              sv[k] = pack_f16x2(p0, p1);
-            }
+            sh = sv1;
           }
-          tmem_st32(s_col + 32 * h, *reinterpret_cast<uint32_t(*)[32]>(sv));
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const uint64_t x2 =
+                f2_fma(f2_pack(__uint_as_float(sh[2 * k]), __uint_as_float(sh[2 * k + 1])),
+                       scale2, negm2);
+            uint64_t p2;
+            if (!masked && (k & kPolyMask) == kPolyMask) {
+              p2 = exp2_fma_x2(x2);
+            } else {
+              float x0, x1;
+              f2_unpack(x2, x0, x1);
+              p2 = f2_pack(ex2(x0), ex2(x1));
+            }
+            acc[k & 3] = f2_add(acc[k & 3], p2);
+            float p0, p1;
+            f2_unpack(p2, p0, p1);
+            sh[k] = pack_f16x2(p0, p1);
+          }
+          tmem_st32(s_col + 32 * h, *reinterpret_cast<uint32_t(*)[32]>(sh));
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(p_full + 2 * i + h);
         }
         acc[0] = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
         float a0, a1;
         f2_unpack(acc[0], a0, a1);
         l += a0 + a1;
-        if (alpha != 1.0f && j > 0) {
-          // O holds the PV products of tiles < j, all complete: the commit
-          // behind this tile's s_full follows them.
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(o_col + c * 32, o);
-#pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-            tmem_st32(o_col + c * 32, o);
-          }
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(p_full + i);
       }
       if (!ok) break;
       if (!mbar_wait(o_full + i, it & 1, ab)) { ok = false; break; }
@@ -560,28 +594,7 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
   } else {
     // ------------------------------------------------------------- repack
     setmaxnreg_dec<L::kRegRepack>();
-    const int rt = threadIdx.x - 128 * (NQ + 1);
-    uint32_t raw_k = 0, stg_k = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-      const Unit w = decode_unit(p, u, NQ);
-      for (int j = 0; ok && j < w.n_kv; ++j) {
-        const int valid = min(kTileKV, w.kv_len - j * kTileKV);
-        for (int t = 0; t < 2; ++t, ++raw_k, ++stg_k) {
-          const int rs = raw_k % kRawStages;
-          const int ss = stg_k % kStgStages;
-          if (!mbar_wait(raw_full + rs, (raw_k / kRawStages) & 1, ab)) { ok = false; break; }
-          if (!mbar_wait(stg_empty + ss, ((stg_k / kStgStages) & 1) ^ 1, ab)) { ok = false; break; }
-          if (t)
-            repack_tile<D, true>(raw_smem + rs * L::kRaw, stg_smem + ss * L::kStg, valid, rt, 128);
-          else
-            repack_tile<D, false>(raw_smem + rs * L::kRaw, stg_smem + ss * L::kStg, valid, rt, 128);
-          fence_proxy_async_smem();
-          mbar_arrive(stg_full + ss);
-          mbar_arrive(raw_empty + rs);
-        }
-      }
-    }
+    repack_role(threadIdx.x - 128 * (NQ + 1));
   }
 
   __syncwarp();

@@ -45,14 +45,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
       : "memory");
 }
 
+// One bounded poll: returns once the phase with `parity` has completed or
+// after at most about kSuspendHintNs (the hardware may return sooner).
+constexpr uint32_t kSuspendHintNs = 20000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -69,19 +73,18 @@ struct AbortState {
 
 // Waits for the phase of `bar` with the given parity.  Returns false if the
 // CTA is aborting or the wait ran out of time (then the abort flag is set).
+// Every poll is bounded (suspend hint) and followed by a check of the clock
+// and of the abort flag, so a wait gives up within about timeout_ns.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const AbortState& ab) {
   if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = global_timer_ns();
-  uint32_t spins = 0;
+  const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((++spins & 255u) == 0) {
-      if (*ab.flag) return false;
-      if (global_timer_ns() - t0 > ab.timeout_ns) {
-        *ab.flag = 1;
-        if (ab.status) atomicOr(ab.status, ab.timeout_bit);
-        return false;
-      }
+    if (*ab.flag) return false;
+    if (global_timer_ns() - t0 > ab.timeout_ns) {
+      *ab.flag = 1;
+      if (ab.status) atomicOr(ab.status, ab.timeout_bit);
+      return false;
     }
   }
 }

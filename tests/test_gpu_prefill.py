@@ -127,3 +127,39 @@ def test_full_size_sampled(name):
     res = compare_attention(out, lse, ref_out, ref_lse, rows=rows)
     print(name, info, res)
     assert_within_tolerance(res)
+
+
+def test_plan_append_run_return_while_the_stream_is_busy():
+    """No hidden host synchronization ([#5043]-style planning, [#6204] append):
+    with the stream held by a bounded sleep kernel, a steady-state plan (its
+    staging buffers already allocated), an append and a run all return
+    before the sleep has finished."""
+    import time
+    m = fi()
+    d = device_inputs("ragged_small")
+    sp = d["spec"]
+    ctx = m.fi_context_create()
+    c = gpu_cache(d)
+    plan = m.fi_plan_create(ctx)
+    args = (d["host"]["qo_indptr"], d["host"]["kv_indptr"], d["page_table"], sp.num_qo_heads,
+            sp.num_kv_heads, sp.head_dim, sp.page_size)
+    out = torch.empty_like(d["q"])
+    for _ in range(2):                      # allocate both staging buffers
+        m.fi_prefill_plan(plan, *args)
+        m.fi_nvfp4_append(ctx, d["k"], d["v"], c.k_scale, c.v_scale, d["slot_mapping"], c)
+        m.fi_prefill_run(plan, d["q"], c, out)
+    torch.cuda.synchronize()
+    done = torch.cuda.Event()
+    torch.cuda._sleep(400_000_000)          # ~0.2 s at 2 GHz, bounded
+    t0 = time.perf_counter()
+    m.fi_prefill_plan(plan, *args)
+    m.fi_nvfp4_append(ctx, d["k"], d["v"], c.k_scale, c.v_scale, d["slot_mapping"], c)
+    m.fi_prefill_run(plan, d["q"], c, out)
+    dt = time.perf_counter() - t0
+    done.record()
+    busy = not done.query()
+    torch.cuda.synchronize()
+    assert busy and dt < 0.05, (busy, dt)
+    assert m.fi_device_status(ctx) == 0
+    m.fi_plan_destroy(plan)
+    m.fi_context_destroy(ctx)
