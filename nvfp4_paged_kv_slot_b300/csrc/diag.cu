@@ -82,7 +82,7 @@ __global__ void repack_probe_kernel(const uint8_t* raw, int valid, uint16_t* out
   constexpr int kRaw = 128 * (D / 2 + D / 16);
   for (int i = threadIdx.x; i < kRaw; i += blockDim.x) rs[i] = raw[i];
   __syncthreads();
-  repack_tile<D, IS_V>(rs, st, valid, threadIdx.x, blockDim.x);
+  repack_tile<D, IS_V, 128>(rs, st, valid, threadIdx.x);
   __syncthreads();
   for (int i = threadIdx.x; i < 128 * (D / 8); i += blockDim.x) {
     const int row = i / (D / 8), c = i % (D / 8);

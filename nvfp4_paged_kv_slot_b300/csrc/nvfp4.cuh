@@ -153,26 +153,55 @@ __device__ __forceinline__ uint4 dequant8_f16(uint32_t w, uint32_t s8) {
 // Repacks one raw NVFP4 KV tile (128 token rows of D/2 code bytes, then 128
 // rows of D/16 scale bytes, as copied from the cache pages) into the 16-bit
 // staging tile: K as bf16 (operand of QK^T), V as fp16 (operand of PV).  Rows
-// at or beyond `valid` are written as zeros.  Thread `tid` of `nthreads`
-// converts 8 elements per step: consecutive threads read consecutive 32-bit
+// at or beyond `valid` are written as zeros.  Thread `tid` of NT (NT a
+// multiple of D/8 and of 64) converts 8 elements per task: task t is row
+// t / (D/8), chunk t % (D/8); consecutive threads read consecutive 32-bit
 // words and write distinct 16-byte chunk positions of one row, so neither the
-// loads nor the swizzled stores conflict on shared-memory banks.
-template <int D, bool IS_V>
-__device__ __forceinline__ void repack_tile(const uint8_t* raw, uint8_t* dst, int valid, int tid,
-                                            int nthreads) {
+// loads nor the swizzled stores conflict on shared-memory banks.  A thread's
+// tasks keep its chunk and the row's phase in the swizzle, so its addresses
+// advance by constant strides.  Full tiles take a branch-free path in batches
+// of four tasks, the batch's loads issued before its conversions (the
+// conversions of different tasks are independent, which keeps the warp busy
+// within a small register budget).
+template <int D, bool IS_V, int NT>
+__device__ __forceinline__ void repack_tile(const uint8_t* raw, uint8_t* dst, int valid,
+                                            int tid) {
+  static_assert(NT % (D / 8) == 0 && NT % 64 == 0, "constant-stride tasks");
+  constexpr int kPer = 128 * (D / 8) / NT;       // tasks per thread
+  constexpr int kRowStep = NT / (D / 8);         // rows between a thread's tasks
   const uint32_t* words = reinterpret_cast<const uint32_t*>(raw);
   const uint8_t* sf = raw + 128 * (D / 2);
-#pragma unroll 4
-  for (int task = tid; task < 128 * (D / 8); task += nthreads) {
-    const int row = task / (D / 8);
-    const int c = task % (D / 8);
-    uint4 o = make_uint4(0u, 0u, 0u, 0u);
-    if (row < valid) {
-      const uint32_t w = words[task];
-      const uint32_t s8 = sf[row * (D / 16) + c / 2];
-      o = IS_V ? dequant8_f16(w, s8) : dequant8_bf16(w, s8);
+  const int c = tid % (D / 8);
+  const int row0 = tid / (D / 8);
+  const uint32_t off0 = sw128_offset(row0, c);
+  if (valid >= 128) {
+    // batches of kBatch tasks: the batch's loads, then its conversions
+    constexpr int kBatch = kPer < 4 ? kPer : 4;
+#pragma unroll 1
+    for (int k0 = 0; k0 < kPer; k0 += kBatch) {
+      uint32_t w[kBatch], s8[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        w[k] = words[tid + (k0 + k) * NT];
+        s8[k] = sf[(row0 + (k0 + k) * kRowStep) * (D / 16) + c / 2];
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const uint4 o = IS_V ? dequant8_f16(w[k], s8[k]) : dequant8_bf16(w[k], s8[k]);
+        *reinterpret_cast<uint4*>(dst + off0 + (k0 + k) * kRowStep * 128) = o;
+      }
     }
-    *reinterpret_cast<uint4*>(dst + sw128_offset(row, c)) = o;
+  } else {
+#pragma unroll 4
+    for (int k = 0; k < kPer; ++k) {
+      const int row = row0 + k * kRowStep;
+      uint4 o = make_uint4(0u, 0u, 0u, 0u);
+      if (row < valid) {
+        const uint32_t s8 = sf[row * (D / 16) + c / 2];
+        o = IS_V ? dequant8_f16(words[tid + k * NT], s8) : dequant8_bf16(words[tid + k * NT], s8);
+      }
+      *reinterpret_cast<uint4*>(dst + off0 + k * kRowStep * 128) = o;
+    }
   }
 }
 

@@ -94,9 +94,9 @@ struct Layout {
   static constexpr int kTmemCols = (NQ * 128 + NQ * D) <= 256 ? 256 : 512;
   static constexpr int kThreads = 128 * (NQ + 2);
   // Per-thread register counts after the warpgroup reallocation: the repack
-  // warpgroup gives registers up, each softmax warpgroup takes more, the
-  // load/MMA warpgroup keeps the launch's count.  The launcher checks that
-  // the sum fits in what the CTA is launched with.
+  // warpgroup gives registers up, each softmax warpgroup takes more (a whole
+  // row of S), the load/MMA warpgroup keeps the launch's count.  The
+  // launcher checks that the sum fits in what the CTA is launched with.
   static constexpr int kRegRepack = 64;
   static constexpr int kRegSoftmax = NQ == 2 ? 160 : 232;
   static_assert(kOffStg % 1024 == 0 && kStg % 1024 == 0, "swizzled tiles need 1 KB alignment");
@@ -260,11 +260,11 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
           if (!mbar_wait(raw_full + rs, (raw_k / kRawStages) & 1, ab)) { ok = false; break; }
           if (!mbar_wait(stg_empty + ss, ((stg_k / kStgStages) & 1) ^ 1, ab)) { ok = false; break; }
           if (t)
-            repack_tile<D, true>(raw_smem + rs * L::kRaw, stg_smem + ss * L::kStg, valid, rt,
-                                 kRepackThreads);
+            repack_tile<D, true, kRepackThreads>(raw_smem + rs * L::kRaw,
+                                                 stg_smem + ss * L::kStg, valid, rt);
           else
-            repack_tile<D, false>(raw_smem + rs * L::kRaw, stg_smem + ss * L::kStg, valid, rt,
-                                  kRepackThreads);
+            repack_tile<D, false, kRepackThreads>(raw_smem + rs * L::kRaw,
+                                                  stg_smem + ss * L::kStg, valid, rt);
           fence_proxy_async_smem();
           mbar_arrive(stg_full + ss);
           mbar_arrive(raw_empty + rs);
@@ -469,6 +469,9 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
         // keys beyond this row's causal limit exist only in tiles that reach
         // past the first row's limit (the diagonal tiles)
         const bool masked = key0 + kTileKV - 1 > tile_first_limit;
+        // The whole row of S in registers: one tensor-memory read per tile
+        // (each read costs hundreds of cycles, so their number matters more
+        // than the registers).
         uint32_t sv[128];
         tmem_ld128(s_col, sv);
         if (masked) {
@@ -496,47 +499,35 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
         // lazy rescale: the running max moves only when it grows by more than
         // 2^kLazyRescale (P stays below that power of two otherwise).  O holds
         // the PV products of tiles < j, all complete (the commit behind this
-        // tile's s_full follows them); it is rescaled before any P of this
-        // tile is released.
+        // tile's s_full follows them); it is rescaled, 16 columns at a time,
+        // before any P of this tile is released.
         if (m_new > m_ref + kLazyRescale) {
           const float alpha = ex2(m_ref - m_new);
           l *= alpha;
           m_ref = m_new;
           if (j > 0) {
+#pragma unroll 1
+            for (int c = 0; c < D / 16; ++c) {
+              uint32_t o[16];
+              tmem_ld16(o_col + c * 16, o);
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t o[32];
-              tmem_ld32(o_col + c * 32, o);
-#pragma unroll
-              for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-              tmem_st32(o_col + c * 32, o);
+              for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+              tmem_st16(o_col + c * 16, o);
             }
           }
         }
         const uint64_t negm2 = f2_pack(-m_ref, -m_ref);
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-        // Exponentials in two halves of 64 columns.  Half 0 uses the S values
-        // still in registers; half 1 reads its columns again (its registers are
-        // given up after the maximum).  P (fp16 pairs) of columns 64h..64h+63
-        // goes to columns 32h..32h+31, over S values already read, and each
-        // half is released to the MMA as soon as it is stored.
+        // P (fp16 pairs) over the consumed S registers, pair k in sv[k];
+        // columns 64h..64h+63 of S give P columns 32h..32h+31.  Half 0 is
+        // stored, half 1 computed while that store completes, then half 0
+        // is released to the MMA, then half 1 stored and released.
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          uint32_t* sh = sv;
-          uint32_t sv1[64];
-          if (h == 1) {
-            tmem_ld64(s_col + 64, sv1);
-            if (masked) {
 #pragma unroll
-              for (int k = 0; k < 64; ++k)
-                if (key0 + 64 + k > limit) sv1[k] = 0xFF800000u;
-            }
-            sh = sv1;
-          }
-#pragma unroll
-          for (int k = 0; k < 32; ++k) {
+          for (int k = 32 * h; k < 32 * h + 32; ++k) {
             const uint64_t x2 =
-                f2_fma(f2_pack(__uint_as_float(sh[2 * k]), __uint_as_float(sh[2 * k + 1])),
+                f2_fma(f2_pack(__uint_as_float(sv[2 * k]), __uint_as_float(sv[2 * k + 1])),
                        scale2, negm2);
             uint64_t p2;
             if (!masked && (k & kPolyMask) == kPolyMask) {
@@ -549,12 +540,19 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
             acc[k & 3] = f2_add(acc[k & 3], p2);
             float p0, p1;
             f2_unpack(p2, p0, p1);
-            sh[k] = pack_f16x2(p0, p1);
+            sv[k] = pack_f16x2(p0, p1);
           }
-          tmem_st32(s_col + 32 * h, *reinterpret_cast<uint32_t(*)[32]>(sh));
-          tmem_st_wait();
-          tc_fence_before();
-          mbar_arrive(p_full + 2 * i + h);
+          if (h == 0) {
+            tmem_st32(s_col, *reinterpret_cast<uint32_t(*)[32]>(sv));
+          } else {
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(p_full + 2 * i);
+            tmem_st32(s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(p_full + 2 * i + 1);
+          }
         }
         acc[0] = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
         float a0, a1;

@@ -18,7 +18,8 @@ def _need_gpu():
         pytest.skip("no CUDA device")
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged_small", "ragged_small_d64", "uniform_small"])
+@pytest.mark.parametrize("name", ["tiny", "ragged_small", "ragged_small_d64", "uniform_small",
+                                  "gqa3_small", "mha_small_d64"])
 @pytest.mark.parametrize("schedule", [0, 1, 2])
 def test_prefill_matches_oracle(name, schedule):
     d = device_inputs(name)

@@ -12,7 +12,8 @@ Workloads (shapes follow the pages' workloads; data is synthetic):
   uniform     1024 x 1024 tokens, H_q=32, H_kv=8, D=128, ps=16, random page table
   ragged      256 sequences, L = round(exp(U[ln 128, ln 16384])), qo_len = kv_len,
               H_q=32, H_kv=8, D=128, ps=16, random page table
-plus small ragged cases used by the parity tests.
+plus small ragged cases used by the parity tests (several tiles and ragged tails,
+head_dim 64 and 128, page sizes 16 to 64, GQA groups of 1 to 4).
 
 K, V, Q ~ N(0, 1) in fp32, rounded to bf16.  The global decode scales are
 k_scale = amax|K| / (6 * 448) and likewise v_scale (fp32, host).  The seed of
@@ -83,6 +84,13 @@ def spec(name: str) -> Spec:
     if name == "ragged_small_d64":
         return Spec("ragged_small_d64", 6000, num_kv_heads=2, head_dim=64, page_size=32,
                     num_qo_heads=4, seq_lens=[5, 130, 257, 64])
+    # Odd GQA groups (one query head per CTA): group of 3, and plain multi-head.
+    if name == "gqa3_small":
+        return Spec("gqa3_small", 8000, num_kv_heads=2, head_dim=128, page_size=16,
+                    num_qo_heads=6, seq_lens=[100, 300, 129])
+    if name == "mha_small_d64":
+        return Spec("mha_small_d64", 9000, num_kv_heads=2, head_dim=64, page_size=64,
+                    num_qo_heads=2, seq_lens=[70, 200])
     if name == "uniform_small":
         return Spec("uniform_small", 7000, num_kv_heads=2, head_dim=128, page_size=16,
                     num_qo_heads=8, seq_lens=[384] * 6)
