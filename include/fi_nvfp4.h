@@ -126,6 +126,8 @@ typedef struct {
                        2: per-(sequence, head) reverse order */
   int32_t num_ctas; /* persistent CTAs; 0 = number of SMs */
   int64_t l2_bytes; /* L2 size for the gate; 0 = the device's */
+  int32_t cta_pairs; /* 0: GQA groups of a multiple of 4 query heads run on 2-CTA
+                        clusters that share their KV staging tiles; 1: never */
 } fi_plan_options;
 
 /* What the planner decided (host values). */
@@ -138,11 +140,12 @@ typedef struct {
   int32_t is_uniform;     /* every qo_len equal and every kv_len equal */
   int32_t global_reverse; /* heaviest q-tiles of all sequences and heads first */
   int32_t q_tiles;        /* ceil(max_qo_len / 128) */
-  int32_t heads_per_cta;  /* q heads of one GQA group sharing each staged KV tile */
-  int32_t head_units;     /* num_kv_heads * group / heads_per_cta */
+  int32_t heads_per_cta;  /* q heads per CTA sharing each staged KV tile */
+  int32_t head_units;     /* num_kv_heads * group / (heads_per_cta * ctas_per_unit) */
   int64_t num_units;      /* work units (sequence, head unit, q-tile) */
   int64_t kv_bytes;       /* NVFP4 bytes of K and V the batch reads */
-  int32_t num_ctas;
+  int32_t num_ctas;       /* CTAs the run launches (at most; pairs may be fewer) */
+  int32_t ctas_per_unit;  /* 2 when units run on CTA pairs, else 1 */
 } fi_plan_info;
 
 /* Creates an empty, reusable plan bound to `ctx`. */

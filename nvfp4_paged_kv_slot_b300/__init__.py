@@ -49,7 +49,8 @@ class fi_nvfp4_cache(C.Structure):
 
 
 class fi_plan_options(C.Structure):
-    _fields_ = [("schedule", C.c_int32), ("num_ctas", C.c_int32), ("l2_bytes", C.c_int64)]
+    _fields_ = [("schedule", C.c_int32), ("num_ctas", C.c_int32), ("l2_bytes", C.c_int64),
+                ("cta_pairs", C.c_int32)]
 
 
 class fi_plan_info(C.Structure):
@@ -58,7 +59,7 @@ class fi_plan_info(C.Structure):
                 ("is_uniform", C.c_int32), ("global_reverse", C.c_int32),
                 ("q_tiles", C.c_int32), ("heads_per_cta", C.c_int32),
                 ("head_units", C.c_int32), ("num_units", C.c_int64), ("kv_bytes", C.c_int64),
-                ("num_ctas", C.c_int32)]
+                ("num_ctas", C.c_int32), ("ctas_per_unit", C.c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -225,14 +226,14 @@ def fi_plan_destroy(plan):
 
 def fi_prefill_plan(plan, qo_indptr, kv_indptr, page_table, num_qo_heads, num_kv_heads,
                     head_dim, page_size, sm_scale=0.0, schedule=0, num_ctas=0, l2_bytes=0,
-                    stream=None):
+                    cta_pairs=0, stream=None):
     """qo_indptr, kv_indptr: host int32 [B+1] (other integer types are
     converted); page_table: device int32 [B][stride]."""
     qo = _host_i32(qo_indptr)
     kv = _host_i32(kv_indptr)
     if qo.size != kv.size or qo.size < 1:
         raise ValueError("qo_indptr and kv_indptr must both have batch+1 entries")
-    opts = fi_plan_options(schedule, num_ctas, l2_bytes)
+    opts = fi_plan_options(schedule, num_ctas, l2_bytes, cta_pairs)
     _check(lib.fi_prefill_plan(plan, qo.ctypes.data, kv.ctypes.data, qo.size - 1,
                                _ptr(page_table), page_table.stride(0) if page_table is not None
                                else 0, num_qo_heads, num_kv_heads, head_dim, page_size,
@@ -258,11 +259,12 @@ def fi_prefill_run(plan, q, cache: NVFP4Cache, out, lse=None, stream=None):
 
 
 def fi_prefill_plan_host(qo_indptr, kv_indptr, num_qo_heads, num_kv_heads, head_dim, page_size,
-                         l2_bytes=126 * 2**20, schedule=0, num_ctas=0, with_list=True):
+                         l2_bytes=126 * 2**20, schedule=0, num_ctas=0, with_list=True,
+                         cta_pairs=0):
     """Host-only planning (no CUDA): returns (info dict, work [units][4] int32)."""
     qo = _host_i32(qo_indptr)
     kv = _host_i32(kv_indptr)
-    opts = fi_plan_options(schedule, num_ctas, l2_bytes)
+    opts = fi_plan_options(schedule, num_ctas, l2_bytes, cta_pairs)
     info = fi_plan_info()
     _check(lib.fi_prefill_plan_host(qo.ctypes.data, kv.ctypes.data, qo.size - 1, num_qo_heads,
                                     num_kv_heads, head_dim, page_size, l2_bytes, C.byref(opts),

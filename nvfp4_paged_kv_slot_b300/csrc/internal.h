@@ -44,6 +44,7 @@ struct HostPlan {
   int32_t group = 0;              // num_qo_heads / num_kv_heads
   int32_t units_per_kv_head = 0;  // group / heads_per_cta
   int32_t uniform_qo_len = 0, uniform_kv_len = 0;
+  bool pair = false;              // units run on 2-CTA clusters sharing KV staging
   float sm_scale = 0.0f;
   std::vector<int32_t> work;      // 4 int32 per unit (ragged batches only)
 };

@@ -205,4 +205,43 @@ __device__ __forceinline__ void repack_tile(const uint8_t* raw, uint8_t* dst, in
   }
 }
 
+// Repacks half a tile, for a pair of CTAs that share their staging tiles:
+// `raw` holds 64 token rows (D/2 code bytes each, then 64 rows of D/16 scale
+// bytes); they become rows row_base .. row_base+63 of the staging tile, both
+// in this CTA's shared memory (`dst`) and in the other CTA's (`peer_dst`, the
+// same tile's shared::cluster address there).  Rows at or beyond `valid` (of
+// the 64) are written as zeros.  Same task layout and store order as
+// repack_tile; row_base is a multiple of 8, so the swizzle phase is unchanged.
+template <int D, bool IS_V, int NT>
+__device__ __forceinline__ void repack_half(const uint8_t* raw, uint8_t* dst, uint32_t peer_dst,
+                                            int row_base, int valid, int tid) {
+  static_assert(NT % (D / 8) == 0 && NT % 64 == 0, "constant-stride tasks");
+  constexpr int kPer = 64 * (D / 8) / NT;        // tasks per thread
+  constexpr int kRowStep = NT / (D / 8);
+  constexpr int kBatch = kPer < 4 ? kPer : 4;
+  const uint32_t* words = reinterpret_cast<const uint32_t*>(raw);
+  const uint8_t* sf = raw + 64 * (D / 2);
+  const int c = tid % (D / 8);
+  const int row0 = tid / (D / 8);
+  const uint32_t off0 = sw128_offset(row_base + row0, c);
+#pragma unroll 1
+  for (int k0 = 0; k0 < kPer; k0 += kBatch) {
+    uint32_t w[kBatch], s8[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      w[k] = words[tid + (k0 + k) * NT];
+      s8[k] = sf[(row0 + (k0 + k) * kRowStep) * (D / 16) + c / 2];
+    }
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      uint4 o = make_uint4(0u, 0u, 0u, 0u);
+      if (row0 + (k0 + k) * kRowStep < valid)
+        o = IS_V ? dequant8_f16(w[k], s8[k]) : dequant8_bf16(w[k], s8[k]);
+      const uint32_t off = off0 + (k0 + k) * kRowStep * 128;
+      *reinterpret_cast<uint4*>(dst + off) = o;
+      st_cluster_v4(peer_dst + off, o);
+    }
+  }
+}
+
 }  // namespace fi

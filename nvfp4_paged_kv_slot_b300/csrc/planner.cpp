@@ -43,6 +43,7 @@ fi_status plan_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t 
     return FI_ERR_UNSUPPORTED;
   const int32_t schedule = opts ? opts->schedule : 0;
   if (schedule < 0 || schedule > 2) return FI_ERR_INVALID_ARGUMENT;
+  if (opts && (opts->cta_pairs < 0 || opts->cta_pairs > 1)) return FI_ERR_INVALID_ARGUMENT;
   if (opts && opts->num_ctas < 0) return FI_ERR_INVALID_ARGUMENT;
   if (batch > 0 && (qo_indptr[0] != 0 || kv_indptr[0] != 0)) return FI_ERR_INVALID_ARGUMENT;
 
@@ -76,7 +77,11 @@ fi_status plan_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t 
                      ? 1
                      : 0;
   I.heads_per_cta = (P.group % 2 == 0) ? 2 : 1;
-  P.units_per_kv_head = P.group / I.heads_per_cta;
+  // Groups of a multiple of 4 query heads run on CTA pairs (2 heads each)
+  // that share their KV staging tiles, unless the options ask otherwise.
+  P.pair = (P.group % 4 == 0) && !(opts && opts->cta_pairs == 1);
+  I.ctas_per_unit = P.pair ? 2 : 1;
+  P.units_per_kv_head = P.group / (I.heads_per_cta * I.ctas_per_unit);
   I.head_units = num_kv_heads * P.units_per_kv_head;
   I.q_tiles = (max_qo + kTileQ - 1) / kTileQ;
   I.kv_bytes = I.total_kv_len * num_kv_heads * 2 * (head_dim / 2 + head_dim / 16);
@@ -165,7 +170,9 @@ fi_status plan_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t 
     }
   }
   const int32_t ctas = (opts && opts->num_ctas > 0) ? opts->num_ctas : default_ctas;
-  I.num_ctas = static_cast<int32_t>(std::min<int64_t>(I.num_units, std::max(ctas, 1)));
+  I.num_ctas = static_cast<int32_t>(std::min<int64_t>(I.num_units * I.ctas_per_unit,
+                                                      std::max(ctas, I.ctas_per_unit)));
+  if (P.pair) I.num_ctas &= ~1;
   return FI_OK;
 }
 

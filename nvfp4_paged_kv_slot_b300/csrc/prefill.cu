@@ -25,6 +25,7 @@
 // positions, so every staged KV tile is repacked once and used NQ times.
 // Tensor memory: S_i at column 128 i, O_i after all S.  Registers are moved
 // to the softmax warpgroups with setmaxnreg.  All waits are bounded.
+#include <algorithm>
 #include <cmath>
 
 #include "internal.h"
@@ -73,12 +74,16 @@ struct PrefillParams {
   float sm_scale;
 };
 
-template <int D, int NQ>
+// PAIR: a 2-CTA cluster shares its KV staging tiles; each CTA loads and
+// repacks half of every tile's rows (64 of 128) and writes them into both
+// CTAs' staging tiles, so the raw slots hold 64 rows.
+template <int D, int NQ, bool PAIR>
 struct Layout {
   static constexpr int kQTile = kTileQ * D * 2;
   static constexpr int kStg = kTileKV * D * 2;
-  static constexpr int kRawData = kTileKV * D / 2;
-  static constexpr int kRawSf = kTileKV * D / 16;
+  static constexpr int kRawRows = PAIR ? kTileKV / 2 : kTileKV;
+  static constexpr int kRawData = kRawRows * D / 2;
+  static constexpr int kRawSf = kRawRows * D / 16;
   static constexpr int kRaw = kRawData + kRawSf;
   static constexpr int kOffQ = 0;
   static constexpr int kOffStg = kOffQ + NQ * kQTile;
@@ -109,7 +114,10 @@ struct Unit {
 
 // tile id -> (sequence, head unit, q-tile): arithmetic for uniform batches
 // (#3575 §1, §2), the planner's list otherwise.
-__device__ __forceinline__ Unit decode_unit(const PrefillParams& p, int u, int nq) {
+// A unit covers heads_per_unit query heads of one GQA group; this CTA takes
+// the nq of them starting head_off heads into the unit.
+__device__ __forceinline__ Unit decode_unit(const PrefillParams& p, int u, int heads_per_unit,
+                                            int head_off) {
   Unit w;
   int hu;
   if (p.uniform) {
@@ -139,7 +147,7 @@ __device__ __forceinline__ Unit decode_unit(const PrefillParams& p, int u, int n
     w.kv_len = __ldg(p.kv_indptr + w.b + 1) - __ldg(p.kv_indptr + w.b);
   }
   w.hk = hu / p.units_per_kv_head;
-  w.hq0 = w.hk * p.group + (hu % p.units_per_kv_head) * nq;
+  w.hq0 = w.hk * p.group + (hu % p.units_per_kv_head) * heads_per_unit + head_off;
   const int last_row = min(w.qo_len, (w.qt + 1) * kTileQ) - 1;
   w.n_kv = (last_row + w.kv_len - w.qo_len) / kTileKV + 1;
   return w;
@@ -186,10 +194,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-template <int D, int NQ>
-__global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
+template <int D, int NQ, bool PAIR>
+__global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
     nvfp4_prefill_kernel(const __grid_constant__ PrefillParams p) {
-  using L = Layout<D, NQ>;
+  using L = Layout<D, NQ, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -212,6 +220,13 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
+  // Units: one per CTA, or one per CTA pair (both CTAs walk the same units;
+  // CTA rank r takes the unit's query heads r*NQ .. r*NQ+NQ-1).
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const int u0 = PAIR ? static_cast<int>(blockIdx.x / 2) : static_cast<int>(blockIdx.x);
+  const int ustride = PAIR ? static_cast<int>(gridDim.x / 2) : static_cast<int>(gridDim.x);
+  const int heads_per_unit = PAIR ? 2 * NQ : NQ;
+  const int head_off = static_cast<int>(rank) * NQ;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -221,8 +236,10 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
       mbar_init(raw_empty + s, kRepackThreads);
     }
     for (int s = 0; s < kStgStages; ++s) {
-      mbar_init(stg_full + s, kRepackThreads);
-      mbar_init(stg_empty + s, 1);
+      // PAIR: rows arrive from both CTAs' repack threads, and a slot is free
+      // once both CTAs' MMAs have read it.
+      mbar_init(stg_full + s, PAIR ? 2 * kRepackThreads : kRepackThreads);
+      mbar_init(stg_empty + s, PAIR ? 2 : 1);
     }
     for (int i = 0; i < NQ; ++i) {
       mbar_init(s_full + i, 1);
@@ -239,7 +256,12 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  if (PAIR) {
+    __syncwarp();
+    cluster_sync();  // the other CTA's barriers are initialized before any remote arrive
+  } else {
+    __syncthreads();
+  }
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const AbortState ab{abort_flag, p.status, kTimeoutNs, FI_DEV_WAIT_TIMEOUT};
@@ -250,23 +272,38 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
   auto repack_role = [&](int rt) {
     uint32_t raw_k = 0, stg_k = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x) {
-      const Unit w = decode_unit(p, u, NQ);
+    for (int u = u0; ok && u < p.num_units; u += ustride) {
+      const Unit w = decode_unit(p, u, heads_per_unit, head_off);
       for (int j = 0; ok && j < w.n_kv; ++j) {
         const int valid = min(kTileKV, w.kv_len - j * kTileKV);
         for (int t = 0; t < 2; ++t, ++raw_k, ++stg_k) {
           const int rs = raw_k % kRawStages;
           const int ss = stg_k % kStgStages;
           if (!mbar_wait(raw_full + rs, (raw_k / kRawStages) & 1, ab)) { ok = false; break; }
-          if (!mbar_wait(stg_empty + ss, ((stg_k / kStgStages) & 1) ^ 1, ab)) { ok = false; break; }
-          if (t)
-            repack_tile<D, true, kRepackThreads>(raw_smem + rs * L::kRaw,
-                                                 stg_smem + ss * L::kStg, valid, rt);
-          else
-            repack_tile<D, false, kRepackThreads>(raw_smem + rs * L::kRaw,
-                                                  stg_smem + ss * L::kStg, valid, rt);
-          fence_proxy_async_smem();
-          mbar_arrive(stg_full + ss);
+          if (!mbar_wait<PAIR>(stg_empty + ss, ((stg_k / kStgStages) & 1) ^ 1, ab)) { ok = false; break; }
+          if (PAIR) {
+            const int half_valid = min(max(valid - 64 * static_cast<int>(rank), 0), 64);
+            uint8_t* dst = stg_smem + ss * L::kStg;
+            const uint32_t peer_dst = mapa_shared(smem_u32(dst), rank ^ 1u);
+            if (t)
+              repack_half<D, true, kRepackThreads>(raw_smem + rs * L::kRaw, dst, peer_dst,
+                                                   64 * rank, half_valid, rt);
+            else
+              repack_half<D, false, kRepackThreads>(raw_smem + rs * L::kRaw, dst, peer_dst,
+                                                    64 * rank, half_valid, rt);
+            fence_proxy_async_cluster();
+            mbar_arrive(stg_full + ss);
+            mbar_arrive_cluster(mapa_shared(smem_u32(stg_full + ss), rank ^ 1u));
+          } else {
+            if (t)
+              repack_tile<D, true, kRepackThreads>(raw_smem + rs * L::kRaw,
+                                                   stg_smem + ss * L::kStg, valid, rt);
+            else
+              repack_tile<D, false, kRepackThreads>(raw_smem + rs * L::kRaw,
+                                                    stg_smem + ss * L::kStg, valid, rt);
+            fence_proxy_async_smem();
+            mbar_arrive(stg_full + ss);
+          }
           mbar_arrive(raw_empty + rs);
         }
       }
@@ -282,8 +319,15 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
     const uint32_t pg_data = static_cast<uint32_t>(p.page_size) * (D / 2);
     const uint32_t pg_sf = static_cast<uint32_t>(p.page_size) * (D / 16);
     const int pages_per_tile = kTileKV / p.page_size;
-    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
-      const Unit w = decode_unit(p, u, NQ);
+    // PAIR: this CTA's rows of a tile are 64*rank .. 64*rank+63: whole pages
+    // for page sizes up to 64, half a page (its rows 64*rank ..) for 128.
+    const int rows_per_copy = PAIR ? min(p.page_size, 64) : p.page_size;
+    const uint32_t cp_data = static_cast<uint32_t>(rows_per_copy) * (D / 2);
+    const uint32_t cp_sf = static_cast<uint32_t>(rows_per_copy) * (D / 16);
+    const int copies_per_tile = PAIR ? max(pages_per_tile / 2, 1) : pages_per_tile;
+    const uint32_t src_row_off = (PAIR && p.page_size == 128) ? 64u * rank : 0u;
+    for (int u = u0; ok && u < p.num_units; u += ustride, ++it) {
+      const Unit w = decode_unit(p, u, heads_per_unit, head_off);
       if (!mbar_wait(q_empty, (it & 1) ^ 1, ab)) {
         ok = false;
         break;
@@ -306,9 +350,10 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
             ok = false;
             break;
           }
-          const int first = j * pages_per_tile;
-          const int npg = min(pages_per_tile, seq_pages - first);
-          if (lane == 0) mbar_arrive_expect_tx(raw_full + slot, npg * (pg_data + pg_sf));
+          const int first = j * pages_per_tile +
+                            ((PAIR && pages_per_tile > 1) ? static_cast<int>(rank) * copies_per_tile : 0);
+          const int npg = max(min(copies_per_tile, seq_pages - first), 0);
+          if (lane == 0) mbar_arrive_expect_tx(raw_full + slot, npg * (cp_data + cp_sf));
           __syncwarp();
           if (lane < npg) {
             int page = __ldg(pt + first + lane);
@@ -317,11 +362,11 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
               page = 0;
             }
             const int64_t blk = static_cast<int64_t>(page) * p.num_kv_heads + w.hk;
-            const uint8_t* gd = (t ? p.v_data : p.k_data) + blk * pg_data;
-            const uint8_t* gs = (t ? p.v_sf : p.k_sf) + blk * pg_sf;
+            const uint8_t* gd = (t ? p.v_data : p.k_data) + blk * pg_data + src_row_off * (D / 2);
+            const uint8_t* gs = (t ? p.v_sf : p.k_sf) + blk * pg_sf + src_row_off * (D / 16);
             uint8_t* sd = raw_smem + slot * L::kRaw;
-            bulk_g2s(sd + lane * pg_data, gd, pg_data, raw_full + slot);
-            bulk_g2s(sd + L::kRawData + lane * pg_sf, gs, pg_sf, raw_full + slot);
+            bulk_g2s(sd + lane * cp_data, gd, cp_data, raw_full + slot);
+            bulk_g2s(sd + L::kRawData + lane * cp_sf, gs, cp_sf, raw_full + slot);
           }
           __syncwarp();
         }
@@ -365,6 +410,15 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
           mma_ss(d_tmem, qd + off, kd + off, kIdescQK, kk > 0 ? 1u : 0u);
         }
       };
+      // A staging slot is free once this CTA's MMAs have read it (PAIR: the
+      // arrival goes to the slot's barrier in both CTAs, whose repack threads
+      // both write into it).
+      auto release_stg = [&](uint32_t ss) {
+        if (PAIR)
+          mma_commit_multicast(stg_empty + ss, 3);
+        else
+          mma_commit(stg_empty + ss);
+      };
       // PV over keys 64h .. 64h+63 (P columns 32h .. 32h+31)
       auto issue_pv_half = [&](int i, uint32_t ss, int h, bool acc) {
         const uint32_t d_tmem = tmem_base + NQ * 128 + i * D;
@@ -375,12 +429,12 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
           mma_ts(d_tmem, a_tmem + s * 8, vd + ((s * 2048) >> 4), kIdescPV,
                  (acc || s > 0) ? 1u : 0u);
       };
-      for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
-        const Unit w = decode_unit(p, u, NQ);
+      for (int u = u0; ok && u < p.num_units; u += ustride, ++it) {
+        const Unit w = decode_unit(p, u, heads_per_unit, head_off);
         if (!mbar_wait(q_full, it & 1, ab)) { ok = false; break; }
         // K tile 0
         uint32_t ss_k = stg_k % kStgStages;
-        if (!mbar_wait(stg_full + ss_k, (stg_k / kStgStages) & 1, ab)) { ok = false; break; }
+        if (!mbar_wait<PAIR>(stg_full + ss_k, (stg_k / kStgStages) & 1, ab)) { ok = false; break; }
         ++stg_k;
         tc_fence_after();
         for (int i = 0; i < NQ; ++i) {
@@ -388,10 +442,10 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
           mma_commit(s_full + i);
         }
         if (w.n_kv == 1) mma_commit(q_empty);
-        mma_commit(stg_empty + ss_k);
+        release_stg(ss_k);
         for (int j = 0; ok && j < w.n_kv; ++j) {
           const uint32_t ss_v = stg_k % kStgStages;
-          if (!mbar_wait(stg_full + ss_v, (stg_k / kStgStages) & 1, ab)) { ok = false; break; }
+          if (!mbar_wait<PAIR>(stg_full + ss_v, (stg_k / kStgStages) & 1, ab)) { ok = false; break; }
           ++stg_k;
           const bool more = j + 1 < w.n_kv;
           for (int i = 0; i < NQ; ++i) {
@@ -404,18 +458,18 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
             ++pk[i];
             tc_fence_after();
             issue_pv_half(i, ss_v, 1, true);
-            if (i == NQ - 1) mma_commit(stg_empty + ss_v);
+            if (i == NQ - 1) release_stg(ss_v);
             if (more) {
               if (i == 0) {
                 ss_k = stg_k % kStgStages;
-                if (!mbar_wait(stg_full + ss_k, (stg_k / kStgStages) & 1, ab)) { ok = false; break; }
+                if (!mbar_wait<PAIR>(stg_full + ss_k, (stg_k / kStgStages) & 1, ab)) { ok = false; break; }
                 ++stg_k;
                 tc_fence_after();
               }
               issue_qk(i, ss_k);
               mma_commit(s_full + i);
               if (i == NQ - 1) {
-                mma_commit(stg_empty + ss_k);
+                release_stg(ss_k);
                 if (j + 2 == w.n_kv) mma_commit(q_empty);
               }
             }
@@ -453,8 +507,8 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
     uint32_t sk = 0;
     int it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.num_units; u += gridDim.x, ++it) {
-      const Unit w = decode_unit(p, u, NQ);
+    for (int u = u0; ok && u < p.num_units; u += ustride, ++it) {
+      const Unit w = decode_unit(p, u, heads_per_unit, head_off);
       const int row_q = w.qt * kTileQ + r;
       const int delta = w.kv_len - w.qo_len;
       const int limit = row_q + delta;                 // last key this row sees
@@ -597,15 +651,20 @@ __global__ void __launch_bounds__(Layout<D, NQ>::kThreads, 1)
 
   __syncwarp();
   tc_fence_before();
-  __syncthreads();
+  // PAIR: neither CTA leaves while the other may still write into its
+  // staging tiles or arrive on its barriers.
+  if (PAIR)
+    cluster_sync();
+  else
+    __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, L::kTmemCols);
 }
 
-template <int D, int NQ>
+template <int D, int NQ, bool PAIR>
 fi_status launch_impl(const PrefillParams& p, int grid, cudaStream_t stream) {
-  using L = Layout<D, NQ>;
-  auto kern = nvfp4_prefill_kernel<D, NQ>;
+  using L = Layout<D, NQ, PAIR>;
+  auto kern = nvfp4_prefill_kernel<D, NQ, PAIR>;
   // at least ~116 KB so that a single CTA (and its 256-512 TMEM columns)
   // occupies each SM
   const int smem = L::kAlloc > 118784 ? L::kAlloc : 118784;
@@ -618,7 +677,33 @@ fi_status launch_impl(const PrefillParams& p, int grid, cudaStream_t stream) {
   if (cudaFuncGetAttributes(&attr, kern) != cudaSuccess) return FI_ERR_CUDA;
   if (128 * (attr.numRegs + L::kRegRepack + NQ * L::kRegSoftmax) > attr.numRegs * L::kThreads)
     return FI_ERR_UNSUPPORTED;
-  kern<<<grid, L::kThreads, smem, stream>>>(p);
+  if (!PAIR) {
+    kern<<<grid, L::kThreads, smem, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? FI_OK : FI_ERR_CUDA;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute cl[1];
+  cl[0].id = cudaLaunchAttributeClusterDimension;
+  cl[0].val.clusterDim.x = 2;
+  cl[0].val.clusterDim.y = 1;
+  cl[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(L::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = cl;
+  cfg.numAttrs = 1;
+  // as many pairs as can be resident at once (persistent), at most one per unit
+  static int max_clusters = 0;
+  if (max_clusters == 0) {
+    cfg.gridDim = dim3(2 * 74);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0)
+      return FI_ERR_CUDA;
+    max_clusters = n;
+  }
+  const int pairs = std::max(1, std::min(grid / 2, max_clusters));
+  cfg.gridDim = dim3(2 * pairs);
+  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return FI_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? FI_OK : FI_ERR_CUDA;
 }
 
@@ -666,8 +751,16 @@ fi_status launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.sm_scale = P.sm_scale;
   const int grid = P.info.num_ctas;
   const int nq = P.info.heads_per_cta;
-  if (D == 128) return nq == 2 ? launch_impl<128, 2>(p, grid, stream) : launch_impl<128, 1>(p, grid, stream);
-  return nq == 2 ? launch_impl<64, 2>(p, grid, stream) : launch_impl<64, 1>(p, grid, stream);
+  if (P.pair) {
+    if (nq != 2) return FI_ERR_UNSUPPORTED;
+    return D == 128 ? launch_impl<128, 2, true>(p, grid, stream)
+                    : launch_impl<64, 2, true>(p, grid, stream);
+  }
+  if (D == 128)
+    return nq == 2 ? launch_impl<128, 2, false>(p, grid, stream)
+                   : launch_impl<128, 1, false>(p, grid, stream);
+  return nq == 2 ? launch_impl<64, 2, false>(p, grid, stream)
+                 : launch_impl<64, 1, false>(p, grid, stream);
 }
 
 }  // namespace fi

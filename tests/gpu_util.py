@@ -59,7 +59,7 @@ def cache_to_host(c):
             "page_size": c.page_size, "head_dim": c.head_dim}
 
 
-def run_path(d, cache=None, schedule=0, num_ctas=0, with_lse=True):
+def run_path(d, cache=None, schedule=0, num_ctas=0, with_lse=True, cta_pairs=0):
     """append -> plan -> run through the C ABI; returns (out, lse, cache, ctx, plan info)."""
     m = fi()
     sp = d["spec"]
@@ -69,7 +69,8 @@ def run_path(d, cache=None, schedule=0, num_ctas=0, with_lse=True):
     plan = m.fi_plan_create(ctx)
     m.fi_prefill_plan(plan, d["host"]["qo_indptr"], d["host"]["kv_indptr"], d["page_table"],
                       sp.num_qo_heads, sp.num_kv_heads, sp.head_dim, sp.page_size,
-                      sm_scale=d["sm_scale"], schedule=schedule, num_ctas=num_ctas)
+                      sm_scale=d["sm_scale"], schedule=schedule, num_ctas=num_ctas,
+                      cta_pairs=cta_pairs)
     out = torch.empty_like(d["q"])
     lse = torch.empty(d["q"].shape[:2], dtype=torch.float32, device="cuda") if with_lse else None
     m.fi_prefill_run(plan, d["q"], cache, out, lse)

@@ -31,6 +31,21 @@ def test_prefill_matches_oracle(name, schedule):
     assert_within_tolerance(res)
 
 
+@pytest.mark.parametrize("name", ["ragged_small", "uniform_small"])
+@pytest.mark.parametrize("schedule", [0, 1])
+def test_prefill_single_cta_path_for_groups_of_four(name, schedule):
+    """GQA groups of 4 run on CTA pairs by default; the single-CTA kernel (two
+    heads per CTA, no shared staging) must give the same results."""
+    d = device_inputs(name)
+    out, lse, _, status, info = run_path(d, schedule=schedule, cta_pairs=1)
+    assert status == 0 and info["ctas_per_unit"] == 1
+    ref_out, ref_lse = oracle_attention(d, oracle_cache(d))
+    assert_within_tolerance(compare_attention(out, lse, ref_out, ref_lse))
+    pair_out, pair_lse, _, status, info = run_path(d, schedule=schedule)
+    assert status == 0 and info["ctas_per_unit"] == 2
+    assert_within_tolerance(compare_attention(pair_out, pair_lse, ref_out, ref_lse))
+
+
 def test_prefill_single_sequence_2048_sampled():
     d = device_inputs("single")
     out, lse, cache, status, info = run_path(d)

@@ -37,15 +37,20 @@ def test_plan_max_lens(dtype, batch, page_size):
     assert info["batch"] == batch
 
 
-def test_uniform_flag_and_o1_decode_orders():
+@pytest.mark.parametrize("cta_pairs", [0, 1])
+def test_uniform_flag_and_o1_decode_orders(cta_pairs):
     B, L = 6, 300
     ind = fi.indptr_from_lens([L] * B)
     for schedule, global_rev in ((1, 1), (2, 0)):
-        info, work = fi.fi_prefill_plan_host(ind, ind, 8, 2, 128, 16, schedule=schedule)
+        info, work = fi.fi_prefill_plan_host(ind, ind, 8, 2, 128, 16, schedule=schedule,
+                                             cta_pairs=cta_pairs)
         assert info["is_uniform"] == 1 and info["global_reverse"] == global_rev
         q_tiles = (L + 127) // 128
         HU = info["head_units"]
-        assert info["heads_per_cta"] == 2 and HU == 2 * 2
+        # G = 4: a unit is the whole group on a CTA pair, or two heads on one CTA
+        assert info["heads_per_cta"] == 2
+        assert info["ctas_per_unit"] == (2 if cta_pairs == 0 else 1)
+        assert HU == (2 * 1 if cta_pairs == 0 else 2 * 2)
         assert info["num_units"] == B * HU * q_tiles == work.shape[0]
         # every (b, hu, qt) exactly once
         assert len({tuple(w[:3]) for w in work}) == work.shape[0]
@@ -56,6 +61,21 @@ def test_uniform_flag_and_o1_decode_orders():
             else:
                 assert b == t // (HU * q_tiles)
                 assert qt == q_tiles - 1 - (t % (HU * q_tiles)) % q_tiles
+
+
+@pytest.mark.parametrize("hq,hk,pairs,hu", [(4, 2, 1, 2 * 1), (8, 2, 2, 2 * 1), (16, 2, 2, 2 * 2),
+                                             (6, 2, 1, 2 * 3), (2, 2, 1, 2 * 1)])
+def test_cta_pair_decision(hq, hk, pairs, hu):
+    """Groups of a multiple of 4 query heads run on CTA pairs (two heads per
+    CTA); other groups on single CTAs (two heads per CTA if the group is even)."""
+    ind = fi.indptr_from_lens([200, 300])
+    info, work = fi.fi_prefill_plan_host(ind, ind, hq, hk, 128, 16)
+    assert info["ctas_per_unit"] == pairs and info["head_units"] == hu
+    assert info["num_units"] == work.shape[0] == hu * (2 + 3)
+    assert info["num_ctas"] % pairs == 0
+    if pairs == 2:
+        off, _ = fi.fi_prefill_plan_host(ind, ind, hq, hk, 128, 16, cta_pairs=1)
+        assert off["ctas_per_unit"] == 1 and off["head_units"] == 2 * hu
 
 
 def test_uniform_check_is_totals_based():
@@ -143,7 +163,8 @@ def test_workload_shapes():
     info, _ = fi.fi_prefill_plan_host(*([fi.indptr_from_lens(W.spec("uniform").seq_lens)] * 2),
                                       32, 8, 128, 16, with_list=False)
     assert info["is_uniform"] == 1 and info["global_reverse"] == 0   # 1.2 GB KV > L2
-    assert info["num_units"] == 1024 * 16 * 8
+    # G = 4: one unit per (sequence, kv head, q-tile), on a CTA pair
+    assert info["ctas_per_unit"] == 2 and info["num_units"] == 1024 * 8 * 8
     sp = W.spec("single")
     ind = fi.indptr_from_lens(sp.seq_lens)
     info, _ = fi.fi_prefill_plan_host(ind, ind, 32, 8, 128, 16, with_list=False)
