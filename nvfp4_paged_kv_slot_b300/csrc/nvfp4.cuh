@@ -207,14 +207,13 @@ __device__ __forceinline__ void repack_tile(const uint8_t* raw, uint8_t* dst, in
 
 // Repacks half a tile, for a pair of CTAs that share their staging tiles:
 // `raw` holds 64 token rows (D/2 code bytes each, then 64 rows of D/16 scale
-// bytes); they become rows row_base .. row_base+63 of the staging tile, both
-// in this CTA's shared memory (`dst`) and in the other CTA's (`peer_dst`, the
-// same tile's shared::cluster address there).  Rows at or beyond `valid` (of
-// the 64) are written as zeros.  Same task layout and store order as
+// bytes); they become rows row_base .. row_base+63 of the staging tile `dst`
+// (the other CTA receives them by a bulk copy).  Rows at or beyond `valid`
+// (of the 64) are written as zeros.  Same task layout and store order as
 // repack_tile; row_base is a multiple of 8, so the swizzle phase is unchanged.
 template <int D, bool IS_V, int NT>
-__device__ __forceinline__ void repack_half(const uint8_t* raw, uint8_t* dst, uint32_t peer_dst,
-                                            int row_base, int valid, int tid) {
+__device__ __forceinline__ void repack_half(const uint8_t* raw, uint8_t* dst, int row_base,
+                                            int valid, int tid) {
   static_assert(NT % (D / 8) == 0 && NT % 64 == 0, "constant-stride tasks");
   constexpr int kPer = 64 * (D / 8) / NT;        // tasks per thread
   constexpr int kRowStep = NT / (D / 8);
@@ -237,9 +236,7 @@ __device__ __forceinline__ void repack_half(const uint8_t* raw, uint8_t* dst, ui
       uint4 o = make_uint4(0u, 0u, 0u, 0u);
       if (row0 + (k0 + k) * kRowStep < valid)
         o = IS_V ? dequant8_f16(w[k], s8[k]) : dequant8_bf16(w[k], s8[k]);
-      const uint32_t off = off0 + (k0 + k) * kRowStep * 128;
-      *reinterpret_cast<uint4*>(dst + off) = o;
-      st_cluster_v4(peer_dst + off, o);
+      *reinterpret_cast<uint4*>(dst + off0 + (k0 + k) * kRowStep * 128) = o;
     }
   }
 }

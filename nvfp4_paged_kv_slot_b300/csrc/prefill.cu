@@ -35,7 +35,6 @@ namespace fi {
 
 namespace {
 
-constexpr int kRawStages = 4;
 constexpr int kStgStages = 3;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 constexpr uint64_t kDrainNs = 100000000ull;     // 0.1 s per wait while aborting
@@ -82,6 +81,8 @@ struct Layout {
   static constexpr int kQTile = kTileQ * D * 2;
   static constexpr int kStg = kTileKV * D * 2;
   static constexpr int kRawRows = PAIR ? kTileKV / 2 : kTileKV;
+  // raw ring depth: half-size slots give a pair twice the loads in flight
+  static constexpr int kRawStages = PAIR ? 8 : 4;
   static constexpr int kRawData = kRawRows * D / 2;
   static constexpr int kRawSf = kRawRows * D / 16;
   static constexpr int kRaw = kRawData + kRawSf;
@@ -91,8 +92,9 @@ struct Layout {
   static constexpr int kOffBar = kOffRaw + kRawStages * kRaw;
   // q_full, q_empty, raw_full[], raw_empty[], stg_full[], stg_empty[],
   // s_full[NQ], p_full[2 NQ] (P columns of keys 0-63 / 64-127 of head i at
-  // 2i / 2i+1), o_full[NQ], drain
-  static constexpr int kNumBars = 2 + 2 * kRawStages + 2 * kStgStages + 4 * NQ + 1;
+  // 2i / 2i+1), o_full[NQ], drain, rep_done[] (PAIR: this CTA's rows of a
+  // staging slot are written)
+  static constexpr int kNumBars = 2 + 2 * kRawStages + 3 * kStgStages + 4 * NQ + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
@@ -208,13 +210,14 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
   uint64_t* raw_full = bars + 2;
-  uint64_t* raw_empty = raw_full + kRawStages;
-  uint64_t* stg_full = raw_empty + kRawStages;
+  uint64_t* raw_empty = raw_full + L::kRawStages;
+  uint64_t* stg_full = raw_empty + L::kRawStages;
   uint64_t* stg_empty = stg_full + kStgStages;
   uint64_t* s_full = stg_empty + kStgStages;
   uint64_t* p_full = s_full + NQ;
   uint64_t* o_full = p_full + 2 * NQ;
   uint64_t* drain = o_full + NQ;
+  uint64_t* rep_done = drain + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
   int* abort_flag = reinterpret_cast<int*>(smem + L::kOffMisc + 4);
 
@@ -231,14 +234,14 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    for (int s = 0; s < kRawStages; ++s) {
+    for (int s = 0; s < L::kRawStages; ++s) {
       mbar_init(raw_full + s, 1);
       mbar_init(raw_empty + s, kRepackThreads);
     }
     for (int s = 0; s < kStgStages; ++s) {
-      // PAIR: rows arrive from both CTAs' repack threads, and a slot is free
-      // once both CTAs' MMAs have read it.
-      mbar_init(stg_full + s, PAIR ? 2 * kRepackThreads : kRepackThreads);
+      // PAIR: the other CTA's rows arrive as bytes (expected by one local
+      // arrival), and a slot is free once both CTAs' MMAs have read it.
+      mbar_init(stg_full + s, kRepackThreads);
       mbar_init(stg_empty + s, PAIR ? 2 : 1);
     }
     for (int i = 0; i < NQ; ++i) {
@@ -248,6 +251,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
       mbar_init(o_full + i, 1);
     }
     mbar_init(drain, 1);
+    for (int s = 0; s < kStgStages; ++s) mbar_init(rep_done + s, kRepackThreads);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -277,23 +281,41 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
       for (int j = 0; ok && j < w.n_kv; ++j) {
         const int valid = min(kTileKV, w.kv_len - j * kTileKV);
         for (int t = 0; t < 2; ++t, ++raw_k, ++stg_k) {
-          const int rs = raw_k % kRawStages;
+          const int rs = raw_k % L::kRawStages;
           const int ss = stg_k % kStgStages;
-          if (!mbar_wait(raw_full + rs, (raw_k / kRawStages) & 1, ab)) { ok = false; break; }
+          if (!mbar_wait(raw_full + rs, (raw_k / L::kRawStages) & 1, ab)) { ok = false; break; }
           if (!mbar_wait<PAIR>(stg_empty + ss, ((stg_k / kStgStages) & 1) ^ 1, ab)) { ok = false; break; }
           if (PAIR) {
+            // This CTA's 64 rows go into its own staging tile; once all the
+            // repack threads have written them, one thread bulk-copies them
+            // into the other CTA's tile (D/64 contiguous 8 KB pieces, one per
+            // 64-column block), counted in bytes on that CTA's stg_full.
             const int half_valid = min(max(valid - 64 * static_cast<int>(rank), 0), 64);
             uint8_t* dst = stg_smem + ss * L::kStg;
-            const uint32_t peer_dst = mapa_shared(smem_u32(dst), rank ^ 1u);
             if (t)
-              repack_half<D, true, kRepackThreads>(raw_smem + rs * L::kRaw, dst, peer_dst,
-                                                   64 * rank, half_valid, rt);
+              repack_half<D, true, kRepackThreads>(raw_smem + rs * L::kRaw, dst, 64 * rank,
+                                                   half_valid, rt);
             else
-              repack_half<D, false, kRepackThreads>(raw_smem + rs * L::kRaw, dst, peer_dst,
-                                                    64 * rank, half_valid, rt);
-            fence_proxy_async_cluster();
-            mbar_arrive(stg_full + ss);
-            mbar_arrive_cluster(mapa_shared(smem_u32(stg_full + ss), rank ^ 1u));
+              repack_half<D, false, kRepackThreads>(raw_smem + rs * L::kRaw, dst, 64 * rank,
+                                                    half_valid, rt);
+            fence_proxy_async_smem();
+            mbar_arrive(rep_done + ss);
+            if (rt == 0) {
+              // every repack thread's rows of this slot are written (a bounded
+              // wait, like all others: a timed-out sibling cannot hang it)
+              if (!mbar_wait(rep_done + ss, (stg_k / kStgStages) & 1, ab)) { ok = false; break; }
+              const uint32_t peer_bar = mapa_shared(smem_u32(stg_full + ss), rank ^ 1u);
+#pragma unroll
+              for (int cb = 0; cb < D / 64; ++cb) {
+                uint8_t* piece = dst + cb * 16384 + 64 * rank * 128;
+                bulk_s2s_cluster(mapa_shared(smem_u32(piece), rank ^ 1u), piece, 64 * 128,
+                                 peer_bar);
+              }
+              // the bytes the other CTA sends into this CTA's tile
+              mbar_arrive_expect_tx(stg_full + ss, (D / 64) * 64 * 128);
+            } else {
+              mbar_arrive(stg_full + ss);
+            }
           } else {
             if (t)
               repack_tile<D, true, kRepackThreads>(raw_smem + rs * L::kRaw,
@@ -345,8 +367,8 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
       const int seq_pages = (w.kv_len + p.page_size - 1) / p.page_size;
       for (int j = 0; ok && j < w.n_kv; ++j) {
         for (int t = 0; t < 2; ++t, ++raw_k) {
-          const int slot = raw_k % kRawStages;
-          if (!mbar_wait(raw_empty + slot, ((raw_k / kRawStages) & 1) ^ 1, ab)) {
+          const int slot = raw_k % L::kRawStages;
+          if (!mbar_wait(raw_empty + slot, ((raw_k / L::kRawStages) & 1) ^ 1, ab)) {
             ok = false;
             break;
           }
@@ -377,9 +399,9 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
       // flight so that no copy lands in shared memory after the CTA exits.
       volatile int drain_flag = 0;
       const AbortState drain_ab{&drain_flag, nullptr, kDrainNs, 0};
-      const uint32_t n = raw_k < kRawStages ? raw_k : kRawStages;
+      const uint32_t n = raw_k < L::kRawStages ? raw_k : L::kRawStages;
       for (uint32_t f = raw_k - n; f < raw_k; ++f)
-        mbar_wait(raw_full + (f % kRawStages), (f / kRawStages) & 1, drain_ab);
+        mbar_wait(raw_full + (f % L::kRawStages), (f / L::kRawStages) & 1, drain_ab);
       if (q_issued >= 0) mbar_wait(q_full, q_issued & 1, drain_ab);
     }
   } else if (warp == 1) {

@@ -143,6 +143,22 @@ __device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta
       "h"(cta_mask)
       : "memory");
 }
+// Bulk copy (TMA engine) from this CTA's shared memory into another CTA's of
+// the cluster; completion is counted in bytes on the mbarrier there (both
+// addresses are shared::cluster addresses of that CTA, from mapa_shared).
+// Addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_s2s_cluster(uint32_t dst_caddr, const void* src,
+                                                 uint32_t bytes, uint32_t mbar_caddr) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst_caddr),
+      "r"(smem_u32(src)), "r"(bytes), "r"(mbar_caddr)
+      : "memory");
+}
+// Named barrier for `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 // Every thread of both CTAs of the cluster.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
