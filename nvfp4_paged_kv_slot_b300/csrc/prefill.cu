@@ -35,7 +35,6 @@ namespace fi {
 
 namespace {
 
-constexpr int kStgStages = 3;
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 constexpr uint64_t kDrainNs = 100000000ull;     // 0.1 s per wait while aborting
 // The running max is moved (and O rescaled) only when it grows by more than
@@ -81,8 +80,12 @@ struct Layout {
   static constexpr int kQTile = kTileQ * D * 2;
   static constexpr int kStg = kTileKV * D * 2;
   static constexpr int kRawRows = PAIR ? kTileKV / 2 : kTileKV;
-  // raw ring depth: half-size slots give a pair twice the loads in flight
-  static constexpr int kRawStages = PAIR ? 8 : 4;
+  // Ring depths.  Staging slots are used K0 V0 K1 V1 ...; with 3 slots, K of
+  // the next tile reuses the slot of V of the previous one and must be
+  // repacked within about one head's PV + QK^T; with 4 (pairs, whose raw
+  // slots are half size) the deadline doubles.
+  static constexpr int kStgStages = PAIR ? 4 : 3;
+  static constexpr int kRawStages = 4;
   static constexpr int kRawData = kRawRows * D / 2;
   static constexpr int kRawSf = kRawRows * D / 16;
   static constexpr int kRaw = kRawData + kRawSf;
@@ -212,8 +215,8 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
   uint64_t* raw_full = bars + 2;
   uint64_t* raw_empty = raw_full + L::kRawStages;
   uint64_t* stg_full = raw_empty + L::kRawStages;
-  uint64_t* stg_empty = stg_full + kStgStages;
-  uint64_t* s_full = stg_empty + kStgStages;
+  uint64_t* stg_empty = stg_full + L::kStgStages;
+  uint64_t* s_full = stg_empty + L::kStgStages;
   uint64_t* p_full = s_full + NQ;
   uint64_t* o_full = p_full + 2 * NQ;
   uint64_t* drain = o_full + NQ;
@@ -238,7 +241,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
       mbar_init(raw_full + s, 1);
       mbar_init(raw_empty + s, kRepackThreads);
     }
-    for (int s = 0; s < kStgStages; ++s) {
+    for (int s = 0; s < L::kStgStages; ++s) {
       // PAIR: the other CTA's rows arrive as bytes (expected by one local
       // arrival), and a slot is free once both CTAs' MMAs have read it.
       mbar_init(stg_full + s, kRepackThreads);
@@ -251,7 +254,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
       mbar_init(o_full + i, 1);
     }
     mbar_init(drain, 1);
-    for (int s = 0; s < kStgStages; ++s) mbar_init(rep_done + s, kRepackThreads);
+    for (int s = 0; s < L::kStgStages; ++s) mbar_init(rep_done + s, kRepackThreads);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -282,9 +285,9 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
         const int valid = min(kTileKV, w.kv_len - j * kTileKV);
         for (int t = 0; t < 2; ++t, ++raw_k, ++stg_k) {
           const int rs = raw_k % L::kRawStages;
-          const int ss = stg_k % kStgStages;
+          const int ss = stg_k % L::kStgStages;
           if (!mbar_wait(raw_full + rs, (raw_k / L::kRawStages) & 1, ab)) { ok = false; break; }
-          if (!mbar_wait<PAIR>(stg_empty + ss, ((stg_k / kStgStages) & 1) ^ 1, ab)) { ok = false; break; }
+          if (!mbar_wait<PAIR>(stg_empty + ss, ((stg_k / L::kStgStages) & 1) ^ 1, ab)) { ok = false; break; }
           if (PAIR) {
             // This CTA's 64 rows go into its own staging tile; once all the
             // repack threads have written them, one thread bulk-copies them
@@ -303,7 +306,7 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
             if (rt == 0) {
               // every repack thread's rows of this slot are written (a bounded
               // wait, like all others: a timed-out sibling cannot hang it)
-              if (!mbar_wait(rep_done + ss, (stg_k / kStgStages) & 1, ab)) { ok = false; break; }
+              if (!mbar_wait(rep_done + ss, (stg_k / L::kStgStages) & 1, ab)) { ok = false; break; }
               const uint32_t peer_bar = mapa_shared(smem_u32(stg_full + ss), rank ^ 1u);
 #pragma unroll
               for (int cb = 0; cb < D / 64; ++cb) {
@@ -455,8 +458,8 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
         const Unit w = decode_unit(p, u, heads_per_unit, head_off);
         if (!mbar_wait(q_full, it & 1, ab)) { ok = false; break; }
         // K tile 0
-        uint32_t ss_k = stg_k % kStgStages;
-        if (!mbar_wait<PAIR>(stg_full + ss_k, (stg_k / kStgStages) & 1, ab)) { ok = false; break; }
+        uint32_t ss_k = stg_k % L::kStgStages;
+        if (!mbar_wait<PAIR>(stg_full + ss_k, (stg_k / L::kStgStages) & 1, ab)) { ok = false; break; }
         ++stg_k;
         tc_fence_after();
         for (int i = 0; i < NQ; ++i) {
@@ -466,8 +469,8 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
         if (w.n_kv == 1) mma_commit(q_empty);
         release_stg(ss_k);
         for (int j = 0; ok && j < w.n_kv; ++j) {
-          const uint32_t ss_v = stg_k % kStgStages;
-          if (!mbar_wait<PAIR>(stg_full + ss_v, (stg_k / kStgStages) & 1, ab)) { ok = false; break; }
+          const uint32_t ss_v = stg_k % L::kStgStages;
+          if (!mbar_wait<PAIR>(stg_full + ss_v, (stg_k / L::kStgStages) & 1, ab)) { ok = false; break; }
           ++stg_k;
           const bool more = j + 1 < w.n_kv;
           for (int i = 0; i < NQ; ++i) {
@@ -483,8 +486,8 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
             if (i == NQ - 1) release_stg(ss_v);
             if (more) {
               if (i == 0) {
-                ss_k = stg_k % kStgStages;
-                if (!mbar_wait<PAIR>(stg_full + ss_k, (stg_k / kStgStages) & 1, ab)) { ok = false; break; }
+                ss_k = stg_k % L::kStgStages;
+                if (!mbar_wait<PAIR>(stg_full + ss_k, (stg_k / L::kStgStages) & 1, ab)) { ok = false; break; }
                 ++stg_k;
                 tc_fence_after();
               }
