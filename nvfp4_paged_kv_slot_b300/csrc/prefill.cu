@@ -9,11 +9,12 @@
 //    §2 global reverse-Q-tile order, heaviest tiles first; §3 the L2 gate.
 //
 // B300 design (one persistent CTA per SM, warp-specialized):
-//   warp 0        load: TMA of the Q tiles (128B swizzle), bulk copies of the
-//                 FP4 pages and E4M3 scales of each KV tile into a raw ring
+//   warp 0        KV loads: bulk copies of the FP4 pages and E4M3 scales of
+//                 each KV tile into a raw ring
+//   warp 2        Q loads: TMA of the Q tiles (128B swizzle)
 //   warp 1        MMA: one thread issues tcgen05.mma (QK^T: bf16 SS; PV: fp16
 //                 TS with P in tensor memory) and tcgen05.commit
-//   warps 2-3     idle
+//   warp 3        idle
 //   WG 1..NQ      softmax, one warpgroup per Q tile, one thread per query row:
 //                 the row of S in registers (one tensor-memory read), online
 //                 softmax in fp32 (base 2, paired fp32 arithmetic, exp2 split
@@ -335,12 +336,10 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
     }
   };
   if (warp == 0) {
-    // ------------------------------------------------------------- load warp
-    if (lane == 0) prefetch_tensormap(&p.tmap_q);
+    // ------------------------------------------------------- KV load warp
     uint32_t raw_k = 0;
     int it = 0;
     bool ok = true;
-    int q_issued = -1;  // iteration of the last Q load issued
     const uint32_t pg_data = static_cast<uint32_t>(p.page_size) * (D / 2);
     const uint32_t pg_sf = static_cast<uint32_t>(p.page_size) * (D / 16);
     const int pages_per_tile = kTileKV / p.page_size;
@@ -353,19 +352,6 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
     const uint32_t src_row_off = (PAIR && p.page_size == 128) ? 64u * rank : 0u;
     for (int u = u0; ok && u < p.num_units; u += ustride, ++it) {
       const Unit w = decode_unit(p, u, heads_per_unit, head_off);
-      if (!mbar_wait(q_empty, (it & 1) ^ 1, ab)) {
-        ok = false;
-        break;
-      }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(q_full, NQ * L::kQTile);
-        for (int i = 0; i < NQ; ++i)
-          for (int h = 0; h < D / 64; ++h)
-            tma_load_3d(q_smem + i * L::kQTile + h * 16384, &p.tmap_q, q_full, h * 64,
-                        w.hq0 + i, w.qo_start + w.qt * kTileQ);
-      }
-      q_issued = it;
-      __syncwarp();
       const int32_t* pt = p.page_table + static_cast<int64_t>(w.b) * p.pt_stride;
       const int seq_pages = (w.kv_len + p.page_size - 1) / p.page_size;
       for (int j = 0; ok && j < w.n_kv; ++j) {
@@ -405,7 +391,6 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
       const uint32_t n = raw_k < L::kRawStages ? raw_k : L::kRawStages;
       for (uint32_t f = raw_k - n; f < raw_k; ++f)
         mbar_wait(raw_full + (f % L::kRawStages), (f / L::kRawStages) & 1, drain_ab);
-      if (q_issued >= 0) mbar_wait(q_full, q_issued & 1, drain_ab);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA warp
@@ -509,8 +494,32 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
       const AbortState drain_ab{&drain_flag, nullptr, ok ? kTimeoutNs : kDrainNs, 0};
       mbar_wait(drain, 0, drain_ab);
     }
+  } else if (warp == 2) {
+    // -------------------------------------------------------- Q load warp
+    // Q tiles are loaded as soon as the buffer is free (the last QK^T of the
+    // previous unit has completed), independently of the KV loads, so the
+    // next unit's Q is in flight while the current unit finishes.
+    if (lane == 0) {
+      prefetch_tensormap(&p.tmap_q);
+      int it = 0;
+      int q_issued = -1;  // iteration of the last Q load issued
+      for (int u = u0; u < p.num_units; u += ustride, ++it) {
+        const Unit w = decode_unit(p, u, heads_per_unit, head_off);
+        if (!mbar_wait(q_empty, (it & 1) ^ 1, ab)) break;
+        mbar_arrive_expect_tx(q_full, NQ * L::kQTile);
+        for (int i = 0; i < NQ; ++i)
+          for (int h = 0; h < D / 64; ++h)
+            tma_load_3d(q_smem + i * L::kQTile + h * 16384, &p.tmap_q, q_full, h * 64,
+                        w.hq0 + i, w.qo_start + w.qt * kTileQ);
+        q_issued = it;
+      }
+      // no copy may land in shared memory after the CTA exits
+      volatile int drain_flag = 0;
+      const AbortState drain_ab{&drain_flag, nullptr, kDrainNs, 0};
+      if (q_issued >= 0) mbar_wait(q_full, q_issued & 1, drain_ab);
+    }
   } else if (wg == 0) {
-    // warps 2-3: no role
+    // warp 3: no role
   } else if (wg <= NQ) {
     // ------------------------------------------------------------- softmax
     setmaxnreg_inc<L::kRegSoftmax>();
