@@ -71,6 +71,7 @@ struct PrefillParams {
   int32_t uniform, global_reverse, uni_qo_len, uni_kv_len, q_tiles;
   int32_t num_units;
   float sm_scale;
+  int32_t out_align32;  // `out` is 32-byte aligned: 32-byte stores in the epilogue
 };
 
 // PAIR: a 2-CTA cluster shares its KV staging tiles; each CTA loads and
@@ -654,20 +655,26 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
       const float inv = vs / l;
       __nv_bfloat16* dst =
           p.out + (static_cast<int64_t>(w.qo_start + row_q) * p.num_qo_heads + w.hq0 + i) * D;
+      // the whole row of O in one tensor-memory read, then 32-byte stores
+      // (full sectors; 16-byte stores when `out` is only 16-byte aligned)
+      uint32_t o[D];
+      if constexpr (D == 128)
+        tmem_ld128(o_col, o);
+      else
+        tmem_ld64(o_col, o);
+      if (valid) {
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(o_col + c * 32, o);
-        if (valid) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+        for (int c = 0; c < D / 16; ++c) {
+          uint32_t v[8];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            uint4 v4;
-            v4.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv, __uint_as_float(o[8 * k + 1]) * inv);
-            v4.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv);
-            v4.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv);
-            v4.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv);
-            d4[k] = v4;
+          for (int k = 0; k < 8; ++k)
+            v[k] = pack_bf16x2(__uint_as_float(o[16 * c + 2 * k]) * inv,
+                               __uint_as_float(o[16 * c + 2 * k + 1]) * inv);
+          if (p.out_align32) {
+            st_global_v8(dst + 16 * c, v);
+          } else {
+            reinterpret_cast<uint4*>(dst + 16 * c)[0] = make_uint4(v[0], v[1], v[2], v[3]);
+            reinterpret_cast<uint4*>(dst + 16 * c)[1] = make_uint4(v[4], v[5], v[6], v[7]);
           }
         }
       }
@@ -760,6 +767,7 @@ fi_status launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.k_scale = a.cache.k_scale;
   p.v_scale = a.cache.v_scale;
   p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.out_align32 = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0 ? 1 : 0;
   p.lse = a.lse;
   p.qo_indptr = a.qo_indptr_dev;
   p.kv_indptr = a.kv_indptr_dev;
