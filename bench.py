@@ -296,6 +296,7 @@ def time_append_cold(fi, device, n_sets=24, reps=20):
         sum(t.numel() for t in (sets[0][3].k_data, sets[0][3].v_data, sets[0][3].k_sf,
                                  sets[0][3].v_sf))
     s = torch.cuda.Stream(device=device)
+    s.wait_stream(torch.cuda.current_stream(device))  # inputs are made on the current stream
     for k, v, sl, c in sets:
         fi.fi_nvfp4_append(ctx, k, v, ks, vs, sl, c, stream=s)
     s.synchronize()
@@ -455,6 +456,7 @@ def main():
         return 0 if a["status"] == 0 else 1
     runner = PathRunner(fi, args.workload, device, args.seqs)
     stream = torch.cuda.Stream(device=device)
+    stream.wait_stream(torch.cuda.current_stream(device))  # inputs are made on the current stream
     # correctness guard: the step must run clean before it is timed
     runner.step(stream)
     st = runner.status()

@@ -57,7 +57,11 @@ __global__ void div_check_kernel(const float* d_values, unsigned long long* coun
     const uint32_t cb = e2m1x4_from_f32(b, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f) & 0xFu;
     const bool bits_differ = __float_as_uint(a) != __float_as_uint(b);
     const bool exact_range = fabsf(x) >= 0x1p-100f && fabsf(b) >= 0x1p-126f;
-    if (ca != cb) c[1] = 1;
+    // the block-scale division t = amax / RN(6 g) takes this path for
+    // amax >= 2^-100; its E4M3 code must not change either
+    const bool e4_differ =
+        fabsf(x) >= 0x1p-100f && e4m3_from_f32(fabsf(a)) != e4m3_from_f32(fabsf(b));
+    if (ca != cb || e4_differ) c[1] = 1;
     if (bits_differ && exact_range) c[2] = 1;
     if (bits_differ && fabsf(x) < 0x1p-100f) c[3] = 1;
     if (c[1] || c[2]) {

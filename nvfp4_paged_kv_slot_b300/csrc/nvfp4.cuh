@@ -32,32 +32,25 @@ struct Quant16 {
 // a block when d is in [2^-98, 2^100] and amax <= 2^100 d: an element with
 // |x| >= 2^-100 has an exact residual, and one with |x| < 2^-100 has
 // |x/d| < 1/4, where every value within a few ulps encodes to the same E2M1
-// code (0, or 8 for negative inputs).  The sign is restored for zero inputs
-// (-0 stays -0, as an IEEE division gives).  Callers outside that range use
-// the IEEE division itself.
+// code (0, or 8 for negative inputs).  Callers outside that range use the
+// IEEE division itself.
+// Signed zeros: the residual is computed rounding toward -infinity.  An exact
+// residual does not depend on the rounding direction, except that an exact
+// zero comes out as -0 (IEEE 754, section 6.3).  So a zero input x = s0
+// gives q0 = s0, e = -0 and q1 = -0 * r + s0 = s0, the sign an IEEE division
+// gives, and a nonzero input is unaffected (q0 + (-0) = q0).
 __device__ __forceinline__ bool markstein_range_ok(float d, float amax) {
   return d >= 0x1p-98f && d <= 0x1p100f && amax <= d * 0x1p100f;
 }
 
-__device__ __forceinline__ float div_markstein(float x, float d, float r) {
-  const float q0 = __fmul_rn(x, r);
-  const float e = __fmaf_rn(-q0, d, x);
-  const float q1 = __fmaf_rn(e, r, q0);
-  return copysignf(q1, x);
-}
-
-// The same for a pair of elements with paired fp32 arithmetic (each lane one
-// IEEE operation, as above; fma(q0, -d, x) rounds x - q0 d exactly like
-// fma(-q0, d, x)).
+// Two elements with paired fp32 arithmetic (each lane one IEEE operation;
+// fma(q0, -d, x) computes x - q0 d).
 __device__ __forceinline__ void div_markstein_x2(float& x0, float& x1, uint64_t d2n,
                                                  uint64_t r2) {
   const uint64_t x2 = f2_pack(x0, x1);
   const uint64_t q0 = f2_mul(x2, r2);
-  const uint64_t e = f2_fma(q0, d2n, x2);
-  float y0, y1;
-  f2_unpack(f2_fma(e, r2, q0), y0, y1);
-  x0 = copysignf(y0, x0);
-  x1 = copysignf(y1, x1);
+  const uint64_t e = f2_fma_rm(q0, d2n, x2);
+  f2_unpack(f2_fma(e, r2, q0), x0, x1);
 }
 
 // Quantizes one 16-element NVFP4 block with global decode scale g:
@@ -104,6 +97,80 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 w, float* x) {
     x[2 * j] = __uint_as_float(v[j] << 16);
     x[2 * j + 1] = __uint_as_float(v[j] & 0xFFFF0000u);
   }
+}
+
+// Per-tensor constants of the quantizer that depend only on g or on the scale
+// byte, computed once per CTA instead of once per block:
+//   d6 = RN(6 g), r6 = RN(1 / d6), lim6 = d6 * 2^100 when d6 is in the
+//   Markstein range (else -1, which sends every block to the IEEE division);
+//   per E4M3 code s in [0, 127]: d = RN(e4m3(s) g), r = RN(1 / d) and
+//   lim = d * 2^100 when d is in range (else -1).
+// quantize16_tab with these constants stores the same bytes as quantize16.
+struct QuantConsts {
+  float d6, r6, lim6;
+};
+
+__device__ __forceinline__ QuantConsts quant_consts(float g) {
+  QuantConsts c;
+  c.d6 = __fmul_rn(6.0f, g);
+  c.r6 = __frcp_rn(c.d6);
+  c.lim6 = (c.d6 >= 0x1p-98f && c.d6 <= 0x1p100f) ? c.d6 * 0x1p100f : -1.0f;
+  return c;
+}
+
+__device__ __forceinline__ float4 quant_scale_entry(uint32_t s, float g) {
+  const float d = __fmul_rn(e4m3_value(s), g);
+  const float lim = (d >= 0x1p-98f && d <= 0x1p100f) ? d * 0x1p100f : -1.0f;
+  return make_float4(d, __frcp_rn(d), lim, 0.0f);
+}
+
+// max |x| of 16 bf16 values (two 128-bit words) as fp32, computed on the
+// packed halves: exact (a maximum), NaN halves ignored like fmaxf.
+__device__ __forceinline__ float amax16_bf16(const uint4& w0, const uint4& w1) {
+  const uint32_t m = bmax_abs2(bmax_abs2(bmax_abs2(w0.x, w0.y), bmax_abs2(w0.z, w0.w)),
+                               bmax_abs2(bmax_abs2(w1.x, w1.y), bmax_abs2(w1.z, w1.w)));
+  const uint32_t m2 = bmax_abs2(m, __byte_perm(m, 0u, 0x1032));
+  return __uint_as_float((m2 & 0x7FFFu) << 16);
+}
+
+// quantize16 with the constants above.  The block scale t = amax / d6 is
+// also divided by Markstein's method: amax >= 2^-100 makes its residual
+// exact, and a quotient below the fp32 normal range rounds to the E4M3 code 0
+// either way.  tab: the 128 entries of quant_scale_entry for this tensor.
+// Input: the block's 16 bf16 values as two 128-bit words.
+__device__ __forceinline__ Quant16 quantize16_tab(const uint4& w0, const uint4& w1,
+                                                 const QuantConsts& c, const float4* tab) {
+  Quant16 q{0u, 0u, 0u};
+  const float amax = amax16_bf16(w0, w1);
+  if (amax == 0.0f) return q;
+  float t;
+  if (amax >= 0x1p-100f && amax <= c.lim6) {
+    const float q0 = __fmul_rn(amax, c.r6);
+    t = __fmaf_rn(__fmaf_rn(-q0, c.d6, amax), c.r6, q0);
+  } else {
+    t = __fdiv_rn(amax, c.d6);
+  }
+  const uint32_t s = e4m3_from_f32(t);
+  if (s == 0u) return q;  // t >= 0: code 0 is the only zero
+  const float4 e = tab[s & 0x7Fu];
+  float x[16];
+  bf16x8_to_f32(w0, x);
+  bf16x8_to_f32(w1, x + 8);
+  float y[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) y[j] = x[j];
+  if (amax <= e.z) {
+    const uint64_t r2 = f2_pack(e.y, e.y), d2n = f2_pack(-e.x, -e.x);
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) div_markstein_x2(y[j], y[j + 1], d2n, r2);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) y[j] = __fdiv_rn(x[j], e.x);
+  }
+  q.lo = e2m1x4_from_f32(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
+  q.hi = e2m1x4_from_f32(y[8], y[9], y[10], y[11], y[12], y[13], y[14], y[15]);
+  q.s8 = s;
+  return q;
 }
 
 // --- 16-bit staging tile ------------------------------------------------------

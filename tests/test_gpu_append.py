@@ -78,6 +78,78 @@ def test_append_strided_rows_and_edge_blocks(oracle):
     _assert_cache_equal(c, host)
 
 
+@pytest.mark.parametrize("H,D,N,gk,gv", [
+    (72, 128, 37, 1.0, 0.003),          # rows of 9216 elements: the direct kernel
+    (160, 64, 20, 0.5, 2.0),            # the same at D = 64
+    (8, 128, 333, 1e-32, 7e30),         # staged; RN(6 g) outside the Markstein range
+    (2, 64, 1000, 1e-39, 3e-5),         # staged, 32 tokens per stage; subnormal g
+])
+def test_append_wide_rows_ragged_stages_extreme_scales(oracle, H, D, N, gk, gv):
+    """Both append kernels (rows that fit a shared-memory stage and rows that
+    do not), a partial last stage, blocks whose amax is below 2^-100 or far
+    above 1, and global scales on both sides of the fast division's range:
+    the whole cache must equal the oracle's bytes."""
+    m = fi()
+    ps = 16
+    P = (N + ps - 1) // ps + 3
+    g = torch.Generator().manual_seed(H * 1000 + N)
+    x = torch.randn((2, N, H, D), generator=g)
+    mag = torch.tensor([1.0, 1e-33, 1e-20, 1e4, 1e30, 3e-5])
+    pick = torch.randint(0, len(mag), (2, N, H, D // 16, 1), generator=g)
+    x = (x.view(2, N, H, D // 16, 16) * mag[pick]).view(2, N, H, D)
+    kv = x.to(torch.bfloat16)
+    slots = torch.randperm(P * ps, generator=g)[:N].to(torch.int64)
+    slots[:: 7] = -1
+    c = m.NVFP4Cache(P, H, ps, D, fill=0xA5)
+    c.k_scale.fill_(gk)
+    c.v_scale.fill_(gv)
+    ctx = m.fi_context_create()
+    m.fi_nvfp4_append(ctx, kv[0].cuda(), kv[1].cuda(), c.k_scale, c.v_scale, slots.cuda(), c)
+    assert m.fi_device_status(ctx) == 0
+    m.fi_context_destroy(ctx)
+    host = oracle.new_cache(P, H, ps, D)
+    sk = float(np.float32(gk))
+    sv = float(np.float32(gv))
+    assert oracle.append(W.bits(kv[0]), W.bits(kv[1]), sk, sv, slots.numpy(), host) == 0
+    _assert_cache_equal(c, host)
+
+
+@pytest.mark.parametrize("H,D,N,strided", [
+    (8, 128, 70001, False),   # dense token rows: one bulk copy per tensor and stage
+    (4, 64, 66000, True),     # rows of a wider buffer: one bulk copy per token row
+])
+def test_append_long_staged(oracle, H, D, N, strided):
+    """Appends of 65536 tokens or more take the shared-memory staged kernel:
+    whole cache bit-exact against the oracle, with a partial last stage,
+    skipped and repeated-page slots."""
+    m = fi()
+    ps = 16
+    P = (N + ps - 1) // ps + 5
+    g = torch.Generator().manual_seed(N)
+    width = 3 * H * D if strided else H * D
+    base = torch.randn((N, 2 * width), generator=g).to(torch.bfloat16)
+    k = base[:, :H * D].view(N, H, D)
+    v = base[:, width:width + H * D].view(N, H, D)
+    slots = torch.randperm(P * ps, generator=g)[:N].to(torch.int64)
+    slots[::13] = -1
+    c = m.NVFP4Cache(P, H, ps, D, fill=0xA5)
+    c.k_scale.fill_(0.0021)
+    c.v_scale.fill_(0.0017)
+    bd = base.cuda()
+    kd = bd[:, :H * D].view(N, H, D)
+    vd = bd[:, width:width + H * D].view(N, H, D)
+    ctx = m.fi_context_create()
+    m.fi_nvfp4_append(ctx, kd, vd, c.k_scale, c.v_scale, slots.cuda(), c)
+    assert m.fi_device_status(ctx) == 0
+    m.fi_context_destroy(ctx)
+    host = oracle.new_cache(P, H, ps, D)
+    sk = float(np.float32(0.0021))
+    sv = float(np.float32(0.0017))
+    assert oracle.append(W.bits(k.contiguous()), W.bits(v.contiguous()), sk, sv, slots.numpy(),
+                         host) == 0
+    _assert_cache_equal(c, host)
+
+
 @pytest.mark.parametrize("mode", ["eager", "graph"])
 @pytest.mark.parametrize("bad", [0.0, -0.0, -1.0, float("inf"), float("nan")])
 def test_bad_device_scale_sets_flag_and_writes_nothing(mode, bad):

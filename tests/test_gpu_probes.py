@@ -94,7 +94,9 @@ def test_markstein_division_matches_ieee_division(diag, oracle):
     scales and many global scales g, plus log-uniform and edge divisors, the
     quotient must give the IEEE quotient's E2M1 code wherever the quantizer
     uses that path, and its exact bits wherever Markstein's theorem applies
-    (|x| >= 2^-100, normal quotient)."""
+    (|x| >= 2^-100, normal quotient).  The block scale amax / RN(6 g) is
+    divided the same way for amax >= 2^-100: divisors RN(6 g) are included and
+    the E4M3 code of the quotient is compared as well."""
     e4 = np.array([oracle.e4m3_value(c) for c in range(1, 127)], np.float32)
     rng = np.random.default_rng(11)
     gs = np.concatenate([[1.0, 0.0021, 3.7e-5, 1 / 2688.0, 1e-20, 7.5e30, 2.0 ** -60],
@@ -104,7 +106,8 @@ def test_markstein_division_matches_ieee_division(diag, oracle):
     edges = np.array([2.0 ** -98, 2.0 ** 100, np.nextafter(np.float32(2.0 ** -98), np.float32(1)),
                       np.nextafter(np.float32(2.0 ** 100), np.float32(0)), 1.0, 3.0, 448.0],
                      np.float32)
-    d = np.concatenate([ds, extra, edges]).astype(np.float32)
+    d6 = (np.float32(6.0) * gs).astype(np.float32)                      # RN(6 g)
+    d = np.concatenate([ds, d6, extra, edges]).astype(np.float32)
     dv = torch.from_numpy(d).cuda()
     counts = torch.zeros(4, dtype=torch.int64, device="cuda")
     first = torch.zeros(2, dtype=torch.int32, device="cuda")
