@@ -530,7 +530,10 @@ def main():
                      "frac_of_burst_peak": pf_tflops / peak_burst,
                      "ms_per_launch": pf_ms},
         "append_in_step": {"ms_per_launch": ap_ms, "gbs": runner_append_gbs,
-                           "frac": runner_append_gbs / peaks["hbm_gbs"]},
+                           "frac": runner_append_gbs / peaks["hbm_gbs"],
+                           "kernel": "nvfp4_append_staged_kernel",
+                           "traffic": recorded_traffic("append_uniform")
+                           if args.workload == "uniform" and not args.seqs else None},
         "append_bench": app,
         "clocks": clk,
         "e2e": e2e,
