@@ -146,6 +146,11 @@ typedef struct {
   int64_t kv_bytes;       /* NVFP4 bytes of K and V the batch reads */
   int32_t num_ctas;       /* CTAs the run launches (at most; pairs may be fewer) */
   int32_t ctas_per_unit;  /* 2 when units run on CTA pairs, else 1 */
+  int32_t balanced;       /* 1: fewer than 16 units per CTA (pair); each unit,
+                             heaviest first, is assigned to the least-loaded one
+                             (longest-processing-time first); 0: round-robin */
+  int32_t max_slot_tiles; /* balanced plans: KV tiles (plus one per unit) of the
+                             most loaded CTA (pair); 0 otherwise */
 } fi_plan_info;
 
 /* Creates an empty, reusable plan bound to `ctx`. */

@@ -59,7 +59,8 @@ class fi_plan_info(C.Structure):
                 ("is_uniform", C.c_int32), ("global_reverse", C.c_int32),
                 ("q_tiles", C.c_int32), ("heads_per_cta", C.c_int32),
                 ("head_units", C.c_int32), ("num_units", C.c_int64), ("kv_bytes", C.c_int64),
-                ("num_ctas", C.c_int32), ("ctas_per_unit", C.c_int32)]
+                ("num_ctas", C.c_int32), ("ctas_per_unit", C.c_int32),
+                ("balanced", C.c_int32), ("max_slot_tiles", C.c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

@@ -110,7 +110,7 @@ struct fi_plan {
   int next = 0;
   const int32_t* page_table = nullptr;
   int32_t page_table_stride = 0;
-  size_t off_kv = 0, off_work = 0;
+  size_t off_kv = 0, off_work = 0, off_slot_units = 0, off_slot_begin = 0;
 };
 
 extern "C" {
@@ -221,11 +221,13 @@ fi_status fi_prefill_plan(fi_plan* plan, const int32_t* qo_indptr_host,
   plan->page_table = page_table_dev;
   plan->page_table_stride = page_table_stride;
 
-  // Device copy: qo_indptr | kv_indptr | work list.
+  // Device copy: qo_indptr | kv_indptr | work list | slot units | slot begins.
   const size_t nb = static_cast<size_t>(batch) + 1;
   plan->off_kv = nb;
   plan->off_work = (2 * nb + 3) & ~static_cast<size_t>(3);  // 16-byte aligned work list
-  const size_t words = plan->off_work + plan->host.work.size();
+  plan->off_slot_units = plan->off_work + plan->host.work.size();
+  plan->off_slot_begin = plan->off_slot_units + plan->host.slot_units.size();
+  const size_t words = plan->off_slot_begin + plan->host.slot_begin.size();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (words > plan->dev_words) {
     if (plan->dev) cudaFree(plan->dev);  // growth only: amortized
@@ -259,6 +261,12 @@ fi_status fi_prefill_plan(fi_plan* plan, const int32_t* qo_indptr_host,
   if (!plan->host.work.empty())
     std::memcpy(h + plan->off_work, plan->host.work.data(),
                 plan->host.work.size() * sizeof(int32_t));
+  if (!plan->host.slot_units.empty()) {
+    std::memcpy(h + plan->off_slot_units, plan->host.slot_units.data(),
+                plan->host.slot_units.size() * sizeof(int32_t));
+    std::memcpy(h + plan->off_slot_begin, plan->host.slot_begin.data(),
+                plan->host.slot_begin.size() * sizeof(int32_t));
+  }
   if (cudaMemcpyAsync(plan->dev, h, words * sizeof(int32_t), cudaMemcpyHostToDevice, s) !=
       cudaSuccess)
     return FI_ERR_CUDA;
@@ -290,6 +298,10 @@ fi_status fi_prefill_run(const fi_plan* plan, const void* q_dev, const fi_nvfp4_
   a.qo_indptr_dev = plan->dev;
   a.kv_indptr_dev = plan->dev + plan->off_kv;
   a.work_dev = P.work.empty() ? nullptr : plan->dev + plan->off_work;
+  const bool balanced = !P.slot_units.empty();
+  a.slot_units_dev = balanced ? plan->dev + plan->off_slot_units : nullptr;
+  a.slot_begin_dev = balanced ? plan->dev + plan->off_slot_begin : nullptr;
+  a.num_slots = balanced ? static_cast<int32_t>(P.slot_begin.size()) - 1 : 0;
   a.page_table = plan->page_table;
   a.page_table_stride = plan->page_table_stride;
   a.q = q_dev;

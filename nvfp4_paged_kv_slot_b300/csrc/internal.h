@@ -46,7 +46,12 @@ struct HostPlan {
   int32_t uniform_qo_len = 0, uniform_kv_len = 0;
   bool pair = false;              // units run on 2-CTA clusters sharing KV staging
   float sm_scale = 0.0f;
-  std::vector<int32_t> work;      // 4 int32 per unit (ragged batches only)
+  std::vector<int32_t> work;      // 4 int32 per unit (ragged batches, and balanced plans)
+  // Balanced plans (few units per CTA slot): the work-list indices of each
+  // slot's units, heaviest first; slot s runs slot_units[slot_begin[s] ..
+  // slot_begin[s + 1]).  Empty otherwise (units are dealt round-robin).
+  std::vector<int32_t> slot_units;
+  std::vector<int32_t> slot_begin;
 };
 
 // Validates the arguments and plans on the host only (no CUDA calls).
@@ -61,7 +66,10 @@ struct PrefillArgs {
   const HostPlan* plan;
   const int32_t* qo_indptr_dev;
   const int32_t* kv_indptr_dev;
-  const int32_t* work_dev;       // null for uniform batches
+  const int32_t* work_dev;       // null for uniform batches without a work list
+  const int32_t* slot_units_dev; // balanced plans only (else null)
+  const int32_t* slot_begin_dev;
+  int32_t num_slots;
   const int32_t* page_table;
   int32_t page_table_stride;
   const void* q;

@@ -198,6 +198,9 @@ extern "C" fi_status fi_prefill_noalloc(const int32_t* qo_indptr_host,
   a.qo_indptr_dev = scratch + off_qo;
   a.kv_indptr_dev = scratch + off_kv;
   a.work_dev = I.is_uniform ? nullptr : scratch + off_work;
+  a.slot_units_dev = nullptr;  // units dealt round-robin
+  a.slot_begin_dev = nullptr;
+  a.num_slots = 0;
   a.page_table = page_table_dev;
   a.page_table_stride = page_table_stride;
   a.q = q_dev;

@@ -11,9 +11,15 @@
 //    reverse-Q-tile order (the heaviest causal q-tiles of every sequence and
 //    head first); §3 the L2 gate (global order only if 2 * KV bytes fit in L2).
 // Ragged batches get an explicit work list in the same spirit: heaviest first.
+// Plans with few units per persistent CTA (or CTA pair) are balanced: each
+// unit, heaviest first, goes to the least-loaded slot (the longest-processing-
+// time-first rule), since dealing a handful of units round-robin leaves some
+// slots with twice the average work.
 #include <algorithm>
 #include <cstring>
+#include <functional>
 #include <numeric>
+#include <queue>
 
 #include "internal.h"
 
@@ -26,6 +32,45 @@ inline int32_t n_kv_tiles(int32_t qt, int32_t qo_len, int32_t kv_len) {
   const int32_t last_row = std::min(qo_len, (qt + 1) * kTileQ) - 1;
   const int32_t last_key = last_row + (kv_len - qo_len);
   return last_key / kTileKV + 1;
+}
+
+// Plans with fewer units than this per slot are balanced.
+constexpr int64_t kBalanceUnitsPerSlot = 16;
+
+// Longest-processing-time-first assignment of the work list's units to
+// `slots` slots; a unit costs its KV tiles plus one for its Q load and
+// epilogue.
+void balance(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t slots, HostPlan& P) {
+  const int64_t n = static_cast<int64_t>(P.work.size() / 4);
+  std::vector<int32_t> cost(static_cast<size_t>(n));
+  for (int64_t t = 0; t < n; ++t) {
+    const int32_t b = P.work[4 * t + 0], qt = P.work[4 * t + 2];
+    cost[t] = n_kv_tiles(qt, qo_indptr[b + 1] - qo_indptr[b], kv_indptr[b + 1] - kv_indptr[b]) + 1;
+  }
+  std::vector<int32_t> order(static_cast<size_t>(n));
+  std::iota(order.begin(), order.end(), 0);
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int32_t x, int32_t y) { return cost[x] > cost[y]; });
+  using Load = std::pair<int64_t, int32_t>;  // (load, slot): ties go to the lower slot
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+  for (int32_t k = 0; k < slots; ++k) heap.push({0, k});
+  std::vector<int32_t> owner(static_cast<size_t>(n));
+  int64_t max_load = 0;
+  for (int32_t t : order) {
+    const Load top = heap.top();
+    heap.pop();
+    owner[t] = top.second;
+    heap.push({top.first + cost[t], top.second});
+    max_load = std::max(max_load, top.first + cost[t]);
+  }
+  P.info.balanced = 1;
+  P.info.max_slot_tiles = static_cast<int32_t>(std::min<int64_t>(max_load, 0x7FFFFFFF));
+  P.slot_begin.assign(static_cast<size_t>(slots) + 1, 0);
+  for (int32_t t : order) ++P.slot_begin[owner[t] + 1];
+  for (int32_t k = 0; k < slots; ++k) P.slot_begin[k + 1] += P.slot_begin[k];
+  P.slot_units.assign(static_cast<size_t>(n), 0);
+  std::vector<int32_t> fill(P.slot_begin.begin(), P.slot_begin.end() - 1);
+  for (int32_t t : order) P.slot_units[fill[owner[t]]++] = t;  // heaviest first per slot
 }
 
 }  // namespace
@@ -94,11 +139,13 @@ fi_status plan_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t 
   }
 
   const int32_t HU = I.head_units;
+  const int32_t ctas = (opts && opts->num_ctas > 0) ? opts->num_ctas : default_ctas;
   if (I.is_uniform) {
     P.uniform_qo_len = max_qo;
     P.uniform_kv_len = max_kv;
     I.num_units = static_cast<int64_t>(batch) * HU * I.q_tiles;
-    if (want_list) {
+    const int64_t slots = std::max(ctas, I.ctas_per_unit) / I.ctas_per_unit;
+    if (want_list || I.num_units < kBalanceUnitsPerSlot * slots) {
       P.work.resize(static_cast<size_t>(I.num_units) * 4);
       const int64_t BH = static_cast<int64_t>(batch) * HU;
       for (int64_t t = 0; t < I.num_units; ++t) {
@@ -169,10 +216,12 @@ fi_status plan_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t 
       P.work[4 * t + 3] = items[t].cost;
     }
   }
-  const int32_t ctas = (opts && opts->num_ctas > 0) ? opts->num_ctas : default_ctas;
   I.num_ctas = static_cast<int32_t>(std::min<int64_t>(I.num_units * I.ctas_per_unit,
                                                       std::max(ctas, I.ctas_per_unit)));
   if (P.pair) I.num_ctas &= ~1;
+  const int32_t slots = I.num_ctas / I.ctas_per_unit;
+  if (slots > 0 && !P.work.empty() && I.num_units < kBalanceUnitsPerSlot * slots)
+    balance(qo_indptr, kv_indptr, slots, P);
   return FI_OK;
 }
 

@@ -63,6 +63,9 @@ struct PrefillParams {
   const int32_t* qo_indptr;
   const int32_t* kv_indptr;
   const int4* work;
+  const int32_t* slot_units;  // balanced plans: work-list indices grouped by slot
+  const int32_t* slot_begin;  // slot s: slot_units[slot_begin[s] .. slot_begin[s + 1])
+  int32_t num_slots;
   const int32_t* page_table;
   int32_t* status;
   int64_t pt_stride;
@@ -158,6 +161,47 @@ __device__ __forceinline__ Unit decode_unit(const PrefillParams& p, int u, int h
   const int last_row = min(w.qo_len, (w.qt + 1) * kTileQ) - 1;
   w.n_kv = (last_row + w.kv_len - w.qo_len) / kTileKV + 1;
   return w;
+}
+
+// The units one CTA (or CTA pair) runs: round-robin over the unit index
+// (u0, u0 + stride, ...), or, for balanced plans, the units of slots u0,
+// u0 + stride, ... (a launch with fewer CTAs than planned slots runs several
+// slots).  Every role of the CTA walks the same sequence.
+struct UnitCursor {
+  int unit;  // -1 once done
+  int k, end, slot;
+};
+
+__device__ __forceinline__ void unit_seek(const PrefillParams& p, int stride, UnitCursor& c) {
+  for (; c.slot < p.num_slots; c.slot += stride) {
+    c.k = __ldg(p.slot_begin + c.slot);
+    c.end = __ldg(p.slot_begin + c.slot + 1);
+    if (c.k < c.end) {
+      c.unit = __ldg(p.slot_units + c.k);
+      return;
+    }
+  }
+  c.unit = -1;
+}
+
+__device__ __forceinline__ UnitCursor unit_first(const PrefillParams& p, int u0, int stride) {
+  UnitCursor c{u0 < p.num_units ? u0 : -1, 0, 0, u0};
+  if (p.slot_units) unit_seek(p, stride, c);
+  return c;
+}
+
+__device__ __forceinline__ void unit_next(const PrefillParams& p, int stride, UnitCursor& c) {
+  if (p.slot_units) {
+    if (++c.k < c.end) {
+      c.unit = __ldg(p.slot_units + c.k);
+      return;
+    }
+    c.slot += stride;
+    unit_seek(p, stride, c);
+  } else {
+    c.unit += stride;
+    if (c.unit >= p.num_units) c.unit = -1;
+  }
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -281,7 +325,8 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
   auto repack_role = [&](int rt) {
     uint32_t raw_k = 0, stg_k = 0;
     bool ok = true;
-    for (int u = u0; ok && u < p.num_units; u += ustride) {
+    for (UnitCursor uc = unit_first(p, u0, ustride); ok && uc.unit >= 0; unit_next(p, ustride, uc)) {
+      const int u = uc.unit;
       const Unit w = decode_unit(p, u, heads_per_unit, head_off);
       for (int j = 0; ok && j < w.n_kv; ++j) {
         const int valid = min(kTileKV, w.kv_len - j * kTileKV);
@@ -351,7 +396,9 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
     const uint32_t cp_sf = static_cast<uint32_t>(rows_per_copy) * (D / 16);
     const int copies_per_tile = PAIR ? max(pages_per_tile / 2, 1) : pages_per_tile;
     const uint32_t src_row_off = (PAIR && p.page_size == 128) ? 64u * rank : 0u;
-    for (int u = u0; ok && u < p.num_units; u += ustride, ++it) {
+    for (UnitCursor uc = unit_first(p, u0, ustride); ok && uc.unit >= 0;
+         unit_next(p, ustride, uc), ++it) {
+      const int u = uc.unit;
       const Unit w = decode_unit(p, u, heads_per_unit, head_off);
       const int32_t* pt = p.page_table + static_cast<int64_t>(w.b) * p.pt_stride;
       const int seq_pages = (w.kv_len + p.page_size - 1) / p.page_size;
@@ -440,7 +487,9 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
           mma_ts(d_tmem, a_tmem + s * 8, vd + ((s * 2048) >> 4), kIdescPV,
                  (acc || s > 0) ? 1u : 0u);
       };
-      for (int u = u0; ok && u < p.num_units; u += ustride, ++it) {
+      for (UnitCursor uc = unit_first(p, u0, ustride); ok && uc.unit >= 0;
+           unit_next(p, ustride, uc), ++it) {
+        const int u = uc.unit;
         const Unit w = decode_unit(p, u, heads_per_unit, head_off);
         if (!mbar_wait(q_full, it & 1, ab)) { ok = false; break; }
         // K tile 0
@@ -504,7 +553,9 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
       prefetch_tensormap(&p.tmap_q);
       int it = 0;
       int q_issued = -1;  // iteration of the last Q load issued
-      for (int u = u0; u < p.num_units; u += ustride, ++it) {
+      for (UnitCursor uc = unit_first(p, u0, ustride); uc.unit >= 0;
+           unit_next(p, ustride, uc), ++it) {
+        const int u = uc.unit;
         const Unit w = decode_unit(p, u, heads_per_unit, head_off);
         if (!mbar_wait(q_empty, (it & 1) ^ 1, ab)) break;
         mbar_arrive_expect_tx(q_full, NQ * L::kQTile);
@@ -542,7 +593,9 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
     uint32_t sk = 0;
     int it = 0;
     bool ok = true;
-    for (int u = u0; ok && u < p.num_units; u += ustride, ++it) {
+    for (UnitCursor uc = unit_first(p, u0, ustride); ok && uc.unit >= 0;
+         unit_next(p, ustride, uc), ++it) {
+      const int u = uc.unit;
       const Unit w = decode_unit(p, u, heads_per_unit, head_off);
       const int row_q = w.qt * kTileQ + r;
       const int delta = w.kv_len - w.qo_len;
@@ -783,7 +836,10 @@ fi_status launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.group = P.group;
   p.units_per_kv_head = P.units_per_kv_head;
   p.head_units = P.info.head_units;
-  p.uniform = P.info.is_uniform;
+  p.uniform = (P.info.is_uniform && !a.work_dev) ? 1 : 0;  // else: decode from the work list
+  p.slot_units = a.slot_units_dev;
+  p.slot_begin = a.slot_begin_dev;
+  p.num_slots = a.num_slots;
   p.global_reverse = P.info.global_reverse;
   p.uni_qo_len = P.uniform_qo_len;
   p.uni_kv_len = P.uniform_kv_len;

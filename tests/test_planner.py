@@ -171,3 +171,38 @@ def test_workload_shapes():
     assert info["global_reverse"] == 1                                 # 2.4 MB KV fits in L2
     sp = W.spec("ragged")
     assert len(sp.seq_lens) == 256 and min(sp.seq_lens) >= 128 and max(sp.seq_lens) <= 16384
+
+
+def test_balanced_schedule_for_few_units():
+    """A plan with fewer than 16 units per CTA slot assigns units heaviest
+    first to the least-loaded slot.  One 2048-token sequence with 32/8 heads
+    has 128 pair units of 1..16 KV tiles over 74 pair slots: dealt round-robin
+    from a heaviest-first list the first slot would get 16 + 7 tiles; the
+    greedy rule keeps every slot within one unit of the average load."""
+    ind = fi.indptr_from_lens([2048])
+    info, work = fi.fi_prefill_plan_host(ind, ind, 32, 8, 128, 16)
+    assert info["num_units"] == 128 and info["ctas_per_unit"] == 2
+    assert info["balanced"] == 1
+    slots = info["num_ctas"] // info["ctas_per_unit"]
+    # a unit's cost: its KV tiles (q-tile index + 1 for a square causal tile
+    # grid) plus one for its Q load and epilogue
+    costs = [int(w[2]) + 1 + 1 for w in work]
+    avg = sum(costs) / slots
+    # Graham's bound for the greedy rule on a heaviest-first list
+    assert max(costs) <= info["max_slot_tiles"] <= avg + max(costs)
+    assert info["max_slot_tiles"] <= 18
+    # many units per slot: round-robin, no assignment
+    big = fi.indptr_from_lens([1024] * 64)
+    info2, _ = fi.fi_prefill_plan_host(big, big, 32, 8, 128, 16, with_list=False)
+    assert info2["balanced"] == 0 and info2["max_slot_tiles"] == 0
+
+
+def test_balanced_ragged_plan_bounds():
+    rng = np.random.default_rng(5)
+    lens = [int(x) for x in rng.integers(1, 1500, size=6)]
+    ind = fi.indptr_from_lens(lens)
+    info, work = fi.fi_prefill_plan_host(ind, ind, 8, 2, 128, 16)
+    assert info["balanced"] == 1
+    slots = info["num_ctas"] // info["ctas_per_unit"]
+    costs = [int(w[3]) + 1 for w in work]
+    assert max(costs) <= info["max_slot_tiles"] <= sum(costs) / slots + max(costs)
