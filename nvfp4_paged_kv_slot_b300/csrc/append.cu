@@ -104,6 +104,10 @@ __global__ void __launch_bounds__(kAppendThreads, kCtasPerSm)
   constexpr int kTpr = kBlocks / BPT;  // threads per (token, tensor, head) row
   constexpr int kTokPerCta = kAppendThreads / kTpr;
   __shared__ float4 tab[128];
+  // Inputs may come from the previous grid of the stream (programmatic
+  // dependent launch): wait for it, then let the next grid start launching.
+  grid_dep_wait();
+  grid_dep_launch();
 
   // Scale check, once per CTA before any store: a bad scale means no CTA
   // writes anything, for K and V alike.
@@ -194,6 +198,8 @@ template <int D>
 __global__ void __launch_bounds__(kStagedThreads, 1)
     nvfp4_append_staged_kernel(const AppendParams p) {
   constexpr int kBlocks = D / 16;  // 16-element blocks per head row
+  grid_dep_wait();  // inputs may come from the previous grid (see the direct kernel)
+  grid_dep_launch();
   const float ks = p.k_scale_dev ? __ldg(p.k_scale_dev) : p.k_scale_host;
   const float vs = p.v_scale_dev ? __ldg(p.v_scale_dev) : p.v_scale_host;
   if (!scale_ok(ks) || !scale_ok(vs)) {
@@ -393,18 +399,12 @@ fi_status launch_append(const AppendArgs& a, cudaStream_t stream) {
     const int smem = staged_smem_bytes(p.num_stages, p.stage_bytes);
     const int64_t groups = (a.num_tokens + p.tok_per_stage - 1) / p.tok_per_stage;
     const unsigned grid = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(groups, sms)));
-    cudaError_t e;
-    if (D == 128) {
-      e = cudaFuncSetAttribute(nvfp4_append_staged_kernel<128>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e == cudaSuccess) nvfp4_append_staged_kernel<128><<<grid, kStagedThreads, smem, stream>>>(p);
-    } else {
-      e = cudaFuncSetAttribute(nvfp4_append_staged_kernel<64>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e == cudaSuccess) nvfp4_append_staged_kernel<64><<<grid, kStagedThreads, smem, stream>>>(p);
-    }
-    if (e != cudaSuccess) return FI_ERR_CUDA;
-    return cudaGetLastError() == cudaSuccess ? FI_OK : FI_ERR_CUDA;
+    void (*kern)(AppendParams) =
+        D == 128 ? nvfp4_append_staged_kernel<128> : nvfp4_append_staged_kernel<64>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return FI_ERR_CUDA;
+    return launch_pdl(kern, dim3(grid), dim3(kStagedThreads), smem, stream, p);
   }
   const int tok_per_cta = kAppendThreads / (D / 16 / kDirectBlocksPerThread);
   const int64_t groups = (a.num_tokens + tok_per_cta - 1) / tok_per_cta;
@@ -417,12 +417,9 @@ fi_status launch_append(const AppendArgs& a, cudaStream_t stream) {
   const int64_t per_cta = (groups + want - 1) / want;
   const int64_t gx = std::max<int64_t>(1, (groups + per_cta - 1) / per_cta);
   const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
-  if (D == 128) {
-    nvfp4_append_kernel<128, kDirectBlocksPerThread><<<grid, kAppendThreads, 0, stream>>>(p);
-  } else {
-    nvfp4_append_kernel<64, kDirectBlocksPerThread><<<grid, kAppendThreads, 0, stream>>>(p);
-  }
-  return cudaGetLastError() == cudaSuccess ? FI_OK : FI_ERR_CUDA;
+  void (*kern)(AppendParams) = D == 128 ? nvfp4_append_kernel<128, kDirectBlocksPerThread>
+                                         : nvfp4_append_kernel<64, kDirectBlocksPerThread>;
+  return launch_pdl(kern, grid, dim3(kAppendThreads), 0, stream, p);
 }
 
 }  // namespace fi

@@ -37,6 +37,30 @@ struct AppendArgs {
 };
 fi_status launch_append(const AppendArgs& a, cudaStream_t stream);
 
+// Launches `kern` as a programmatic dependent of the stream's previous grid:
+// it may start while that grid finishes and waits for it with
+// griddepcontrol.wait before touching memory (extra attributes, e.g. a
+// cluster shape, are added by the caller through `more`).
+template <typename Params>
+fi_status launch_pdl(void (*kern)(Params), dim3 grid, dim3 block, int smem, cudaStream_t stream,
+                     const Params& p, const cudaLaunchAttribute* more = nullptr, int n_more = 0) {
+  cudaLaunchAttribute attrs[4];
+  int n = 0;
+  attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  for (int k = 0; k < n_more && n < 4; ++k) attrs[n++] = more[k];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cfg.attrs = attrs;
+  cfg.numAttrs = static_cast<unsigned>(n);
+  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return FI_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? FI_OK : FI_ERR_CUDA;
+}
+
 // ---- planner ---------------------------------------------------------------
 struct HostPlan {
   fi_plan_info info{};

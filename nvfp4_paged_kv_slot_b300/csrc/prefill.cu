@@ -318,6 +318,11 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const AbortState ab{abort_flag, p.status, kTimeoutNs, FI_DEV_WAIT_TIMEOUT};
+  // Everything above overlaps the previous grid of the stream when this one
+  // is launched as its programmatic dependent; every input (Q, the cache
+  // the append wrote, the plan, the page table) is read after this wait.
+  grid_dep_wait();
+  grid_dep_launch();
 
   const int wg = threadIdx.x / 128;
   // Repack: raw FP4 tiles -> 16-bit staging tiles, by kRepackThreads threads
@@ -771,34 +776,29 @@ fi_status launch_impl(const PrefillParams& p, int grid, cudaStream_t stream) {
   if (cudaFuncGetAttributes(&attr, kern) != cudaSuccess) return FI_ERR_CUDA;
   if (128 * (attr.numRegs + L::kRegRepack + NQ * L::kRegSoftmax) > attr.numRegs * L::kThreads)
     return FI_ERR_UNSUPPORTED;
-  if (!PAIR) {
-    kern<<<grid, L::kThreads, smem, stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? FI_OK : FI_ERR_CUDA;
-  }
-  cudaLaunchConfig_t cfg = {};
+  if (!PAIR) return launch_pdl(kern, dim3(grid), dim3(L::kThreads), smem, stream, p);
   cudaLaunchAttribute cl[1];
   cl[0].id = cudaLaunchAttributeClusterDimension;
   cl[0].val.clusterDim.x = 2;
   cl[0].val.clusterDim.y = 1;
   cl[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(L::kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cfg.attrs = cl;
-  cfg.numAttrs = 1;
   // as many pairs as can be resident at once (persistent), at most one per unit
   static int max_clusters = 0;
   if (max_clusters == 0) {
+    cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * 74);
+    cfg.blockDim = dim3(L::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = cl;
+    cfg.numAttrs = 1;
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0)
       return FI_ERR_CUDA;
     max_clusters = n;
   }
   const int pairs = std::max(1, std::min(grid / 2, max_clusters));
-  cfg.gridDim = dim3(2 * pairs);
-  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return FI_ERR_CUDA;
-  return cudaGetLastError() == cudaSuccess ? FI_OK : FI_ERR_CUDA;
+  return launch_pdl(kern, dim3(2 * pairs), dim3(L::kThreads), smem, stream, p, cl, 1);
 }
 
 }  // namespace

@@ -20,6 +20,17 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// ---------------------------------------------------------------- PDL
+// Programmatic dependent launch.  grid_dep_wait returns once every grid this
+// launch depends on has completed and its memory is visible (at once when
+// the launch has no such dependency); grid_dep_launch lets the next grid of
+// the stream, if launched as a programmatic dependent, start its own prologue
+// (its grid_dep_wait still waits for this grid to complete).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
