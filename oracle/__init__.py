@@ -58,6 +58,20 @@ def lib():
                                   C.c_double, C.c_double, C.c_double, C.c_void_p, C.c_int64,
                                   _f64p, _f64p, C.c_int32]
         L.orc_prefill.restype = C.c_int
+        L.orc_prefill_fmt.argtypes = [_u16p, C.c_int32, _i32p, _i32p, _i32p, C.c_int32, C.c_int32,
+                                      C.c_int32, C.c_int32, C.c_int32, C.c_int32, _u8p, _u8p,
+                                      C.c_void_p, C.c_void_p, C.c_double, C.c_double, C.c_double,
+                                      C.c_void_p, C.c_int64, _f64p, _f64p, C.c_int32]
+        L.orc_prefill_fmt.restype = C.c_int
+        L.orc_fp8_quantize.argtypes = [C.c_float, C.c_float]
+        L.orc_fp8_quantize.restype = C.c_uint8
+        L.orc_fp8_append.argtypes = [_u16p, _u16p, C.c_int64, C.c_int64, C.c_int64, C.c_int32,
+                                     C.c_int32, C.c_float, C.c_float, _i64p, _u8p, _u8p,
+                                     C.c_int32, C.c_int32]
+        L.orc_fp8_append.restype = C.c_int
+        L.orc_fp8_dequant_row.argtypes = [_u8p, C.c_int32, C.c_int32, C.c_int32, C.c_int64,
+                                          C.c_int32, C.c_double, _f64p]
+        L.orc_fp8_dequant_row.restype = None
         L.orc_dense_causal.argtypes = [_f64p, _f64p, _f64p, C.c_int32, C.c_int32, C.c_int32,
                                        C.c_double, _f64p, _f64p]
         L.orc_dense_causal.restype = None
@@ -169,11 +183,47 @@ def dequant_row(cache: dict, which: str, slot: int, head: int, g: float) -> np.n
     return out
 
 
+# --- FP8 (E4M3) paged KV variant ---------------------------------------------
+def fp8_quantize(x: float, g: float) -> int:
+    """E4M3 code of RN32(x / g) (x, g taken as fp32)."""
+    return int(lib().orc_fp8_quantize(float(np.float32(x)), float(np.float32(g))))
+
+
+def new_fp8_cache(num_pages: int, num_kv_heads: int, page_size: int, head_dim: int,
+                  fill: int = 0xA5) -> dict:
+    """Host FP8 cache arrays [P][H_kv][ps][D], pre-filled with `fill`."""
+    shape = (num_pages, num_kv_heads, page_size, head_dim)
+    return {"format": "fp8", "k_data": np.full(shape, fill, np.uint8),
+            "v_data": np.full(shape, fill, np.uint8), "num_pages": num_pages,
+            "num_kv_heads": num_kv_heads, "page_size": page_size, "head_dim": head_dim}
+
+
+def fp8_append(k_bits: np.ndarray, v_bits: np.ndarray, k_scale: float, v_scale: float,
+               slot_mapping: np.ndarray, cache: dict) -> int:
+    """k_bits, v_bits: uint16 [N][H_kv][D] (contiguous).  Mutates `cache`."""
+    k = np.ascontiguousarray(k_bits, dtype=np.uint16)
+    v = np.ascontiguousarray(v_bits, dtype=np.uint16)
+    n, h, d = k.shape
+    slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    return lib().orc_fp8_append(k.reshape(-1), v.reshape(-1), n, h * d, h * d, h, d,
+                                float(np.float32(k_scale)), float(np.float32(v_scale)), slots,
+                                cache["k_data"].reshape(-1), cache["v_data"].reshape(-1),
+                                cache["num_pages"], cache["page_size"])
+
+
+def fp8_dequant_row(cache: dict, which: str, slot: int, head: int, g: float) -> np.ndarray:
+    out = np.empty(cache["head_dim"], np.float64)
+    lib().orc_fp8_dequant_row(cache[f"{which}_data"].reshape(-1), cache["num_kv_heads"],
+                              cache["head_dim"], cache["page_size"], slot, head, g, out)
+    return out
+
+
 # --- attention --------------------------------------------------------------
 def prefill(q_bits: np.ndarray, qo_indptr, kv_indptr, page_table: np.ndarray, cache: dict,
             num_qo_heads: int, k_scale: float, v_scale: float, sm_scale: float,
             rows: np.ndarray | None = None, threads: int = 0):
-    """q_bits: uint16 [total_q][H_q][D].  Returns (out [n][D], lse [n]) in fp64,
+    """q_bits: uint16 [total_q][H_q][D]; cache: an NVFP4 cache (new_cache) or an
+    FP8 one (new_fp8_cache).  Returns (out [n][D], lse [n]) in fp64,
     n = total_q*H_q (row r = token r // H_q, head r % H_q) or len(rows)."""
     q = np.ascontiguousarray(q_bits, dtype=np.uint16).reshape(-1)
     qo = np.ascontiguousarray(qo_indptr, dtype=np.int32)
@@ -190,12 +240,15 @@ def prefill(q_bits: np.ndarray, qo_indptr, kv_indptr, page_table: np.ndarray, ca
         rows_ptr = rows_arr.ctypes.data_as(C.c_void_p)
     out = np.empty((n, d), np.float64)
     lse = np.empty(n, np.float64)
-    rc = lib().orc_prefill(q, batch, qo, kv, pt.reshape(-1), pt.shape[1] if pt.ndim == 2 else 0,
-                           num_qo_heads, cache["num_kv_heads"], d, cache["page_size"],
-                           cache["k_data"].reshape(-1), cache["v_data"].reshape(-1),
-                           cache["k_sf"].reshape(-1), cache["v_sf"].reshape(-1),
-                           float(k_scale), float(v_scale), float(sm_scale), rows_ptr, n,
-                           out.reshape(-1), lse, threads)
+    fp8 = cache.get("format") == "fp8"
+    rc = lib().orc_prefill_fmt(q, batch, qo, kv, pt.reshape(-1),
+                               pt.shape[1] if pt.ndim == 2 else 0, num_qo_heads,
+                               cache["num_kv_heads"], d, cache["page_size"], 1 if fp8 else 0,
+                               cache["k_data"].reshape(-1), cache["v_data"].reshape(-1),
+                               None if fp8 else cache["k_sf"].ctypes.data_as(C.c_void_p),
+                               None if fp8 else cache["v_sf"].ctypes.data_as(C.c_void_p),
+                               float(k_scale), float(v_scale), float(sm_scale), rows_ptr, n,
+                               out.reshape(-1), lse, threads)
     if rc != 0:
         raise ValueError("oracle prefill: invalid arguments")
     return out, lse

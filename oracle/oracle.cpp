@@ -255,6 +255,51 @@ void orc_dequant_row(const uint8_t* data, const uint8_t* sf, int32_t num_kv_head
   }
 }
 
+// FP8 (E4M3) paged KV: every element is divided by the tensor's decode scale
+// (one fp32 IEEE division) and rounded to the nearest E4M3 value by the
+// exhaustive encoder above (ties to even, saturating at 448, sign kept).
+uint8_t orc_fp8_quantize(float x, float g) { return orc_e4m3_encode(x / g); }
+
+int orc_fp8_append(const uint16_t* k, const uint16_t* v, int64_t num_tokens,
+                   int64_t k_tok_stride, int64_t v_tok_stride, int32_t num_kv_heads,
+                   int32_t head_dim, float k_scale, float v_scale,
+                   const int64_t* slot_mapping, uint8_t* k_data, uint8_t* v_data,
+                   int32_t num_pages, int32_t page_size) {
+  int status = 0;
+  if (!(std::isfinite(k_scale) && k_scale > 0.0f)) status |= ORC_BAD_K_SCALE;
+  if (!(std::isfinite(v_scale) && v_scale > 0.0f)) status |= ORC_BAD_V_SCALE;
+  if (status != 0) return status;
+  const int64_t num_slots = static_cast<int64_t>(num_pages) * page_size;
+  for (int64_t i = 0; i < num_tokens; ++i) {
+    int64_t slot = slot_mapping[i];
+    if (slot < 0) continue;
+    if (slot >= num_slots) {
+      status |= ORC_SLOT_OOB;
+      continue;
+    }
+    int64_t page = slot / page_size;
+    int64_t off = slot % page_size;
+    for (int32_t h = 0; h < num_kv_heads; ++h) {
+      int64_t row = (page * num_kv_heads + h) * page_size + off;
+      for (int32_t e = 0; e < head_dim; ++e) {
+        k_data[row * head_dim + e] =
+            orc_fp8_quantize(bf16_to_float(k[i * k_tok_stride + h * head_dim + e]), k_scale);
+        v_data[row * head_dim + e] =
+            orc_fp8_quantize(bf16_to_float(v[i * v_tok_stride + h * head_dim + e]), v_scale);
+      }
+    }
+  }
+  return status;
+}
+
+void orc_fp8_dequant_row(const uint8_t* data, int32_t num_kv_heads, int32_t head_dim,
+                         int32_t page_size, int64_t slot, int32_t head, double g, double* out) {
+  int64_t page = slot / page_size;
+  int64_t off = slot % page_size;
+  int64_t row = (page * num_kv_heads + head) * page_size + off;
+  for (int32_t e = 0; e < head_dim; ++e) out[e] = orc_e4m3_value(data[row * head_dim + e]) * g;
+}
+
 void orc_dense_causal(const double* q, const double* k, const double* v, int32_t L_q,
                       int32_t L_kv, int32_t head_dim, double sm_scale, double* out,
                       double* lse) {
@@ -294,6 +339,19 @@ int orc_prefill(const uint16_t* q, int32_t batch, const int32_t* qo_indptr,
                 const uint8_t* k_sf, const uint8_t* v_sf, double k_scale, double v_scale,
                 double sm_scale, const int64_t* rows, int64_t n_rows, double* out,
                 double* lse, int32_t threads) {
+  return orc_prefill_fmt(q, batch, qo_indptr, kv_indptr, page_table, pt_stride, num_qo_heads,
+                         num_kv_heads, head_dim, page_size, 0, k_data, v_data, k_sf, v_sf,
+                         k_scale, v_scale, sm_scale, rows, n_rows, out, lse, threads);
+}
+
+int orc_prefill_fmt(const uint16_t* q, int32_t batch, const int32_t* qo_indptr,
+                    const int32_t* kv_indptr, const int32_t* page_table, int32_t pt_stride,
+                    int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                    int32_t page_size, int32_t kv_format, const uint8_t* k_data,
+                    const uint8_t* v_data, const uint8_t* k_sf, const uint8_t* v_sf,
+                    double k_scale, double v_scale, double sm_scale, const int64_t* rows,
+                    int64_t n_rows, double* out, double* lse, int32_t threads) {
+  if (kv_format != 0 && kv_format != 1) return -1;
   if (batch < 0 || num_kv_heads <= 0 || num_qo_heads % num_kv_heads != 0) return -1;
   for (int32_t b = 0; b < batch; ++b) {
     int32_t qo_len = qo_indptr[b + 1] - qo_indptr[b];
@@ -341,10 +399,17 @@ int orc_prefill(const uint16_t* q, int32_t batch, const int32_t* qo_indptr,
     for (int32_t j = 0; j < kv_len; ++j) {
       int64_t page = page_table[static_cast<int64_t>(b) * pt_stride + j / page_size];
       int64_t slot = page * page_size + j % page_size;
-      orc_dequant_row(k_data, k_sf, num_kv_heads, head_dim, page_size, slot, hk, k_scale,
-                      &kd[static_cast<size_t>(j) * head_dim]);
-      orc_dequant_row(v_data, v_sf, num_kv_heads, head_dim, page_size, slot, hk, v_scale,
-                      &vd[static_cast<size_t>(j) * head_dim]);
+      if (kv_format == 1) {
+        orc_fp8_dequant_row(k_data, num_kv_heads, head_dim, page_size, slot, hk, k_scale,
+                            &kd[static_cast<size_t>(j) * head_dim]);
+        orc_fp8_dequant_row(v_data, num_kv_heads, head_dim, page_size, slot, hk, v_scale,
+                            &vd[static_cast<size_t>(j) * head_dim]);
+      } else {
+        orc_dequant_row(k_data, k_sf, num_kv_heads, head_dim, page_size, slot, hk, k_scale,
+                        &kd[static_cast<size_t>(j) * head_dim]);
+        orc_dequant_row(v_data, v_sf, num_kv_heads, head_dim, page_size, slot, hk, v_scale,
+                        &vd[static_cast<size_t>(j) * head_dim]);
+      }
     }
 #pragma omp parallel for schedule(dynamic, 4)
     for (int64_t idx = start; idx < end; ++idx) {

@@ -19,6 +19,10 @@
  *   OCP Microscaling Formats (MX) v1.0 — the bit formats of E2M1 and E4M3 (the
  *           pages name NVFP4 but never spell out its bits).
  *
+ * The FP8 (E4M3) paged-KV variant (the pages measure FP8 attention but give
+ * no FP8 cache format): one E4M3 code per element, code = e4m3(x / g) with one
+ * fp32 decode scale g per tensor, pages [P][H_kv][ps][D] bytes (a reading).
+ *
  * Readings where the pages are silent (all listed in the design notes):
  *   - codes and scales are rounded to nearest, ties to the even code, with
  *     saturation to the largest finite magnitude and the sign kept (-0.2 -> -0);
@@ -80,6 +84,21 @@ void orc_dequant_row(const uint8_t* data, const uint8_t* sf, int32_t num_kv_head
                      int32_t head_dim, int32_t page_size, int64_t slot, int32_t head,
                      double g, double* out);
 
+/* --- FP8 (E4M3) paged KV variant ------------------------------------- */
+/* One E4M3 code per head-dim element, HND pages [P][H_kv][ps][D] bytes, and
+ * one positive finite fp32 decode scale g per tensor (k_scale / v_scale):
+ *   code = e4m3(x / g)   (fp32 IEEE division, then nearest even, saturating
+ *                         to +-448, sign kept; NaN gives the NaN code)
+ *   value = e4m3(code) * g. */
+uint8_t orc_fp8_quantize(float x, float g);
+int orc_fp8_append(const uint16_t* k, const uint16_t* v, int64_t num_tokens,
+                   int64_t k_tok_stride, int64_t v_tok_stride, int32_t num_kv_heads,
+                   int32_t head_dim, float k_scale, float v_scale,
+                   const int64_t* slot_mapping, uint8_t* k_data, uint8_t* v_data,
+                   int32_t num_pages, int32_t page_size);
+void orc_fp8_dequant_row(const uint8_t* data, int32_t num_kv_heads, int32_t head_dim,
+                         int32_t page_size, int64_t slot, int32_t head, double g, double* out);
+
 /* --- causal batched prefill over the paged cache (fp64) --------------- */
 /* q: bf16 bits [total_q][H_q][D].  page_table: [B][pt_stride] int32.
  * rows == NULL: every (token, q head) row; else n_rows pairs
@@ -94,6 +113,16 @@ int orc_prefill(const uint16_t* q, int32_t batch, const int32_t* qo_indptr,
                 const uint8_t* k_sf, const uint8_t* v_sf, double k_scale, double v_scale,
                 double sm_scale, const int64_t* rows, int64_t n_rows, double* out,
                 double* lse, int32_t threads);
+
+/* The same over either cache format: kv_format 0 = NVFP4 (k_sf, v_sf used),
+ * 1 = FP8 (k_sf, v_sf ignored). */
+int orc_prefill_fmt(const uint16_t* q, int32_t batch, const int32_t* qo_indptr,
+                    const int32_t* kv_indptr, const int32_t* page_table, int32_t pt_stride,
+                    int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                    int32_t page_size, int32_t kv_format, const uint8_t* k_data,
+                    const uint8_t* v_data, const uint8_t* k_sf, const uint8_t* v_sf,
+                    double k_scale, double v_scale, double sm_scale, const int64_t* rows,
+                    int64_t n_rows, double* out, double* lse, int32_t threads);
 
 /* Dense causal attention on already-dequantized K/V (no pages), one head:
  * q [L_q][D] (double), k/v [L_kv][D] (double).  Used to pin the paged path. */
