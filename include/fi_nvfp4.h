@@ -128,6 +128,8 @@ typedef struct {
   int64_t l2_bytes; /* L2 size for the gate; 0 = the device's */
   int32_t cta_pairs; /* 0: GQA groups of a multiple of 4 query heads run on 2-CTA
                         clusters that share their KV staging tiles; 1: never */
+  int32_t kv_format; /* cache the runs read: 0 NVFP4 (fi_prefill_run), 1 FP8
+                        (fi_prefill_run_fp8); sets the KV bytes of the L2 gate */
 } fi_plan_options;
 
 /* What the planner decided (host values). */
@@ -194,6 +196,40 @@ fi_status fi_plan_get_info(const fi_plan* plan, fi_plan_info* info);
  * Head counts, head_dim and page_size must match the plan. */
 fi_status fi_prefill_run(const fi_plan* plan, const void* q_dev, const fi_nvfp4_cache* cache,
                          void* out_dev, float* lse_dev, void* stream);
+
+/* ---- FP8 (E4M3) paged KV variant --------------------------------------
+ * The same paged layout with one E4M3 code per element and no block scales
+ * (a reading: the pages measure FP8 attention ([#3575]) but give no FP8
+ * cache format):
+ *   data uint8 [num_pages][num_kv_heads][page_size][head_dim], per tensor;
+ *   value = e4m3(code) * g, code = e4m3(x / g) (one fp32 IEEE division, then
+ *   nearest even, saturating to +-448, sign kept), g the tensor's positive
+ *   finite fp32 decode scale.  Both arrays 16-byte aligned. */
+typedef struct {
+  uint8_t* k_data;
+  uint8_t* v_data;
+  const float* k_scale;
+  const float* v_scale;
+  int32_t num_pages;
+  int32_t page_size;    /* 16, 32, 64 or 128 */
+  int32_t num_kv_heads;
+  int32_t head_dim;     /* 64 or 128 */
+} fi_fp8_cache;
+
+/* Quantize-append into the FP8 cache; arguments, scale checks, status bits
+ * and error behaviour as fi_nvfp4_append. */
+fi_status fi_fp8_append(fi_context* ctx, const void* k_dev, const void* v_dev,
+                        int64_t num_tokens, int64_t k_tok_stride, int64_t v_tok_stride,
+                        const float* k_scale_dev, const float* v_scale_dev,
+                        const int64_t* slot_mapping_dev, const fi_fp8_cache* cache,
+                        void* stream);
+
+/* Runs a plan made with kv_format = 1 over the FP8 cache: each KV tile is
+ * converted once into the same 16-bit staging tiles; everything else as
+ * fi_prefill_run.  A plan made for the other format returns
+ * FI_ERR_INVALID_ARGUMENT. */
+fi_status fi_prefill_run_fp8(const fi_plan* plan, const void* q_dev, const fi_fp8_cache* cache,
+                             void* out_dev, float* lse_dev, void* stream);
 
 /* Host-only planning, for inspection and tests: fills `info` and, if
  * `work_out` is non-NULL, up to `work_capacity` work units as 4 int32 each

@@ -38,7 +38,8 @@ FI_DEV_WAIT_TIMEOUT = 16
 EXPORTED = ("fi_context_create", "fi_context_destroy", "fi_nvfp4_append",
             "fi_nvfp4_append_host_scale", "fi_plan_create", "fi_plan_destroy",
             "fi_prefill_plan", "fi_plan_get_info", "fi_prefill_run", "fi_prefill_plan_host",
-            "fi_device_status", "fi_status_string", "fi_version", "fi_prefill_noalloc")
+            "fi_device_status", "fi_status_string", "fi_version", "fi_prefill_noalloc",
+            "fi_fp8_append", "fi_prefill_run_fp8")
 
 
 class fi_nvfp4_cache(C.Structure):
@@ -50,7 +51,13 @@ class fi_nvfp4_cache(C.Structure):
 
 class fi_plan_options(C.Structure):
     _fields_ = [("schedule", C.c_int32), ("num_ctas", C.c_int32), ("l2_bytes", C.c_int64),
-                ("cta_pairs", C.c_int32)]
+                ("cta_pairs", C.c_int32), ("kv_format", C.c_int32)]
+
+
+class fi_fp8_cache(C.Structure):
+    _fields_ = [("k_data", C.c_void_p), ("v_data", C.c_void_p), ("k_scale", C.c_void_p),
+                ("v_scale", C.c_void_p), ("num_pages", C.c_int32), ("page_size", C.c_int32),
+                ("num_kv_heads", C.c_int32), ("head_dim", C.c_int32)]
 
 
 class fi_plan_info(C.Structure):
@@ -74,6 +81,9 @@ _sigs = {
                         C.POINTER(fi_nvfp4_cache), _vp],
     "fi_nvfp4_append_host_scale": [_vp, _vp, _vp, _i64, _i64, _i64, _f32, _f32, _vp,
                                    C.POINTER(fi_nvfp4_cache), _vp],
+    "fi_fp8_append": [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp, _vp,
+                      C.POINTER(fi_fp8_cache), _vp],
+    "fi_prefill_run_fp8": [_vp, _vp, C.POINTER(fi_fp8_cache), _vp, _vp, _vp],
     "fi_plan_create": [_vp, C.POINTER(_vp)],
     "fi_plan_destroy": [_vp],
     "fi_prefill_plan": [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _f32,
@@ -172,6 +182,30 @@ class NVFP4Cache:
                               self.num_pages, self.page_size, self.num_kv_heads, self.head_dim)
 
 
+class FP8Cache:
+    """Device tensors of one FP8 (E4M3) paged KV cache, [P][H_kv][ps][D] bytes
+    per tensor (see the C header), and the ctypes view passed to the library."""
+
+    def __init__(self, num_pages, num_kv_heads, page_size, head_dim, device="cuda",
+                 k_scale=None, v_scale=None, fill=None):
+        import torch
+        shape = (num_pages, num_kv_heads, page_size, head_dim)
+        mk = (lambda: torch.full(shape, fill, dtype=torch.uint8, device=device)) \
+            if fill is not None else (lambda: torch.empty(shape, dtype=torch.uint8, device=device))
+        self.k_data, self.v_data = mk(), mk()
+        self.k_scale = torch.ones(1, dtype=torch.float32, device=device) if k_scale is None \
+            else k_scale
+        self.v_scale = torch.ones(1, dtype=torch.float32, device=device) if v_scale is None \
+            else v_scale
+        self.num_pages, self.num_kv_heads = num_pages, num_kv_heads
+        self.page_size, self.head_dim = page_size, head_dim
+
+    def c(self) -> fi_fp8_cache:
+        return fi_fp8_cache(self.k_data.data_ptr(), self.v_data.data_ptr(),
+                            self.k_scale.data_ptr(), self.v_scale.data_ptr(),
+                            self.num_pages, self.page_size, self.num_kv_heads, self.head_dim)
+
+
 # --- entry points (same names as the C ABI) ------------------------------------
 def fi_context_create():
     h = C.c_void_p()
@@ -227,14 +261,14 @@ def fi_plan_destroy(plan):
 
 def fi_prefill_plan(plan, qo_indptr, kv_indptr, page_table, num_qo_heads, num_kv_heads,
                     head_dim, page_size, sm_scale=0.0, schedule=0, num_ctas=0, l2_bytes=0,
-                    cta_pairs=0, stream=None):
+                    cta_pairs=0, stream=None, kv_format=0):
     """qo_indptr, kv_indptr: host int32 [B+1] (other integer types are
     converted); page_table: device int32 [B][stride]."""
     qo = _host_i32(qo_indptr)
     kv = _host_i32(kv_indptr)
     if qo.size != kv.size or qo.size < 1:
         raise ValueError("qo_indptr and kv_indptr must both have batch+1 entries")
-    opts = fi_plan_options(schedule, num_ctas, l2_bytes, cta_pairs)
+    opts = fi_plan_options(schedule, num_ctas, l2_bytes, cta_pairs, kv_format)
     _check(lib.fi_prefill_plan(plan, qo.ctypes.data, kv.ctypes.data, qo.size - 1,
                                _ptr(page_table), page_table.stride(0) if page_table is not None
                                else 0, num_qo_heads, num_kv_heads, head_dim, page_size,
@@ -259,13 +293,35 @@ def fi_prefill_run(plan, q, cache: NVFP4Cache, out, lse=None, stream=None):
                               _stream(stream)), "fi_prefill_run")
 
 
+def fi_fp8_append(ctx, k, v, k_scale, v_scale, slot_mapping, cache: FP8Cache, stream=None):
+    """FP8 (E4M3) append; arguments as fi_nvfp4_append."""
+    import torch
+    n, ks, vs = _kv_args(k, v)
+    if slot_mapping.dtype != torch.int64:
+        raise ValueError("slot_mapping must be int64")
+    cc = cache.c()
+    _check(lib.fi_fp8_append(ctx, _ptr(k), _ptr(v), n, ks, vs, _ptr(k_scale), _ptr(v_scale),
+                             _ptr(slot_mapping), C.byref(cc), _stream(stream)), "fi_fp8_append")
+
+
+def fi_prefill_run_fp8(plan, q, cache: FP8Cache, out, lse=None, stream=None):
+    """Prefill over the FP8 cache with a plan made with kv_format=1."""
+    import torch
+    for name, t in (("q", q), ("out", out)):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 tensor")
+    cc = cache.c()
+    _check(lib.fi_prefill_run_fp8(plan, _ptr(q), C.byref(cc), _ptr(out), _ptr(lse),
+                                  _stream(stream)), "fi_prefill_run_fp8")
+
+
 def fi_prefill_plan_host(qo_indptr, kv_indptr, num_qo_heads, num_kv_heads, head_dim, page_size,
                          l2_bytes=126 * 2**20, schedule=0, num_ctas=0, with_list=True,
-                         cta_pairs=0):
+                         cta_pairs=0, kv_format=0):
     """Host-only planning (no CUDA): returns (info dict, work [units][4] int32)."""
     qo = _host_i32(qo_indptr)
     kv = _host_i32(kv_indptr)
-    opts = fi_plan_options(schedule, num_ctas, l2_bytes, cta_pairs)
+    opts = fi_plan_options(schedule, num_ctas, l2_bytes, cta_pairs, kv_format)
     info = fi_plan_info()
     _check(lib.fi_prefill_plan_host(qo.ctypes.data, kv.ctypes.data, qo.size - 1, num_qo_heads,
                                     num_kv_heads, head_dim, page_size, l2_bytes, C.byref(opts),

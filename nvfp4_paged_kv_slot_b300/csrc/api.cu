@@ -16,10 +16,11 @@ namespace fi {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-bool cache_ok(const fi_nvfp4_cache* c) {
-  if (!c || !c->k_data || !c->v_data || !c->k_sf || !c->v_sf) return false;
-  if (!aligned16(c->k_data) || !aligned16(c->v_data) || !aligned16(c->k_sf) ||
-      !aligned16(c->v_sf))
+bool cache_ok(const fi_nvfp4_cache* c, int kv_format) {
+  if (!c || !c->k_data || !c->v_data) return false;
+  if (!aligned16(c->k_data) || !aligned16(c->v_data)) return false;
+  if (kv_format == 0 &&
+      (!c->k_sf || !c->v_sf || !aligned16(c->k_sf) || !aligned16(c->v_sf)))
     return false;
   if (c->num_pages <= 0 || c->num_kv_heads <= 0) return false;
   return true;
@@ -46,11 +47,27 @@ fi_status cache_supported(const fi_nvfp4_cache* c) {
   return FI_OK;
 }
 
+// The FP8 cache as the common cache description (no block scales).
+fi_nvfp4_cache fp8_view(const fi_fp8_cache* c) {
+  fi_nvfp4_cache v{};
+  v.k_data = c->k_data;
+  v.v_data = c->v_data;
+  v.k_sf = nullptr;
+  v.v_sf = nullptr;
+  v.k_scale = c->k_scale;
+  v.v_scale = c->v_scale;
+  v.num_pages = c->num_pages;
+  v.page_size = c->page_size;
+  v.num_kv_heads = c->num_kv_heads;
+  v.head_dim = c->head_dim;
+  return v;
+}
+
 fi_status append_common(fi_context* ctx, const void* k, const void* v, int64_t num_tokens,
                         int64_t ks, int64_t vs, const float* kd, const float* vd, float kh,
                         float vh, const int64_t* slots, const fi_nvfp4_cache* cache,
-                        void* stream) {
-  if (!ctx || !cache_ok(cache) || num_tokens < 0) return FI_ERR_INVALID_ARGUMENT;
+                        void* stream, int kv_format = 0) {
+  if (!ctx || !cache_ok(cache, kv_format) || num_tokens < 0) return FI_ERR_INVALID_ARGUMENT;
   const fi_status sup = cache_supported(cache);
   if (sup != FI_OK) return sup;
   if (num_tokens == 0) return FI_OK;  // nothing launched, nothing checked
@@ -69,6 +86,7 @@ fi_status append_common(fi_context* ctx, const void* k, const void* v, int64_t n
   a.v_scale_host = vh;
   a.slot_mapping = slots;
   a.cache = *cache;
+  a.kv_format = kv_format;
   a.status = ctx->status_dev;
   return launch_append(a, static_cast<cudaStream_t>(stream));
 }
@@ -159,6 +177,18 @@ fi_status fi_nvfp4_append(fi_context* ctx, const void* k_dev, const void* v_dev,
   if (!k_scale_dev || !v_scale_dev) return FI_ERR_INVALID_ARGUMENT;
   return fi::append_common(ctx, k_dev, v_dev, num_tokens, k_tok_stride, v_tok_stride,
                            k_scale_dev, v_scale_dev, 0.0f, 0.0f, slot_mapping_dev, cache, stream);
+}
+
+fi_status fi_fp8_append(fi_context* ctx, const void* k_dev, const void* v_dev,
+                        int64_t num_tokens, int64_t k_tok_stride, int64_t v_tok_stride,
+                        const float* k_scale_dev, const float* v_scale_dev,
+                        const int64_t* slot_mapping_dev, const fi_fp8_cache* cache,
+                        void* stream) {
+  if (!k_scale_dev || !v_scale_dev || !cache) return FI_ERR_INVALID_ARGUMENT;
+  const fi_nvfp4_cache view = fi::fp8_view(cache);
+  return fi::append_common(ctx, k_dev, v_dev, num_tokens, k_tok_stride, v_tok_stride,
+                           k_scale_dev, v_scale_dev, 0.0f, 0.0f, slot_mapping_dev, &view, stream,
+                           1);
 }
 
 fi_status fi_nvfp4_append_host_scale(fi_context* ctx, const void* k_dev, const void* v_dev,
@@ -282,9 +312,31 @@ fi_status fi_plan_get_info(const fi_plan* plan, fi_plan_info* info) {
   return FI_OK;
 }
 
+namespace fi {
+namespace {
+fi_status run_common(const fi_plan* plan, const void* q_dev, const fi_nvfp4_cache* cache,
+                     int kv_format, void* out_dev, float* lse_dev, void* stream);
+}  // namespace
+}  // namespace fi
+
 fi_status fi_prefill_run(const fi_plan* plan, const void* q_dev, const fi_nvfp4_cache* cache,
                          void* out_dev, float* lse_dev, void* stream) {
-  if (!plan || !plan->planned || !fi::cache_ok(cache) || !cache->k_scale || !cache->v_scale)
+  return fi::run_common(plan, q_dev, cache, 0, out_dev, lse_dev, stream);
+}
+
+fi_status fi_prefill_run_fp8(const fi_plan* plan, const void* q_dev, const fi_fp8_cache* cache,
+                             void* out_dev, float* lse_dev, void* stream) {
+  if (!cache) return FI_ERR_INVALID_ARGUMENT;
+  const fi_nvfp4_cache view = fi::fp8_view(cache);
+  return fi::run_common(plan, q_dev, &view, 1, out_dev, lse_dev, stream);
+}
+
+namespace fi {
+namespace {
+fi_status run_common(const fi_plan* plan, const void* q_dev, const fi_nvfp4_cache* cache,
+                     int kv_format, void* out_dev, float* lse_dev, void* stream) {
+  if (!plan || !plan->planned || !fi::cache_ok(cache, kv_format) || !cache->k_scale ||
+      !cache->v_scale || plan->host.kv_format != kv_format)
     return FI_ERR_INVALID_ARGUMENT;
   const fi::HostPlan& P = plan->host;
   if (cache->head_dim != P.head_dim || cache->page_size != P.page_size ||
@@ -311,6 +363,8 @@ fi_status fi_prefill_run(const fi_plan* plan, const void* q_dev, const fi_nvfp4_
   a.status = plan->ctx->status_dev;
   return fi::launch_prefill(a, static_cast<cudaStream_t>(stream));
 }
+}  // namespace
+}  // namespace fi
 
 fi_status fi_device_status(fi_context* ctx, void* stream, int32_t* bits, int32_t reset) {
   if (!ctx || !bits) return FI_ERR_INVALID_ARGUMENT;

@@ -168,6 +168,55 @@ __global__ void __launch_bounds__(kAppendThreads, kCtasPerSm)
   }
 }
 
+// FP8 (E4M3) append: each thread quantizes one 16-element group of one
+// (token, tensor, head) row per step (D/16 threads share a row), with the
+// next step's slot and values loaded first; 16 codes are one 16-byte store.
+template <int D>
+__global__ void __launch_bounds__(kAppendThreads, kCtasPerSm)
+    fp8_append_kernel(const AppendParams p) {
+  constexpr int kTpr = D / 16;
+  constexpr int kTokPerCta = kAppendThreads / kTpr;
+  grid_dep_wait();  // inputs may come from the previous grid (programmatic launch)
+  grid_dep_launch();
+  const float ks = p.k_scale_dev ? __ldg(p.k_scale_dev) : p.k_scale_host;
+  const float vs = p.v_scale_dev ? __ldg(p.v_scale_dev) : p.v_scale_host;
+  if (!scale_ok(ks) || !scale_ok(vs)) {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+      atomicOr(p.status, (scale_ok(ks) ? 0 : FI_DEV_BAD_K_SCALE) |
+                             (scale_ok(vs) ? 0 : FI_DEV_BAD_V_SCALE));
+    return;  // uniform across the grid
+  }
+  const int H = p.num_kv_heads;
+  const int t = static_cast<int>(blockIdx.y) >= H ? 1 : 0;  // 0 = K, 1 = V
+  const int h = static_cast<int>(blockIdx.y) - t * H;
+  const Fp8Consts qc = fp8_consts(t ? vs : ks);
+  const int j = threadIdx.x % kTpr;
+  const uint32_t hrow = static_cast<uint32_t>(h) << p.log2_page_size;
+  uint8_t* const dbase = (t ? p.v_data : p.k_data) + static_cast<uint64_t>(hrow) * D + j * 16;
+  const __nv_bfloat16* const src0 = (t ? p.v : p.k) + h * D + j * 16;
+  const int64_t tok_stride = t ? p.v_tok_stride : p.k_tok_stride;
+  const uint32_t page_rows = static_cast<uint32_t>(H) << p.log2_page_size;
+  const uint32_t pmask = (1u << p.log2_page_size) - 1u;
+  const uint64_t num_slots = static_cast<uint64_t>(p.num_slots);
+  const bool report_oob = t == 0 && h == 0 && j == 0;  // one report per token
+  const int64_t step = static_cast<int64_t>(gridDim.x) * kTokPerCta;
+  int64_t tok = static_cast<int64_t>(blockIdx.x) * kTokPerCta + threadIdx.x / kTpr;
+  ItemB<1> cur = load_item<D, 1>(p, src0, tok_stride, tok);
+  while (tok < p.num_tokens) {
+    const ItemB<1> nxt = load_item<D, 1>(p, src0, tok_stride, tok + step);
+    if (static_cast<uint64_t>(cur.slot) < num_slots) {
+      const uint32_t page = static_cast<uint32_t>(static_cast<uint64_t>(cur.slot) >> p.log2_page_size);
+      const uint32_t off = static_cast<uint32_t>(cur.slot) & pmask;
+      const uint64_t r = static_cast<uint64_t>(page) * page_rows + off;
+      *reinterpret_cast<uint4*>(dbase + r * D) = fp8_quantize16(cur.w[0][0], cur.w[0][1], qc);
+    } else if (cur.slot >= 0 && report_oob) {
+      atomicOr(p.status, FI_DEV_SLOT_OOB);
+    }
+    cur = nxt;
+    tok += step;
+  }
+}
+
 // Shared memory of the staged kernel (dynamic, 128-byte aligned base):
 // [num_stages][stage_bytes] token rows, stage layout [K|V][token][H*D] bf16;
 // [2][128] float4 quantizer entries (K, V); full[num_stages],
@@ -384,6 +433,18 @@ fi_status launch_append(const AppendArgs& a, cudaStream_t stream) {
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return FI_ERR_CUDA;
+  if (a.kv_format == 1) {
+    const int64_t gy = 2 * static_cast<int64_t>(a.cache.num_kv_heads);
+    if (gy > 65535) return FI_ERR_INVALID_ARGUMENT;
+    const int tpc = kAppendThreads / (D / 16);
+    const int64_t groups = (a.num_tokens + tpc - 1) / tpc;
+    const int64_t want = (static_cast<int64_t>(sms) * kCtasPerSm + gy - 1) / gy;
+    const int64_t per_cta = (groups + want - 1) / want;
+    const dim3 grid(static_cast<unsigned>(std::max<int64_t>(1, (groups + per_cta - 1) / per_cta)),
+                    static_cast<unsigned>(gy));
+    void (*kern)(AppendParams) = D == 128 ? fp8_append_kernel<128> : fp8_append_kernel<64>;
+    return launch_pdl(kern, grid, dim3(kAppendThreads), 0, stream, p);
+  }
   // Staged kernel for large appends whose (token, K|V) row pair fits a stage;
   // the direct kernel otherwise (its many resident warps start streaming at
   // once, which short appends need more than deep staging).

@@ -32,7 +32,8 @@ struct AppendArgs {
   float k_scale_host;
   float v_scale_host;
   const int64_t* slot_mapping;
-  fi_nvfp4_cache cache;
+  fi_nvfp4_cache cache;   // FP8: k_sf / v_sf null
+  int32_t kv_format;      // 0 NVFP4, 1 FP8 (E4M3, one code per element)
   int32_t* status;
 };
 fi_status launch_append(const AppendArgs& a, cudaStream_t stream);
@@ -69,6 +70,7 @@ struct HostPlan {
   int32_t units_per_kv_head = 0;  // group / heads_per_cta
   int32_t uniform_qo_len = 0, uniform_kv_len = 0;
   bool pair = false;              // units run on 2-CTA clusters sharing KV staging
+  int32_t kv_format = 0;          // 0 NVFP4, 1 FP8
   float sm_scale = 0.0f;
   std::vector<int32_t> work;      // 4 int32 per unit (ragged batches, and balanced plans)
   // Balanced plans (few units per CTA slot): the work-list indices of each
@@ -97,7 +99,7 @@ struct PrefillArgs {
   const int32_t* page_table;
   int32_t page_table_stride;
   const void* q;
-  fi_nvfp4_cache cache;
+  fi_nvfp4_cache cache;          // FP8 (plan kv_format 1): k_sf / v_sf null
   void* out;
   float* lse;
   int32_t* status;

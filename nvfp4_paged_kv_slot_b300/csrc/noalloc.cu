@@ -17,7 +17,7 @@
 
 namespace fi {
 
-bool cache_ok(const fi_nvfp4_cache* c);
+bool cache_ok(const fi_nvfp4_cache* c, int kv_format = 0);
 bool aligned16(const void* p);
 
 namespace {

@@ -173,6 +173,61 @@ __device__ __forceinline__ Quant16 quantize16_tab(const uint4& w0, const uint4& 
   return q;
 }
 
+// --- FP8 (E4M3) per-element codes ---------------------------------------
+// code = e4m3(RN(x / g)) for every element, one fp32 decode scale g per
+// tensor.  The division is Markstein's (as above) when every element of the
+// 16-element group is zero or has |x| in [2^-100, L), L = 2^100 g rounded
+// down to bf16 (and g itself in [2^-98, 2^100]); otherwise the IEEE division.
+// The group test runs on the packed bf16 magnitudes with 16-bit integer
+// max/min (zeros are moved to the top of the range by subtracting one).
+struct Fp8Consts {
+  float g, r;      // decode scale and RN(1 / g)
+  uint32_t lim16;  // bf16 bits of L rounded down (0: no fast path)
+};
+
+__device__ __forceinline__ Fp8Consts fp8_consts(float g) {
+  Fp8Consts c;
+  c.g = g;
+  c.r = __frcp_rn(g);
+  const bool ok = g >= 0x1p-98f && g <= 0x1p100f;
+  c.lim16 = ok ? (__float_as_uint(g * 0x1p100f) >> 16) & 0x7FFFu : 0u;
+  return c;
+}
+
+// Two bf16 words (16 values) -> 16 E4M3 codes, byte e = element e.
+__device__ __forceinline__ uint4 fp8_quantize16(const uint4& w0, const uint4& w1,
+                                               const Fp8Consts& c) {
+  const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+  uint32_t mx = 0u, mn = 0xFFFFFFFFu;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t a = w[k] & 0x7FFF7FFFu;
+    mx = __vmaxu2(mx, a);
+    mn = __vminu2(mn, __vsub2(a, 0x00010001u));
+  }
+  const uint32_t mx16 = max(mx & 0xFFFFu, mx >> 16);
+  const uint32_t mn16 = min(mn & 0xFFFFu, mn >> 16);
+  // 0x0D80: bf16 bits of 2^-100; zeros became 0xFFFF above.  lim16 is 0 when
+  // g is outside [2^-98, 2^100] (its reciprocal may be infinite): then no
+  // group, not even an all-zero one, takes the fast path.
+  const bool fast = mx16 < c.lim16 && mn16 >= 0x0D7Fu;
+  float x[16];
+  bf16x8_to_f32(w0, x);
+  bf16x8_to_f32(w1, x + 8);
+  if (fast) {
+    const uint64_t r2 = f2_pack(c.r, c.r), g2n = f2_pack(-c.g, -c.g);
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) div_markstein_x2(x[j], x[j + 1], g2n, r2);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) x[j] = __fdiv_rn(x[j], c.g);
+  }
+  uint32_t o[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) o[k] = e4m3x4_from_f32(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // --- 16-bit staging tile ------------------------------------------------------
 // A [128 rows][D] tile of 16-bit values is stored as D/64 column blocks of
 // [128 rows][64 elements] (16 KB each), rows 128 B apart, with the 128-byte
@@ -305,6 +360,77 @@ __device__ __forceinline__ void repack_half(const uint8_t* raw, uint8_t* dst, in
         o = IS_V ? dequant8_f16(w[k], s8[k]) : dequant8_bf16(w[k], s8[k]);
       *reinterpret_cast<uint4*>(dst + off0 + (k0 + k) * kRowStep * 128) = o;
     }
+  }
+}
+
+// --- FP8 (E4M3) tiles ------------------------------------------------------
+// Eight E4M3 codes (8 bytes, element e in byte e) -> 8 fp16 values (exact:
+// every E4M3 value is zero or an fp16 normal).
+__device__ __forceinline__ uint4 fp8x8_to_f16(uint2 w) {
+  uint4 o;
+  o.x = e4m3x2_to_f16x2(w.x & 0xFFFFu);
+  o.y = e4m3x2_to_f16x2(w.x >> 16);
+  o.z = e4m3x2_to_f16x2(w.y & 0xFFFFu);
+  o.w = e4m3x2_to_f16x2(w.y >> 16);
+  return o;
+}
+// The same as bf16: the fp16 values are moved to bf16 bit patterns of
+// value * 2^-112 (at most 4 significant bits, zero or normal) and multiplied
+// by 2^112 in bf16 (both steps exact).
+__device__ __forceinline__ uint4 fp8x8_to_bf16(uint2 w) {
+  const uint4 h = fp8x8_to_f16(w);
+  const uint32_t m = 0x77807780u;  // bf16x2 (2^112, 2^112)
+  return make_uint4(bmul2_u32(f16x2_to_bf16x2_scaled(h.x), m),
+                    bmul2_u32(f16x2_to_bf16x2_scaled(h.y), m),
+                    bmul2_u32(f16x2_to_bf16x2_scaled(h.z), m),
+                    bmul2_u32(f16x2_to_bf16x2_scaled(h.w), m));
+}
+
+// Repacks a raw FP8 KV tile (128 rows of D code bytes) into the 16-bit
+// staging tile, as repack_tile does for NVFP4 (K as bf16, V as fp16; rows at
+// or beyond `valid` written as zeros).  Task t (8 elements) is row t / (D/8),
+// chunk t % (D/8), read as one 8-byte word.
+template <int D, bool IS_V, int NT>
+__device__ __forceinline__ void repack_tile_fp8(const uint8_t* raw, uint8_t* dst, int valid,
+                                                int tid) {
+  static_assert(NT % (D / 8) == 0 && NT % 64 == 0, "constant-stride tasks");
+  constexpr int kPer = 128 * (D / 8) / NT;
+  constexpr int kRowStep = NT / (D / 8);
+  const uint2* words = reinterpret_cast<const uint2*>(raw);
+  const int c = tid % (D / 8);
+  const int row0 = tid / (D / 8);
+  const uint32_t off0 = sw128_offset(row0, c);
+#pragma unroll 4
+  for (int k = 0; k < kPer; ++k) {
+    uint4 o = make_uint4(0u, 0u, 0u, 0u);
+    if (row0 + k * kRowStep < valid) {
+      const uint2 w = words[tid + k * NT];
+      o = IS_V ? fp8x8_to_f16(w) : fp8x8_to_bf16(w);
+    }
+    *reinterpret_cast<uint4*>(dst + off0 + k * kRowStep * 128) = o;
+  }
+}
+
+// Half tile (64 raw rows) into rows row_base .. row_base+63 of the staging
+// tile, as repack_half does for NVFP4.
+template <int D, bool IS_V, int NT>
+__device__ __forceinline__ void repack_half_fp8(const uint8_t* raw, uint8_t* dst, int row_base,
+                                                int valid, int tid) {
+  static_assert(NT % (D / 8) == 0 && NT % 64 == 0, "constant-stride tasks");
+  constexpr int kPer = 64 * (D / 8) / NT;
+  constexpr int kRowStep = NT / (D / 8);
+  const uint2* words = reinterpret_cast<const uint2*>(raw);
+  const int c = tid % (D / 8);
+  const int row0 = tid / (D / 8);
+  const uint32_t off0 = sw128_offset(row_base + row0, c);
+#pragma unroll 4
+  for (int k = 0; k < kPer; ++k) {
+    uint4 o = make_uint4(0u, 0u, 0u, 0u);
+    if (row0 + k * kRowStep < valid) {
+      const uint2 w = words[tid + k * NT];
+      o = IS_V ? fp8x8_to_f16(w) : fp8x8_to_bf16(w);
+    }
+    *reinterpret_cast<uint4*>(dst + off0 + k * kRowStep * 128) = o;
   }
 }
 

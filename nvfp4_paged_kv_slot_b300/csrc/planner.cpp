@@ -89,6 +89,7 @@ fi_status plan_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t 
   const int32_t schedule = opts ? opts->schedule : 0;
   if (schedule < 0 || schedule > 2) return FI_ERR_INVALID_ARGUMENT;
   if (opts && (opts->cta_pairs < 0 || opts->cta_pairs > 1)) return FI_ERR_INVALID_ARGUMENT;
+  if (opts && (opts->kv_format < 0 || opts->kv_format > 1)) return FI_ERR_INVALID_ARGUMENT;
   if (opts && opts->num_ctas < 0) return FI_ERR_INVALID_ARGUMENT;
   if (batch > 0 && (qo_indptr[0] != 0 || kv_indptr[0] != 0)) return FI_ERR_INVALID_ARGUMENT;
 
@@ -100,6 +101,7 @@ fi_status plan_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t 
   P.page_size = page_size;
   P.group = num_qo_heads / num_kv_heads;
   P.sm_scale = sm_scale;
+  P.kv_format = opts ? opts->kv_format : 0;
 
   // One pass: the maxima, and the validity of every length.
   int32_t max_qo = 0, max_kv = 0;
@@ -129,7 +131,10 @@ fi_status plan_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t 
   P.units_per_kv_head = P.group / (I.heads_per_cta * I.ctas_per_unit);
   I.head_units = num_kv_heads * P.units_per_kv_head;
   I.q_tiles = (max_qo + kTileQ - 1) / kTileQ;
-  I.kv_bytes = I.total_kv_len * num_kv_heads * 2 * (head_dim / 2 + head_dim / 16);
+  // K and V bytes per token and head: NVFP4 codes and scales, or one FP8 byte
+  // per element ([#3575] §3: the gate counts bytes_per_elt)
+  const int64_t row_bytes = P.kv_format == 1 ? head_dim : head_dim / 2 + head_dim / 16;
+  I.kv_bytes = I.total_kv_len * num_kv_heads * 2 * row_bytes;
   if (schedule == 1) {
     I.global_reverse = 1;
   } else if (schedule == 2) {

@@ -80,7 +80,9 @@ struct PrefillParams {
 // PAIR: a 2-CTA cluster shares its KV staging tiles; each CTA loads and
 // repacks half of every tile's rows (64 of 128) and writes them into both
 // CTAs' staging tiles, so the raw slots hold 64 rows.
-template <int D, int NQ, bool PAIR>
+// KVF: cache format, 0 NVFP4 (codes and E4M3 block scales), 1 FP8 (one E4M3
+// code per element, no block scales).
+template <int D, int NQ, bool PAIR, int KVF = 0>
 struct Layout {
   static constexpr int kQTile = kTileQ * D * 2;
   static constexpr int kStg = kTileKV * D * 2;
@@ -91,8 +93,9 @@ struct Layout {
   // slots are half size) the deadline doubles.
   static constexpr int kStgStages = PAIR ? 4 : 3;
   static constexpr int kRawStages = 4;
-  static constexpr int kRawData = kRawRows * D / 2;
-  static constexpr int kRawSf = kRawRows * D / 16;
+  static constexpr int kRowBytes = KVF ? D : D / 2;  // code bytes per row
+  static constexpr int kRawData = kRawRows * kRowBytes;
+  static constexpr int kRawSf = KVF ? 0 : kRawRows * D / 16;
   static constexpr int kRaw = kRawData + kRawSf;
   static constexpr int kOffQ = 0;
   static constexpr int kOffStg = kOffQ + NQ * kQTile;
@@ -245,10 +248,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-template <int D, int NQ, bool PAIR>
-__global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
+template <int D, int NQ, bool PAIR, int KVF>
+__global__ void __launch_bounds__(Layout<D, NQ, PAIR, KVF>::kThreads, 1)
     nvfp4_prefill_kernel(const __grid_constant__ PrefillParams p) {
-  using L = Layout<D, NQ, PAIR>;
+  using L = Layout<D, NQ, PAIR, KVF>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -347,12 +350,18 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
             // 64-column block), counted in bytes on that CTA's stg_full.
             const int half_valid = min(max(valid - 64 * static_cast<int>(rank), 0), 64);
             uint8_t* dst = stg_smem + ss * L::kStg;
-            if (t)
-              repack_half<D, true, kRepackThreads>(raw_smem + rs * L::kRaw, dst, 64 * rank,
-                                                   half_valid, rt);
-            else
-              repack_half<D, false, kRepackThreads>(raw_smem + rs * L::kRaw, dst, 64 * rank,
-                                                    half_valid, rt);
+            const uint8_t* raw = raw_smem + rs * L::kRaw;
+            if constexpr (KVF == 1) {
+              if (t)
+                repack_half_fp8<D, true, kRepackThreads>(raw, dst, 64 * rank, half_valid, rt);
+              else
+                repack_half_fp8<D, false, kRepackThreads>(raw, dst, 64 * rank, half_valid, rt);
+            } else {
+              if (t)
+                repack_half<D, true, kRepackThreads>(raw, dst, 64 * rank, half_valid, rt);
+              else
+                repack_half<D, false, kRepackThreads>(raw, dst, 64 * rank, half_valid, rt);
+            }
             fence_proxy_async_smem();
             mbar_arrive(rep_done + ss);
             if (rt == 0) {
@@ -372,12 +381,19 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
               mbar_arrive(stg_full + ss);
             }
           } else {
-            if (t)
-              repack_tile<D, true, kRepackThreads>(raw_smem + rs * L::kRaw,
-                                                   stg_smem + ss * L::kStg, valid, rt);
-            else
-              repack_tile<D, false, kRepackThreads>(raw_smem + rs * L::kRaw,
-                                                    stg_smem + ss * L::kStg, valid, rt);
+            const uint8_t* raw = raw_smem + rs * L::kRaw;
+            uint8_t* dst = stg_smem + ss * L::kStg;
+            if constexpr (KVF == 1) {
+              if (t)
+                repack_tile_fp8<D, true, kRepackThreads>(raw, dst, valid, rt);
+              else
+                repack_tile_fp8<D, false, kRepackThreads>(raw, dst, valid, rt);
+            } else {
+              if (t)
+                repack_tile<D, true, kRepackThreads>(raw, dst, valid, rt);
+              else
+                repack_tile<D, false, kRepackThreads>(raw, dst, valid, rt);
+            }
             fence_proxy_async_smem();
             mbar_arrive(stg_full + ss);
           }
@@ -391,14 +407,14 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
     uint32_t raw_k = 0;
     int it = 0;
     bool ok = true;
-    const uint32_t pg_data = static_cast<uint32_t>(p.page_size) * (D / 2);
+    const uint32_t pg_data = static_cast<uint32_t>(p.page_size) * L::kRowBytes;
     const uint32_t pg_sf = static_cast<uint32_t>(p.page_size) * (D / 16);
     const int pages_per_tile = kTileKV / p.page_size;
     // PAIR: this CTA's rows of a tile are 64*rank .. 64*rank+63: whole pages
     // for page sizes up to 64, half a page (its rows 64*rank ..) for 128.
     const int rows_per_copy = PAIR ? min(p.page_size, 64) : p.page_size;
-    const uint32_t cp_data = static_cast<uint32_t>(rows_per_copy) * (D / 2);
-    const uint32_t cp_sf = static_cast<uint32_t>(rows_per_copy) * (D / 16);
+    const uint32_t cp_data = static_cast<uint32_t>(rows_per_copy) * L::kRowBytes;
+    const uint32_t cp_sf = KVF ? 0u : static_cast<uint32_t>(rows_per_copy) * (D / 16);
     const int copies_per_tile = PAIR ? max(pages_per_tile / 2, 1) : pages_per_tile;
     const uint32_t src_row_off = (PAIR && p.page_size == 128) ? 64u * rank : 0u;
     for (UnitCursor uc = unit_first(p, u0, ustride); ok && uc.unit >= 0;
@@ -426,11 +442,14 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
               page = 0;
             }
             const int64_t blk = static_cast<int64_t>(page) * p.num_kv_heads + w.hk;
-            const uint8_t* gd = (t ? p.v_data : p.k_data) + blk * pg_data + src_row_off * (D / 2);
-            const uint8_t* gs = (t ? p.v_sf : p.k_sf) + blk * pg_sf + src_row_off * (D / 16);
+            const uint8_t* gd =
+                (t ? p.v_data : p.k_data) + blk * pg_data + src_row_off * L::kRowBytes;
             uint8_t* sd = raw_smem + slot * L::kRaw;
             bulk_g2s(sd + lane * cp_data, gd, cp_data, raw_full + slot);
-            bulk_g2s(sd + L::kRawData + lane * cp_sf, gs, cp_sf, raw_full + slot);
+            if constexpr (KVF == 0) {
+              const uint8_t* gs = (t ? p.v_sf : p.k_sf) + blk * pg_sf + src_row_off * (D / 16);
+              bulk_g2s(sd + L::kRawData + lane * cp_sf, gs, cp_sf, raw_full + slot);
+            }
           }
           __syncwarp();
         }
@@ -760,10 +779,10 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR>::kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem_base, L::kTmemCols);
 }
 
-template <int D, int NQ, bool PAIR>
+template <int D, int NQ, bool PAIR, int KVF>
 fi_status launch_impl(const PrefillParams& p, int grid, cudaStream_t stream) {
-  using L = Layout<D, NQ, PAIR>;
-  auto kern = nvfp4_prefill_kernel<D, NQ, PAIR>;
+  using L = Layout<D, NQ, PAIR, KVF>;
+  auto kern = nvfp4_prefill_kernel<D, NQ, PAIR, KVF>;
   // at least ~116 KB so that a single CTA (and its 256-512 TMEM columns)
   // occupies each SM
   const int smem = L::kAlloc > 118784 ? L::kAlloc : 118784;
@@ -799,6 +818,22 @@ fi_status launch_impl(const PrefillParams& p, int grid, cudaStream_t stream) {
   }
   const int pairs = std::max(1, std::min(grid / 2, max_clusters));
   return launch_pdl(kern, dim3(2 * pairs), dim3(L::kThreads), smem, stream, p, cl, 1);
+}
+
+template <int KVF>
+fi_status dispatch(const HostPlan& P, const PrefillParams& p, int grid, cudaStream_t stream) {
+  const int D = P.head_dim;
+  const int nq = P.info.heads_per_cta;
+  if (P.pair) {
+    if (nq != 2) return FI_ERR_UNSUPPORTED;
+    return D == 128 ? launch_impl<128, 2, true, KVF>(p, grid, stream)
+                    : launch_impl<64, 2, true, KVF>(p, grid, stream);
+  }
+  if (D == 128)
+    return nq == 2 ? launch_impl<128, 2, false, KVF>(p, grid, stream)
+                   : launch_impl<128, 1, false, KVF>(p, grid, stream);
+  return nq == 2 ? launch_impl<64, 2, false, KVF>(p, grid, stream)
+                 : launch_impl<64, 1, false, KVF>(p, grid, stream);
 }
 
 }  // namespace
@@ -848,17 +883,7 @@ fi_status launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.num_units = static_cast<int32_t>(P.info.num_units);
   p.sm_scale = P.sm_scale;
   const int grid = P.info.num_ctas;
-  const int nq = P.info.heads_per_cta;
-  if (P.pair) {
-    if (nq != 2) return FI_ERR_UNSUPPORTED;
-    return D == 128 ? launch_impl<128, 2, true>(p, grid, stream)
-                    : launch_impl<64, 2, true>(p, grid, stream);
-  }
-  if (D == 128)
-    return nq == 2 ? launch_impl<128, 2, false>(p, grid, stream)
-                   : launch_impl<128, 1, false>(p, grid, stream);
-  return nq == 2 ? launch_impl<64, 2, false>(p, grid, stream)
-                 : launch_impl<64, 1, false>(p, grid, stream);
+  return P.kv_format == 1 ? dispatch<1>(P, p, grid, stream) : dispatch<0>(P, p, grid, stream);
 }
 
 }  // namespace fi

@@ -501,6 +501,19 @@ __device__ __forceinline__ uint32_t e4m3_from_f32(float t) {
   return r & 0xFFu;
 }
 
+// Four fp32 -> four E4M3 bytes (x0 in the low byte), round to nearest even,
+// saturating to +-448, sign kept (native cvt).
+__device__ __forceinline__ uint32_t e4m3x4_from_f32(float x0, float x1, float x2, float x3) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
+  return r;
+}
+
 // Two fp32 -> one byte of E2M1 codes (lo in the low nibble), round to
 // nearest even, saturating to +-6, sign kept (native cvt).
 __device__ __forceinline__ uint32_t e2m1x4_from_f32(float x0, float x1, float x2, float x3,
@@ -522,6 +535,13 @@ __device__ __forceinline__ uint32_t e4m3_to_f16x2_dup(uint32_t code) {
   uint32_t r;
   uint16_t pair = static_cast<uint16_t>((code & 0xFFu) | ((code & 0xFFu) << 8));
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(pair));
+  return r;
+}
+
+// Two E4M3 codes (low byte = first element) -> fp16x2 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<uint16_t>(pair)));
   return r;
 }
 
