@@ -84,12 +84,13 @@ def recorded_traffic(key):
     return rec["dram_bytes_per_launch"] if h.hexdigest()[:16] == rec["source_sha256_16"] else None
 
 
-def append_bytes(num_tokens_written, num_tokens_skipped, num_kv_heads, head_dim):
+def append_bytes(num_tokens_written, num_tokens_skipped, num_kv_heads, head_dim, fp8=False):
     """Algorithmic bytes of one append: per written token read K and V bf16
-    rows, write K and V NVFP4 rows (codes + scales) and read its 8-byte slot;
-    per skipped token read its slot; plus the two 4-byte scales."""
-    per_tok = num_kv_heads * (2 * head_dim * 2) + num_kv_heads * 2 * (head_dim // 2 +
-                                                                        head_dim // 16) + 8
+    rows, write K and V NVFP4 rows (codes + scales; FP8: one byte per
+    element) and read its 8-byte slot; per skipped token read its slot; plus
+    the two 4-byte scales."""
+    row = head_dim if fp8 else head_dim // 2 + head_dim // 16
+    per_tok = num_kv_heads * (2 * head_dim * 2) + num_kv_heads * 2 * row + 8
     return num_tokens_written * per_tok + num_tokens_skipped * 8 + 8
 
 
@@ -145,8 +146,9 @@ class PathRunner:
     """Device-resident inputs and outputs of one workload, and one step of the
     path (append -> plan -> run) through the C ABI."""
 
-    def __init__(self, fi, name, device, seqs=0):
+    def __init__(self, fi, name, device, seqs=0, kv_format="nvfp4"):
         self.fi = fi
+        self.fp8 = kv_format == "fp8"
         sp = W.spec(name)
         if seqs:
             sp.seq_lens = sp.seq_lens[:seqs]
@@ -159,10 +161,17 @@ class PathRunner:
         self.page_table = d["page_table"].to(device)
         self.qo_indptr = d["qo_indptr"].numpy()
         self.kv_indptr = d["kv_indptr"].numpy()
-        ks = torch.tensor([d["k_scale"]], dtype=torch.float32, device=device)
-        vs = torch.tensor([d["v_scale"]], dtype=torch.float32, device=device)
-        self.cache = fi.NVFP4Cache(d["num_pages"], sp.num_kv_heads, sp.page_size, sp.head_dim,
-                                   device=device, k_scale=ks, v_scale=vs, fill=0)
+        if self.fp8:
+            # FP8 decode scales map each tensor's amax to 448
+            ks = (self.k.float().abs().max() / 448.0).reshape(1).to(torch.float32)
+            vs = (self.v.float().abs().max() / 448.0).reshape(1).to(torch.float32)
+            self.cache = fi.FP8Cache(d["num_pages"], sp.num_kv_heads, sp.page_size, sp.head_dim,
+                                     device=device, k_scale=ks, v_scale=vs, fill=0)
+        else:
+            ks = torch.tensor([d["k_scale"]], dtype=torch.float32, device=device)
+            vs = torch.tensor([d["v_scale"]], dtype=torch.float32, device=device)
+            self.cache = fi.NVFP4Cache(d["num_pages"], sp.num_kv_heads, sp.page_size,
+                                       sp.head_dim, device=device, k_scale=ks, v_scale=vs, fill=0)
         self.out = torch.empty_like(self.q)
         self.lse = torch.empty(self.q.shape[:2], dtype=torch.float32, device=device)
         self.ctx = fi.fi_context_create()
@@ -170,22 +179,26 @@ class PathRunner:
         lens = np.diff(self.qo_indptr).tolist()
         self.flops = W.causal_flops(lens, lens, sp.num_qo_heads, sp.head_dim)
         self.tokens = int(self.qo_indptr[-1])
-        self.append_bytes = append_bytes(self.tokens, 0, sp.num_kv_heads, sp.head_dim)
+        self.append_bytes = append_bytes(self.tokens, 0, sp.num_kv_heads, sp.head_dim,
+                                         fp8=self.fp8)
 
     def step(self, stream, ev=None):
         fi, sp = self.fi, self.sp
         if ev is not None:
             ev[0].record(stream)
-        fi.fi_nvfp4_append(self.ctx, self.k, self.v, self.cache.k_scale, self.cache.v_scale,
-                           self.slots, self.cache, stream=stream)
+        append = fi.fi_fp8_append if self.fp8 else fi.fi_nvfp4_append
+        append(self.ctx, self.k, self.v, self.cache.k_scale, self.cache.v_scale, self.slots,
+               self.cache, stream=stream)
         if ev is not None:
             ev[1].record(stream)
         fi.fi_prefill_plan(self.plan, self.qo_indptr, self.kv_indptr, self.page_table,
                            sp.num_qo_heads, sp.num_kv_heads, sp.head_dim, sp.page_size,
-                           sm_scale=self.d["sm_scale"], stream=stream)
+                           sm_scale=self.d["sm_scale"], stream=stream,
+                           kv_format=1 if self.fp8 else 0)
         if ev is not None:
             ev[2].record(stream)
-        fi.fi_prefill_run(self.plan, self.q, self.cache, self.out, self.lse, stream=stream)
+        run = fi.fi_prefill_run_fp8 if self.fp8 else fi.fi_prefill_run
+        run(self.plan, self.q, self.cache, self.out, self.lse, stream=stream)
         if ev is not None:
             ev[3].record(stream)
 
@@ -422,6 +435,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOAD_DESC), default="uniform")
+    ap.add_argument("--kv-format", choices=["nvfp4", "fp8"], default="nvfp4",
+                    help="fp8: the FP8 (E4M3) paged KV variant of the same path")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -454,7 +469,7 @@ def main():
                           "us_warm_l2": a["warm_ms"] * 1e3, "frac": gbs / peaks["hbm_gbs"],
                           "status": a["status"]}), flush=True)
         return 0 if a["status"] == 0 else 1
-    runner = PathRunner(fi, args.workload, device, args.seqs)
+    runner = PathRunner(fi, args.workload, device, args.seqs, kv_format=args.kv_format)
     stream = torch.cuda.Stream(device=device)
     stream.wait_stream(torch.cuda.current_stream(device))  # inputs are made on the current stream
     # correctness guard: the step must run clean before it is timed
@@ -504,7 +519,7 @@ def main():
                "status": a["status"]}
 
     cpu = None
-    if not args.no_cpu_baseline and rank == 0 and world == 1:
+    if not args.no_cpu_baseline and rank == 0 and world == 1 and not runner.fp8:
         f, t, desc, threads, _ = oracle_sample(args.workload, args.cpu_budget)
         cpu = {"value": f / t / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": desc}
@@ -515,7 +530,9 @@ def main():
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD_DESC[args.workload] +
-                   (f" (first {args.seqs} sequences only)" if args.seqs else ""),
+                   (f" (first {args.seqs} sequences only)" if args.seqs else "") +
+                   (" [FP8 (E4M3) paged KV variant]" if runner.fp8 else ""),
+                   "kv_format": args.kv_format,
                    "tokens": runner.tokens,
                    "flops_per_step": runner.flops,
                    "l2": "inputs larger than L2 (Q 8.6 GB, KV cache 1.2 GB per step)"
@@ -524,16 +541,20 @@ def main():
         "roofline": {"bound": "tensor", "achieved": pf_tflops, "peak": peak_sus,
                      "unit": "TFLOP/s", "frac": pf_tflops / peak_sus,
                      "traffic": recorded_traffic("prefill_uniform")
-                     if args.workload == "uniform" and not args.seqs else None,
+                     if args.workload == "uniform" and not args.seqs and not runner.fp8 else None,
                      "kernel": "nvfp4_prefill_kernel", "peak_kind":
                      f"bf16 dense sustained ({peaks['source']})",
                      "frac_of_burst_peak": pf_tflops / peak_burst,
                      "ms_per_launch": pf_ms},
         "append_in_step": {"ms_per_launch": ap_ms, "gbs": runner_append_gbs,
                            "frac": runner_append_gbs / peaks["hbm_gbs"],
-                           "kernel": "nvfp4_append_staged_kernel",
+                           "kernel": ("fp8_append_kernel" if runner.fp8 else
+                                      # the library's switch to the staged kernel
+                                      "nvfp4_append_staged_kernel" if runner.tokens >= 65536
+                                      else "nvfp4_append_kernel"),
                            "traffic": recorded_traffic("append_uniform")
-                           if args.workload == "uniform" and not args.seqs else None},
+                           if args.workload == "uniform" and not args.seqs and not runner.fp8
+                           else None},
         "append_bench": app,
         "clocks": clk,
         "e2e": e2e,
