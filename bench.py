@@ -50,6 +50,8 @@ WORKLOAD_DESC = {
               "append + plan + causal prefill",
     "ragged": "ragged batch: 256 sequences, qo_len=kv_len log-uniform in [128,16384], H_q=32, "
               "H_kv=8, head_dim=128, page_size=16, append + plan + causal prefill",
+    "decode": "decode batch: 128 sequences x kv_len 4096, qo_len 1, H_q=32, H_kv=8, "
+              "head_dim=128, page_size=16, append + decode plan + decode",
 }
 
 
@@ -176,8 +178,15 @@ class PathRunner:
         self.lse = torch.empty(self.q.shape[:2], dtype=torch.float32, device=device)
         self.ctx = fi.fi_context_create()
         self.plan = fi.fi_plan_create(self.ctx)
+        self.decode = bool(sp.qo_lens)
         lens = np.diff(self.qo_indptr).tolist()
-        self.flops = W.causal_flops(lens, lens, sp.num_qo_heads, sp.head_dim)
+        kv_lens = np.diff(self.kv_indptr).tolist()
+        self.flops = W.causal_flops(lens, kv_lens, sp.num_qo_heads, sp.head_dim)
+        # decode: HBM bytes the attention must move (the NVFP4 K and V of every
+        # sequence once, Q in, O and LSE out)
+        self.decode_bytes = (sum(kv_lens) * sp.num_kv_heads * 2 *
+                             (sp.head_dim // 2 + sp.head_dim // 16) +
+                             sum(lens) * sp.num_qo_heads * (2 * sp.head_dim * 2 + 4))
         self.tokens = int(self.qo_indptr[-1])
         self.append_bytes = append_bytes(self.tokens, 0, sp.num_kv_heads, sp.head_dim,
                                          fp8=self.fp8)
@@ -191,13 +200,21 @@ class PathRunner:
                self.cache, stream=stream)
         if ev is not None:
             ev[1].record(stream)
-        fi.fi_prefill_plan(self.plan, self.qo_indptr, self.kv_indptr, self.page_table,
-                           sp.num_qo_heads, sp.num_kv_heads, sp.head_dim, sp.page_size,
-                           sm_scale=self.d["sm_scale"], stream=stream,
-                           kv_format=1 if self.fp8 else 0)
+        if self.decode:
+            fi.fi_decode_plan(self.plan, self.qo_indptr, self.kv_indptr, self.page_table,
+                              sp.num_qo_heads, sp.num_kv_heads, sp.head_dim, sp.page_size,
+                              sm_scale=self.d["sm_scale"], stream=stream)
+        else:
+            fi.fi_prefill_plan(self.plan, self.qo_indptr, self.kv_indptr, self.page_table,
+                               sp.num_qo_heads, sp.num_kv_heads, sp.head_dim, sp.page_size,
+                               sm_scale=self.d["sm_scale"], stream=stream,
+                               kv_format=1 if self.fp8 else 0)
         if ev is not None:
             ev[2].record(stream)
-        run = fi.fi_prefill_run_fp8 if self.fp8 else fi.fi_prefill_run
+        if self.decode:
+            run = fi.fi_decode_run
+        else:
+            run = fi.fi_prefill_run_fp8 if self.fp8 else fi.fi_prefill_run
         run(self.plan, self.q, self.cache, self.out, self.lse, stream=stream)
         if ev is not None:
             ev[3].record(stream)
@@ -538,7 +555,13 @@ def main():
                    "l2": "inputs larger than L2 (Q 8.6 GB, KV cache 1.2 GB per step)"
                    if args.workload == "uniform" else "see workload",
                    "parallelism": f"replicas x{world} (independent shards, no collective)"},
-        "roofline": {"bound": "tensor", "achieved": pf_tflops, "peak": peak_sus,
+        "roofline": {"bound": "hbm", "achieved": runner.decode_bytes / (pf_ms * 1e-3) / 1e9,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": runner.decode_bytes / (pf_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                     "traffic": None, "kernel": "nvfp4_decode_kernel",
+                     "algorithmic_bytes": runner.decode_bytes, "tflops": pf_tflops,
+                     "ms_per_launch": pf_ms} if runner.decode else
+                    {"bound": "tensor", "achieved": pf_tflops, "peak": peak_sus,
                      "unit": "TFLOP/s", "frac": pf_tflops / peak_sus,
                      "traffic": recorded_traffic("prefill_uniform")
                      if args.workload == "uniform" and not args.seqs and not runner.fp8 else None,

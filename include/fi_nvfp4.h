@@ -197,6 +197,30 @@ fi_status fi_plan_get_info(const fi_plan* plan, fi_plan_info* info);
 fi_status fi_prefill_run(const fi_plan* plan, const void* q_dev, const fi_nvfp4_cache* cache,
                          void* out_dev, float* lse_dev, void* stream);
 
+/* ---- decode ----------------------------------------------------------------
+ * Plans attention for the newest query tokens of each sequence (decode and
+ * short speculative steps) over the NVFP4 cache ([#5043] decode.py: max_kv_len
+ * comes from one reduction over the lengths).  Same arguments and causal rule
+ * as fi_prefill_plan; every sequence has qo_len <= 8 and
+ * (num_qo_heads / num_kv_heads) * qo_len <= 32, else FI_ERR_UNSUPPORTED.  The
+ * keys of a sequence are split into chunks (a power of two, 256 .. 16384,
+ * chosen from the batch); a sequence with several chunks is merged by a second
+ * kernel.  The plan owns a device buffer for the chunks' partial results,
+ * grown (after synchronizing `stream`) when a plan needs more; otherwise it
+ * behaves as fi_prefill_plan.  fi_plan_get_info reports the units (sequence,
+ * kv head, chunk) in num_units. */
+fi_status fi_decode_plan(fi_plan* plan, const int32_t* qo_indptr_host,
+                         const int32_t* kv_indptr_host, int32_t batch,
+                         const int32_t* page_table_dev, int32_t page_table_stride,
+                         int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                         int32_t page_size, float sm_scale, void* stream);
+
+/* Runs a decode plan: arguments, layouts and output as fi_prefill_run.  A
+ * prefill plan passed here, or a decode plan passed to fi_prefill_run,
+ * returns FI_ERR_INVALID_ARGUMENT. */
+fi_status fi_decode_run(const fi_plan* plan, const void* q_dev, const fi_nvfp4_cache* cache,
+                        void* out_dev, float* lse_dev, void* stream);
+
 /* ---- FP8 (E4M3) paged KV variant --------------------------------------
  * The same paged layout with one E4M3 code per element and no block scales
  * (a reading: the pages measure FP8 attention ([#3575]) but give no FP8

@@ -39,7 +39,7 @@ EXPORTED = ("fi_context_create", "fi_context_destroy", "fi_nvfp4_append",
             "fi_nvfp4_append_host_scale", "fi_plan_create", "fi_plan_destroy",
             "fi_prefill_plan", "fi_plan_get_info", "fi_prefill_run", "fi_prefill_plan_host",
             "fi_device_status", "fi_status_string", "fi_version", "fi_prefill_noalloc",
-            "fi_fp8_append", "fi_prefill_run_fp8")
+            "fi_fp8_append", "fi_prefill_run_fp8", "fi_decode_plan", "fi_decode_run")
 
 
 class fi_nvfp4_cache(C.Structure):
@@ -81,6 +81,8 @@ _sigs = {
                         C.POINTER(fi_nvfp4_cache), _vp],
     "fi_nvfp4_append_host_scale": [_vp, _vp, _vp, _i64, _i64, _i64, _f32, _f32, _vp,
                                    C.POINTER(fi_nvfp4_cache), _vp],
+    "fi_decode_plan": [_vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _vp],
+    "fi_decode_run": [_vp, _vp, C.POINTER(fi_nvfp4_cache), _vp, _vp, _vp],
     "fi_fp8_append": [_vp, _vp, _vp, _i64, _i64, _i64, _vp, _vp, _vp,
                       C.POINTER(fi_fp8_cache), _vp],
     "fi_prefill_run_fp8": [_vp, _vp, C.POINTER(fi_fp8_cache), _vp, _vp, _vp],
@@ -291,6 +293,30 @@ def fi_prefill_run(plan, q, cache: NVFP4Cache, out, lse=None, stream=None):
     cc = cache.c()
     _check(lib.fi_prefill_run(plan, _ptr(q), C.byref(cc), _ptr(out), _ptr(lse),
                               _stream(stream)), "fi_prefill_run")
+
+
+def fi_decode_plan(plan, qo_indptr, kv_indptr, page_table, num_qo_heads, num_kv_heads,
+                   head_dim, page_size, sm_scale=0.0, stream=None):
+    """Decode plan (qo_len <= 8 per sequence); arguments as fi_prefill_plan."""
+    qo = _host_i32(qo_indptr)
+    kv = _host_i32(kv_indptr)
+    if qo.size != kv.size or qo.size < 1:
+        raise ValueError("qo_indptr and kv_indptr must both have batch+1 entries")
+    _check(lib.fi_decode_plan(plan, qo.ctypes.data, kv.ctypes.data, qo.size - 1,
+                              _ptr(page_table), page_table.stride(0) if page_table is not None
+                              else 0, num_qo_heads, num_kv_heads, head_dim, page_size,
+                              float(sm_scale), _stream(stream)), "fi_decode_plan")
+
+
+def fi_decode_run(plan, q, cache: NVFP4Cache, out, lse=None, stream=None):
+    """Runs a decode plan; arguments as fi_prefill_run."""
+    import torch
+    for name, t in (("q", q), ("out", out)):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 tensor")
+    cc = cache.c()
+    _check(lib.fi_decode_run(plan, _ptr(q), C.byref(cc), _ptr(out), _ptr(lse), _stream(stream)),
+           "fi_decode_run")
 
 
 def fi_fp8_append(ctx, k, v, k_scale, v_scale, slot_mapping, cache: FP8Cache, stream=None):

@@ -27,7 +27,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-shared",
               "--expt-relaxed-constexpr", "-Xptxas", "-warn-spills"]
 
-LIB_SOURCES = ["api.cu", "append.cu", "prefill.cu", "planner.cpp", "noalloc.cu"]
+LIB_SOURCES = ["api.cu", "append.cu", "prefill.cu", "decode.cu", "planner.cpp", "noalloc.cu"]
 DIAG_SOURCES = ["diag.cu"]
 
 

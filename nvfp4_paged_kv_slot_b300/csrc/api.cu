@@ -129,6 +129,9 @@ struct fi_plan {
   const int32_t* page_table = nullptr;
   int32_t page_table_stride = 0;
   size_t off_kv = 0, off_work = 0, off_slot_units = 0, off_slot_begin = 0;
+  // decode plans: partial results of sequences split over several chunks
+  float* part = nullptr;
+  size_t part_floats = 0;
 };
 
 extern "C" {
@@ -220,6 +223,7 @@ fi_status fi_plan_destroy(fi_plan* plan) {
   if (!plan) return FI_ERR_INVALID_ARGUMENT;
   cudaDeviceSynchronize();
   if (plan->dev) cudaFree(plan->dev);
+  if (plan->part) cudaFree(plan->part);
   for (int i = 0; i < 2; ++i) {
     if (plan->pinned[i]) cudaFreeHost(plan->pinned[i]);
     if (plan->copied[i]) cudaEventDestroy(plan->copied[i]);
@@ -228,29 +232,13 @@ fi_status fi_plan_destroy(fi_plan* plan) {
   return FI_OK;
 }
 
-fi_status fi_prefill_plan(fi_plan* plan, const int32_t* qo_indptr_host,
-                          const int32_t* kv_indptr_host, int32_t batch,
-                          const int32_t* page_table_dev, int32_t page_table_stride,
-                          int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
-                          int32_t page_size, float sm_scale, const fi_plan_options* opts,
-                          void* stream) {
-  if (!plan) return FI_ERR_INVALID_ARGUMENT;
-  plan->planned = false;
-  if (batch > 0 && (!page_table_dev || page_table_stride <= 0)) return FI_ERR_INVALID_ARGUMENT;
-  if (!(sm_scale > 0.0f) || !std::isfinite(sm_scale))
-    sm_scale = 1.0f / std::sqrt(static_cast<float>(head_dim));
-  const fi_context* ctx = plan->ctx;
-  const int64_t l2 = (opts && opts->l2_bytes > 0) ? opts->l2_bytes : ctx->l2_bytes;
-  fi_status st = fi::plan_host(qo_indptr_host, kv_indptr_host, batch, num_qo_heads, num_kv_heads,
-                               head_dim, page_size, sm_scale, l2, ctx->num_sms, opts, false,
-                               &plan->host);
-  if (st != FI_OK) return st;
-  // page table rows must cover every sequence's pages
-  if (batch > 0 && (plan->host.info.max_kv_len + page_size - 1) / page_size > page_table_stride)
-    return FI_ERR_INVALID_ARGUMENT;
-  plan->page_table = page_table_dev;
-  plan->page_table_stride = page_table_stride;
+}  // extern "C"
 
+namespace {
+// Copies qo_indptr | kv_indptr | work list | slot units | slot begins of the
+// plan's host description to plan-owned device memory (see fi_prefill_plan).
+fi_status upload_plan(fi_plan* plan, const int32_t* qo_indptr_host,
+                      const int32_t* kv_indptr_host, int32_t batch, void* stream) {
   // Device copy: qo_indptr | kv_indptr | work list | slot units | slot begins.
   const size_t nb = static_cast<size_t>(batch) + 1;
   plan->off_kv = nb;
@@ -305,6 +293,101 @@ fi_status fi_prefill_plan(fi_plan* plan, const int32_t* qo_indptr_host,
   plan->planned = true;
   return FI_OK;
 }
+}  // namespace
+
+extern "C" {
+
+fi_status fi_prefill_plan(fi_plan* plan, const int32_t* qo_indptr_host,
+                          const int32_t* kv_indptr_host, int32_t batch,
+                          const int32_t* page_table_dev, int32_t page_table_stride,
+                          int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                          int32_t page_size, float sm_scale, const fi_plan_options* opts,
+                          void* stream) {
+  if (!plan) return FI_ERR_INVALID_ARGUMENT;
+  plan->planned = false;
+  if (batch > 0 && (!page_table_dev || page_table_stride <= 0)) return FI_ERR_INVALID_ARGUMENT;
+  if (!(sm_scale > 0.0f) || !std::isfinite(sm_scale))
+    sm_scale = 1.0f / std::sqrt(static_cast<float>(head_dim));
+  const fi_context* ctx = plan->ctx;
+  const int64_t l2 = (opts && opts->l2_bytes > 0) ? opts->l2_bytes : ctx->l2_bytes;
+  fi_status st = fi::plan_host(qo_indptr_host, kv_indptr_host, batch, num_qo_heads, num_kv_heads,
+                               head_dim, page_size, sm_scale, l2, ctx->num_sms, opts, false,
+                               &plan->host);
+  if (st != FI_OK) return st;
+  // page table rows must cover every sequence's pages
+  if (batch > 0 && (plan->host.info.max_kv_len + page_size - 1) / page_size > page_table_stride)
+    return FI_ERR_INVALID_ARGUMENT;
+  plan->page_table = page_table_dev;
+  plan->page_table_stride = page_table_stride;
+
+  return upload_plan(plan, qo_indptr_host, kv_indptr_host, batch, stream);
+}
+
+fi_status fi_decode_plan(fi_plan* plan, const int32_t* qo_indptr_host,
+                         const int32_t* kv_indptr_host, int32_t batch,
+                         const int32_t* page_table_dev, int32_t page_table_stride,
+                         int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                         int32_t page_size, float sm_scale, void* stream) {
+  if (!plan) return FI_ERR_INVALID_ARGUMENT;
+  plan->planned = false;
+  if (batch > 0 && (!page_table_dev || page_table_stride <= 0)) return FI_ERR_INVALID_ARGUMENT;
+  if (!(sm_scale > 0.0f) || !std::isfinite(sm_scale))
+    sm_scale = 1.0f / std::sqrt(static_cast<float>(head_dim));
+  fi::HostPlan& P = plan->host;
+  fi_status st = fi::plan_decode_host(qo_indptr_host, kv_indptr_host, batch, num_qo_heads,
+                                      num_kv_heads, head_dim, page_size, sm_scale,
+                                      plan->ctx->num_sms, &P);
+  if (st != FI_OK) return st;
+  if (batch > 0 && (P.info.max_kv_len + page_size - 1) / page_size > page_table_stride)
+    return FI_ERR_INVALID_ARGUMENT;
+  plan->page_table = page_table_dev;
+  plan->page_table_stride = page_table_stride;
+  // the units and merges travel in the work-list and slot-unit regions
+  P.work = P.dec_units;
+  P.slot_units = P.dec_merges;
+  P.slot_begin.clear();
+  const size_t need = static_cast<size_t>(P.dec_parts) * P.dec_rows * (head_dim + 2);
+  if (need > plan->part_floats) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return FI_ERR_CUDA;  // earlier runs use it
+    if (plan->part) cudaFree(plan->part);
+    plan->part = nullptr;
+    plan->part_floats = 0;
+    const size_t cap = need * 3 / 2;
+    if (cudaMalloc(&plan->part, cap * sizeof(float)) != cudaSuccess) return FI_ERR_OUT_OF_MEMORY;
+    plan->part_floats = cap;
+  }
+  return upload_plan(plan, qo_indptr_host, kv_indptr_host, batch, stream);
+}
+
+fi_status fi_decode_run(const fi_plan* plan, const void* q_dev, const fi_nvfp4_cache* cache,
+                        void* out_dev, float* lse_dev, void* stream) {
+  if (!plan || !plan->planned || !plan->host.decode || !fi::cache_ok(cache, 0) ||
+      !cache->k_scale || !cache->v_scale)
+    return FI_ERR_INVALID_ARGUMENT;
+  const fi::HostPlan& P = plan->host;
+  if (cache->head_dim != P.head_dim || cache->page_size != P.page_size ||
+      cache->num_kv_heads != P.num_kv_heads)
+    return FI_ERR_INVALID_ARGUMENT;
+  if (P.info.num_units == 0) return FI_OK;
+  if (!q_dev || !out_dev || !fi::aligned16(q_dev) || !fi::aligned16(out_dev))
+    return FI_ERR_INVALID_ARGUMENT;
+  fi::DecodeArgs a;
+  a.plan = &P;
+  a.qo_indptr_dev = plan->dev;
+  a.kv_indptr_dev = plan->dev + plan->off_kv;
+  a.units_dev = plan->dev + plan->off_work;
+  a.merges_dev = plan->dev + plan->off_slot_units;
+  a.part = plan->part;
+  a.page_table = plan->page_table;
+  a.page_table_stride = plan->page_table_stride;
+  a.q = q_dev;
+  a.cache = *cache;
+  a.out = out_dev;
+  a.lse = lse_dev;
+  a.status = plan->ctx->status_dev;
+  return fi::launch_decode(a, static_cast<cudaStream_t>(stream));
+}
 
 fi_status fi_plan_get_info(const fi_plan* plan, fi_plan_info* info) {
   if (!plan || !info || !plan->planned) return FI_ERR_INVALID_ARGUMENT;
@@ -336,7 +419,7 @@ namespace {
 fi_status run_common(const fi_plan* plan, const void* q_dev, const fi_nvfp4_cache* cache,
                      int kv_format, void* out_dev, float* lse_dev, void* stream) {
   if (!plan || !plan->planned || !fi::cache_ok(cache, kv_format) || !cache->k_scale ||
-      !cache->v_scale || plan->host.kv_format != kv_format)
+      !cache->v_scale || plan->host.kv_format != kv_format || plan->host.decode)
     return FI_ERR_INVALID_ARGUMENT;
   const fi::HostPlan& P = plan->host;
   if (cache->head_dim != P.head_dim || cache->page_size != P.page_size ||

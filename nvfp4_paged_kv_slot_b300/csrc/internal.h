@@ -78,7 +78,39 @@ struct HostPlan {
   // slot_begin[s + 1]).  Empty otherwise (units are dealt round-robin).
   std::vector<int32_t> slot_units;
   std::vector<int32_t> slot_begin;
+  // decode plans (fi_decode_plan): units (sequence, kv head, chunk, partial
+  // slot or -1) and merges (sequence, kv head, first slot, chunks), 4 int32
+  // each; dec_rows = G * max qo_len rows per partial slot
+  bool decode = false;
+  int32_t dec_chunk = 0, dec_rows = 0;
+  int64_t dec_parts = 0;
+  std::vector<int32_t> dec_units;
+  std::vector<int32_t> dec_merges;
 };
+
+// Plans a decode (qo_len <= kDecodeMaxQo per sequence, G * qo_len <= 32).
+constexpr int kDecodeMaxQo = 8;
+constexpr int kDecodeMaxRows = 32;
+fi_status plan_decode_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t batch,
+                           int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                           int32_t page_size, float sm_scale, int32_t num_sms, HostPlan* out);
+
+struct DecodeArgs {
+  const HostPlan* plan;
+  const int32_t* qo_indptr_dev;
+  const int32_t* kv_indptr_dev;
+  const int32_t* units_dev;
+  const int32_t* merges_dev;
+  float* part;
+  const int32_t* page_table;
+  int32_t page_table_stride;
+  const void* q;
+  fi_nvfp4_cache cache;
+  void* out;
+  float* lse;
+  int32_t* status;
+};
+fi_status launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
 // Validates the arguments and plans on the host only (no CUDA calls).
 // `want_list`: also fill the ordered work list for uniform batches.

@@ -230,6 +230,98 @@ fi_status plan_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t 
   return FI_OK;
 }
 
+// Decode plan ([#5043] decode.py: max_kv_len from one reduction over the
+// lengths).  Units are (sequence, kv head, chunk of keys); the chunk length
+// (a power of two, 256 .. 16384) is the smallest that keeps the units below
+// 32 per SM, so that short batches still fill the GPU and long ones do not
+// pay for many merges.  A sequence with several chunks gets one partial slot
+// per chunk and one merge.
+fi_status plan_decode_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t batch,
+                           int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                           int32_t page_size, float sm_scale, int32_t num_sms, HostPlan* out) {
+  if (!out || batch < 0 || (batch > 0 && (!qo_indptr || !kv_indptr)))
+    return FI_ERR_INVALID_ARGUMENT;
+  if (num_kv_heads <= 0 || num_qo_heads <= 0 || num_qo_heads % num_kv_heads != 0)
+    return FI_ERR_INVALID_ARGUMENT;
+  if (head_dim != 64 && head_dim != 128) return FI_ERR_UNSUPPORTED;
+  if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128)
+    return FI_ERR_UNSUPPORTED;
+  if (batch > 0 && (qo_indptr[0] != 0 || kv_indptr[0] != 0)) return FI_ERR_INVALID_ARGUMENT;
+  HostPlan& P = *out;
+  P = HostPlan{};
+  P.decode = true;
+  P.num_qo_heads = num_qo_heads;
+  P.num_kv_heads = num_kv_heads;
+  P.head_dim = head_dim;
+  P.page_size = page_size;
+  P.group = num_qo_heads / num_kv_heads;
+  P.sm_scale = sm_scale;
+  int32_t max_qo = 0, max_kv = 0;
+  for (int32_t b = 0; b < batch; ++b) {
+    const int32_t qo = qo_indptr[b + 1] - qo_indptr[b];
+    const int32_t kv = kv_indptr[b + 1] - kv_indptr[b];
+    if (qo < 0 || kv < 0 || qo > kv) return FI_ERR_INVALID_ARGUMENT;
+    max_qo = std::max(max_qo, qo);
+    max_kv = std::max(max_kv, kv);
+  }
+  if (max_qo > kDecodeMaxQo || P.group * max_qo > kDecodeMaxRows) return FI_ERR_UNSUPPORTED;
+  fi_plan_info& I = P.info;
+  I.batch = batch;
+  I.max_qo_len = max_qo;
+  I.max_kv_len = max_kv;
+  I.total_qo_len = batch > 0 ? qo_indptr[batch] : 0;
+  I.total_kv_len = batch > 0 ? kv_indptr[batch] : 0;
+  I.is_uniform = (I.total_qo_len == static_cast<int64_t>(batch) * max_qo &&
+                  I.total_kv_len == static_cast<int64_t>(batch) * max_kv)
+                     ? 1
+                     : 0;
+  I.heads_per_cta = P.group;
+  I.head_units = num_kv_heads;
+  I.ctas_per_unit = 1;
+  I.kv_bytes = I.total_kv_len * num_kv_heads * 2 * (head_dim / 2 + head_dim / 16);
+  P.dec_rows = std::max(1, P.group * max_qo);
+  auto count_units = [&](int64_t chunk) {
+    int64_t n = 0;
+    for (int32_t b = 0; b < batch; ++b) {
+      const int32_t qo = qo_indptr[b + 1] - qo_indptr[b];
+      const int32_t kv = kv_indptr[b + 1] - kv_indptr[b];
+      if (qo > 0) n += (kv + chunk - 1) / chunk;
+    }
+    return n * num_kv_heads;
+  };
+  int64_t chunk = 256;
+  const int64_t cap = 32 * static_cast<int64_t>(std::max(num_sms, 1));
+  while (chunk < 16384 && count_units(chunk) > cap) chunk *= 2;
+  P.dec_chunk = static_cast<int32_t>(chunk);
+  int64_t slots = 0;
+  for (int32_t b = 0; b < batch; ++b) {
+    const int32_t qo = qo_indptr[b + 1] - qo_indptr[b];
+    const int32_t kv = kv_indptr[b + 1] - kv_indptr[b];
+    if (qo == 0) continue;
+    const int32_t n = static_cast<int32_t>((kv + chunk - 1) / chunk);
+    for (int32_t hk = 0; hk < num_kv_heads; ++hk) {
+      for (int32_t c = 0; c < n; ++c) {
+        P.dec_units.push_back(b);
+        P.dec_units.push_back(hk);
+        P.dec_units.push_back(c);
+        P.dec_units.push_back(n > 1 ? static_cast<int32_t>(slots + c) : -1);
+      }
+      if (n > 1) {
+        P.dec_merges.push_back(b);
+        P.dec_merges.push_back(hk);
+        P.dec_merges.push_back(static_cast<int32_t>(slots));
+        P.dec_merges.push_back(n);
+        slots += n;
+      }
+    }
+  }
+  if (slots > 0x7FFFFFFF) return FI_ERR_UNSUPPORTED;
+  P.dec_parts = slots;
+  I.num_units = static_cast<int64_t>(P.dec_units.size() / 4);
+  I.num_ctas = static_cast<int32_t>(std::min<int64_t>((I.num_units + 3) / 4, 0x7FFFFFFF));
+  return FI_OK;
+}
+
 }  // namespace fi
 
 extern "C" fi_status fi_prefill_plan_host(const int32_t* qo_indptr_host,

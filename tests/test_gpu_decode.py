@@ -1,0 +1,117 @@
+"""Decode through the C ABI vs the oracle: the newest 1..8 tokens of each
+sequence attend to its whole NVFP4 cache (query row t sees keys
+j <= t + kv_len - qo_len), split into KV chunks and merged, within the same
+tolerances as the prefill."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import (assert_within_tolerance, compare_attention, device_inputs, fi, gpu_cache,
+                      oracle_attention, oracle_cache)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _run_decode(d):
+    m = fi()
+    sp = d["spec"]
+    ctx = m.fi_context_create()
+    c = gpu_cache(d)
+    m.fi_nvfp4_append(ctx, d["k"], d["v"], c.k_scale, c.v_scale, d["slot_mapping"], c)
+    plan = m.fi_plan_create(ctx)
+    m.fi_decode_plan(plan, d["host"]["qo_indptr"], d["host"]["kv_indptr"], d["page_table"],
+                     sp.num_qo_heads, sp.num_kv_heads, sp.head_dim, sp.page_size,
+                     sm_scale=d["sm_scale"])
+    info = m.fi_plan_get_info(plan)
+    out = torch.empty_like(d["q"])
+    lse = torch.empty(d["q"].shape[:2], dtype=torch.float32, device="cuda")
+    m.fi_decode_run(plan, d["q"], c, out, lse)
+    status = m.fi_device_status(ctx)
+    m.fi_plan_destroy(plan)
+    m.fi_context_destroy(ctx)
+    return out, lse, c, status, info
+
+
+@pytest.mark.parametrize("name", ["decode_small", "decode_spec_small", "decode_d64"])
+def test_decode_matches_oracle(name):
+    d = device_inputs(name)
+    out, lse, c, status, info = _run_decode(d)
+    assert status == 0
+    sp = d["spec"]
+    assert info["max_qo_len"] == max(sp.qo_lens) and info["max_kv_len"] == max(sp.seq_lens)
+    host = oracle_cache(d)
+    ref_out, ref_lse = oracle_attention(d, host)
+    res = compare_attention(out, lse, ref_out, ref_lse)
+    print(name, info["num_units"], res)
+    assert_within_tolerance(res)
+
+
+def test_decode_splits_long_sequences_into_merged_chunks():
+    """decode_small has a 5000-key sequence: several chunks, merged; its rows
+    must agree with the oracle like the single-chunk ones."""
+    d = device_inputs("decode_small")
+    out, lse, _, status, info = _run_decode(d)
+    assert status == 0
+    sp = d["spec"]
+    # units = sum over sequences of ceil(kv_len / chunk) per kv head, chunk >= 256
+    assert info["num_units"] > sp.num_kv_heads * len(sp.seq_lens)
+    host = oracle_cache(d)
+    ref_out, ref_lse = oracle_attention(d, host)
+    last = int(d["host"]["qo_indptr"][-1]) - 1   # the 5000-key sequence's query row
+    rows = np.array([(last, h) for h in range(sp.num_qo_heads)], np.int64)
+    sel = rows[:, 0] * sp.num_qo_heads + rows[:, 1]
+    res = compare_attention(out, lse, ref_out[sel], ref_lse[sel], rows=rows)
+    assert_within_tolerance(res)
+
+
+def test_decode_plan_limits_and_plan_kinds():
+    m = fi()
+    d = device_inputs("decode_small")
+    sp = d["spec"]
+    ctx = m.fi_context_create()
+    plan = m.fi_plan_create(ctx)
+    qo = np.array([0, 9], np.int32)           # 9 query tokens: more than a decode plan takes
+    kv = np.array([0, 40], np.int32)
+    with pytest.raises(m.FiError):
+        m.fi_decode_plan(plan, qo, kv, d["page_table"][:1], sp.num_qo_heads, sp.num_kv_heads,
+                         sp.head_dim, sp.page_size)
+    m.fi_decode_plan(plan, d["host"]["qo_indptr"], d["host"]["kv_indptr"], d["page_table"],
+                     sp.num_qo_heads, sp.num_kv_heads, sp.head_dim, sp.page_size)
+    c = gpu_cache(d)
+    out = torch.empty_like(d["q"])
+    with pytest.raises(m.FiError):
+        m.fi_prefill_run(plan, d["q"], c, out)     # a decode plan is not a prefill plan
+    m.fi_prefill_plan(plan, d["host"]["qo_indptr"], d["host"]["kv_indptr"], d["page_table"],
+                      sp.num_qo_heads, sp.num_kv_heads, sp.head_dim, sp.page_size)
+    with pytest.raises(m.FiError):
+        m.fi_decode_run(plan, d["q"], c, out)      # and the other way round
+    m.fi_plan_destroy(plan)
+    m.fi_context_destroy(ctx)
+
+
+def test_decode_equals_prefill_path_on_the_same_inputs():
+    """The prefill path also serves decode shapes; both must agree closely."""
+    m = fi()
+    d = device_inputs("decode_spec_small")
+    sp = d["spec"]
+    out_d, lse_d, c, status, _ = _run_decode(d)
+    assert status == 0
+    ctx = m.fi_context_create()
+    plan = m.fi_plan_create(ctx)
+    m.fi_prefill_plan(plan, d["host"]["qo_indptr"], d["host"]["kv_indptr"], d["page_table"],
+                      sp.num_qo_heads, sp.num_kv_heads, sp.head_dim, sp.page_size,
+                      sm_scale=d["sm_scale"])
+    out_p = torch.empty_like(d["q"])
+    lse_p = torch.empty_like(lse_d)
+    m.fi_prefill_run(plan, d["q"], c, out_p, lse_p)
+    assert m.fi_device_status(ctx) == 0
+    assert (out_d.float() - out_p.float()).abs().max().item() <= 2e-2
+    assert (lse_d - lse_p).abs().max().item() <= 1e-3
+    m.fi_plan_destroy(plan)
+    m.fi_context_destroy(ctx)

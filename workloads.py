@@ -38,7 +38,8 @@ class Spec:
     head_dim: int
     page_size: int
     num_qo_heads: int = 0          # 0: append-only workload
-    seq_lens: list = field(default_factory=list)   # qo_len == kv_len per sequence
+    seq_lens: list = field(default_factory=list)   # kv_len per sequence (qo_len too, unless qo_lens)
+    qo_lens: list = field(default_factory=list)    # decode: the newest qo_len tokens query
     append_tokens: int = 0         # append-only workloads
     num_pages: int = 0             # append-only workloads
     skip_fraction: float = 0.0     # fraction of slots set to -1 (append-only)
@@ -91,6 +92,19 @@ def spec(name: str) -> Spec:
     if name == "mha_small_d64":
         return Spec("mha_small_d64", 9000, num_kv_heads=2, head_dim=64, page_size=64,
                     num_qo_heads=2, seq_lens=[70, 200])
+    # Decode: the newest 1..8 tokens of each sequence query its whole cache.
+    if name == "decode":
+        return Spec("decode", 10000, num_kv_heads=8, head_dim=128, page_size=16,
+                    num_qo_heads=32, seq_lens=[4096] * 128, qo_lens=[1] * 128)
+    if name == "decode_small":
+        return Spec("decode_small", 11000, num_kv_heads=2, head_dim=128, page_size=16,
+                    num_qo_heads=8, seq_lens=[1, 40, 300, 1000, 5000], qo_lens=[1] * 5)
+    if name == "decode_spec_small":
+        return Spec("decode_spec_small", 12000, num_kv_heads=2, head_dim=128, page_size=16,
+                    num_qo_heads=8, seq_lens=[8, 130, 700, 2600], qo_lens=[1, 3, 8, 2])
+    if name == "decode_d64":
+        return Spec("decode_d64", 13000, num_kv_heads=4, head_dim=64, page_size=32,
+                    num_qo_heads=8, seq_lens=[257, 1500, 90], qo_lens=[1, 2, 1])
     if name == "uniform_small":
         return Spec("uniform_small", 7000, num_kv_heads=2, head_dim=128, page_size=16,
                     num_qo_heads=8, seq_lens=[384] * 6)
@@ -105,7 +119,8 @@ def sample_spec(name: str, n_seqs: int, seed: int = 0) -> Spec:
     idx = torch.randperm(sp.batch, generator=g)[:min(n_seqs, sp.batch)].tolist()
     return Spec(f"{name}_sample{seed}", sp.seed + 100 + seed, num_kv_heads=sp.num_kv_heads,
                 head_dim=sp.head_dim, page_size=sp.page_size, num_qo_heads=sp.num_qo_heads,
-                seq_lens=[sp.seq_lens[i] for i in sorted(idx)])
+                seq_lens=[sp.seq_lens[i] for i in sorted(idx)],
+                qo_lens=[sp.qo_lens[i] for i in sorted(idx)] if sp.qo_lens else [])
 
 
 def _bf16_normal(shape, gen, device, outlier_p=0.0, outlier_scale=20.0):
@@ -163,9 +178,15 @@ def make(sp: Spec, device="cpu") -> dict:
             page_table[b, pos // ps].to(torch.int64) * ps + pos % ps)
     k = _bf16_normal((total, H, D), gen, device)
     v = _bf16_normal((total, H, D), gen, device)
-    q = _bf16_normal((total, sp.num_qo_heads, D), gen, device)
+    if sp.qo_lens:
+        qlens = torch.tensor(sp.qo_lens, dtype=torch.int64)
+        qo_indptr = torch.zeros(sp.batch + 1, dtype=torch.int64)
+        qo_indptr[1:] = torch.cumsum(qlens, 0)
+    else:
+        qo_indptr = indptr
+    q = _bf16_normal((int(qo_indptr[-1]), sp.num_qo_heads, D), gen, device)
     out.update(k=k, v=v, q=q, slot_mapping=slot_mapping, page_table=page_table,
-               qo_indptr=indptr.to(torch.int32), kv_indptr=indptr.to(torch.int32),
+               qo_indptr=qo_indptr.to(torch.int32), kv_indptr=indptr.to(torch.int32),
                num_pages=num_pages, k_scale=global_scale(k), v_scale=global_scale(v),
                sm_scale=1.0 / math.sqrt(D))
     return out
