@@ -7,16 +7,15 @@
 // j <= t + kv_len - qo_len).
 //
 // Decode rows are few (G * qo_len per KV head) and every key is read once, so
-// the work is HBM-bound and runs on the CUDA cores, not the tensor cores.
-// One warp owns one unit = (sequence, KV head, chunk of keys): each lane
-// dequantizes its own key's K row (E2M1 x E4M3, exact in fp32) and forms the
-// logits of every query row against it (Q rows in shared memory, prescaled
-// by sm_scale * k_scale * log2 e); the online softmax takes warp-wide maxima;
-// for P V every lane owns D/32 output columns of every row and reads its
-// columns of each key's V row from the warp's shared-memory copy of the 32
-// V rows (each lane loads its own key's K and V rows with 16-byte loads).  A
-// sequence whose keys span several chunks writes unnormalized partial results
-// (row max, row sum, O) that a merge kernel combines.
+// the work is HBM-bound.  One warp owns one unit = (sequence, KV head, chunk
+// of keys) and takes its keys 32 at a time: each lane dequantizes its own
+// key's K and V rows into exact fp16 rows in shared memory (E2M1 x E4M3 fits
+// fp16), then the warp computes S = Q K^T and O += P V with m16n8k16
+// warp-level MMAs (fp16 in, fp32 accumulators; Q in registers, scaled by a
+// power of two into fp16 range), the online softmax running on the
+// accumulator fragments.  A sequence whose keys span several chunks writes
+// unnormalized partial results (row max, row sum, O) that a merge kernel
+// combines.
 #include <algorithm>
 
 #include "internal.h"
@@ -62,18 +61,6 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Exact fp32 values of 8 E2M1 codes (one word) times the block's E4M3 scale.
-__device__ __forceinline__ void dequant8_f32(uint32_t w, float sv, float (&x)[8]) {
-  uint32_t h[4];
-  e2m1x8_to_f16x2(w, h);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[k]));
-    x[2 * k] = f.x * sv;
-    x[2 * k + 1] = f.y * sv;
-  }
-}
-
 // Cache row of key `key` of sequence b, KV head hk (page checked).
 __device__ __forceinline__ int64_t key_row(const DecodeParams& p, const int32_t* pt, int key,
                                            int hk) {
@@ -85,15 +72,43 @@ __device__ __forceinline__ int64_t key_row(const DecodeParams& p, const int32_t*
   return (static_cast<int64_t>(page) * p.num_kv_heads + hk) * p.page_size + key % p.page_size;
 }
 
-// RMAX: compile-time bound on the rows (G * qo_len) of a unit.
-// Bytes of one staged V row (codes, then scales), padded to 16.
-template <int D>
-constexpr int kVRow = (D / 2 + D / 16 + 15) / 16 * 16;
+// m16n8k16 MMA with fp16 inputs and fp32 accumulators (the warp-level tensor
+// core path: decode is HBM-bound, so its rate is ample), and the 8x8
+// shared-memory matrix loads that feed it.
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
 
-template <int D, int RMAX>
-__global__ void __launch_bounds__(32 * kDecWarps) nvfp4_decode_kernel(const DecodeParams p) {
-  constexpr int kDpl = D / 32;  // output columns per lane
-  extern __shared__ float dsm[];
+// Bytes of one staged K or V row (fp16), padded so that the eight rows of an
+// 8x8 matrix load fall on distinct banks.
+template <int D>
+constexpr int kRowStride = D * 2 + 16;
+
+// MT: 16-row MMA tiles per unit (rows G * qo_len <= 16 MT).
+template <int D, int MT>
+__global__ void __launch_bounds__(32 * kDecWarps, MT == 1 ? 3 : 2)
+    nvfp4_decode_kernel(const DecodeParams p) {
+  constexpr int kS = kRowStride<D>;
+  extern __shared__ __align__(16) uint8_t dsm[];
   grid_dep_wait();  // Q and the cache may come from the previous grid
   grid_dep_launch();
   const int warp = threadIdx.x / 32;
@@ -106,173 +121,245 @@ __global__ void __launch_bounds__(32 * kDecWarps) nvfp4_decode_kernel(const Deco
   const int qo_len = __ldg(p.qo_indptr + b + 1) - qo_start;
   const int kv_len = __ldg(p.kv_indptr + b + 1) - __ldg(p.kv_indptr + b);
   const int G = p.group;
-  const int R = G * qo_len;  // <= RMAX (the planner guarantees it)
+  const int R = G * qo_len;  // <= 16 MT (the planner guarantees it)
   const int delta = kv_len - qo_len;
   const int k0 = c * p.chunk;
   const int k1 = min(k0 + p.chunk, kv_len);
   const float ks = __ldg(p.k_scale), vs = __ldg(p.v_scale);
-  // Q rows (row r = token r / G, head hk * G + r % G) prescaled to log2 units;
-  // after all warps' Q rows: each warp's 32 V rows (codes, then scales)
-  float* sq = dsm + warp * RMAX * D;
-  uint8_t* svr = reinterpret_cast<uint8_t*>(dsm + kDecWarps * RMAX * D) +
-                 warp * 32 * kVRow<D>;
-  const float qs = p.sm_scale * ks * 1.4426950408889634f;
-  for (int i = lane; i < R * (D / 8); i += 32) {
-    const int r = i / (D / 8), ch = i % (D / 8);
-    const int t = r / G, g = r % G;
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-        p.q + (static_cast<int64_t>(qo_start + t) * p.num_qo_heads + hk * G + g) * D + ch * 8));
-    float x[8];
-    bf16x8_to_f32(v, x);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) sq[r * D + ch * 8 + e] = x[e] * qs;
-  }
-  __syncwarp();
+  uint8_t* sk = dsm + warp * 2 * 32 * kS;  // this warp's 32 staged K rows, then V rows
+  uint8_t* sv = sk + 32 * kS;
+  const uint32_t sk_addr = smem_u32(sk), sv_addr = smem_u32(sv);
   const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.pt_stride;
+  auto q_ptr = [&](int r) {  // row r = token r / G, head hk * G + r % G
+    return p.q + (static_cast<int64_t>(qo_start + r / G) * p.num_qo_heads + hk * G + r % G) * D;
+  };
 
-  float m[RMAX], l[RMAX], o[RMAX][kDpl];
+  // Q as fp16 A fragments: Q * sm_scale * k_scale * log2 e * 2^-e with e
+  // chosen so that every |value| < 2^14 (a power of two: exact); the logits
+  // are multiplied back by 2^e.
+  const float qs = p.sm_scale * ks * 1.4426950408889634f;
+  float qmax = 0.0f;
+  for (int i = lane; i < R * (D / 8); i += 32) {
+    float x[8];
+    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(q_ptr(i / (D / 8)) + (i % (D / 8)) * 8)), x);
 #pragma unroll
-  for (int r = 0; r < RMAX; ++r) {
-    m[r] = -INFINITY;
-    l[r] = 0.0f;
-#pragma unroll
-    for (int e = 0; e < kDpl; ++e) o[r][e] = 0.0f;
+    for (int e = 0; e < 8; ++e) qmax = fmaxf(qmax, fabsf(x[e]));
   }
+  qmax = warp_max(qmax) * qs;
+  const int qe = qmax > 0.0f ? ilogbf(qmax) - 13 : 0;
+  const float qsc = ldexpf(qs, -qe);
+  const float ssc = ldexpf(1.0f, qe);
+  uint32_t qa[MT][D / 16][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    const int r0 = 16 * mt + lane / 4, r1 = r0 + 8;
+#pragma unroll
+    for (int s = 0; s < D / 16; ++s) {
+      const int d0 = 16 * s + 2 * (lane % 4);
+      float v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = 0.0f;
+      if (r0 < R) {
+        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(q_ptr(r0) + d0);
+        const __nv_bfloat162 bb = *reinterpret_cast<const __nv_bfloat162*>(q_ptr(r0) + d0 + 8);
+        v[0] = __low2float(a) * qsc;
+        v[1] = __high2float(a) * qsc;
+        v[4] = __low2float(bb) * qsc;
+        v[5] = __high2float(bb) * qsc;
+      }
+      if (r1 < R) {
+        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(q_ptr(r1) + d0);
+        const __nv_bfloat162 bb = *reinterpret_cast<const __nv_bfloat162*>(q_ptr(r1) + d0 + 8);
+        v[2] = __low2float(a) * qsc;
+        v[3] = __high2float(a) * qsc;
+        v[6] = __low2float(bb) * qsc;
+        v[7] = __high2float(bb) * qsc;
+      }
+      qa[mt][s][0] = f16x2_of(v[0], v[1]);
+      qa[mt][s][1] = f16x2_of(v[2], v[3]);
+      qa[mt][s][2] = f16x2_of(v[4], v[5]);
+      qa[mt][s][3] = f16x2_of(v[6], v[7]);
+    }
+  }
+
+  float o[MT][D / 8][4];
+  float mrow[MT][2], lrow[MT][2];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      mrow[mt][h] = -INFINITY;
+      lrow[mt][h] = 0.0f;
+    }
+#pragma unroll
+    for (int nd = 0; nd < D / 8; ++nd)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[mt][nd][e] = 0.0f;
+  }
+
   for (int kb = k0; kb < k1; kb += 32) {
-    const int key = kb + lane;
-    const bool kvalid = key < k1;
-    // ---- logits of every row against this lane's key
-    float s[RMAX];
+    // ---- stage this lane's key: K and V rows as exact fp16 (zeros past k1)
+    __syncwarp();  // the previous batch's rows have been read
+    {
+      uint4* dk = reinterpret_cast<uint4*>(sk + lane * kS);
+      uint4* dv = reinterpret_cast<uint4*>(sv + lane * kS);
+      const int key = kb + lane;
+      if (key < k1) {
+        const int64_t row = key_row(p, pt, key, hk);
+        const uint4* kg = reinterpret_cast<const uint4*>(p.k_data + row * (D / 2));
+        const uint4* vg = reinterpret_cast<const uint4*>(p.v_data + row * (D / 2));
+        uint4 kc4[D / 32], vc4[D / 32];
+        uint32_t ksf4[D / 64], vsf4[D / 64];
 #pragma unroll
-    for (int r = 0; r < RMAX; ++r) s[r] = 0.0f;
-    // this lane's key: its K and V rows with 16-byte loads (one page lookup);
-    // the V row goes to the warp's staging area for the P V step
-    __syncwarp();  // the previous batch's V rows have been read
-    if (kvalid) {
-      const int64_t row = key_row(p, pt, key, hk);
-      uint4 kc4[D / 32], vc4[D / 32];
-      uint32_t ksf4[D / 64], vsf4[D / 64];
-      const uint4* kg = reinterpret_cast<const uint4*>(p.k_data + row * (D / 2));
-      const uint4* vg = reinterpret_cast<const uint4*>(p.v_data + row * (D / 2));
+        for (int i = 0; i < D / 32; ++i) {
+          kc4[i] = __ldg(kg + i);
+          vc4[i] = __ldg(vg + i);
+        }
 #pragma unroll
-      for (int i = 0; i < D / 32; ++i) {
-        kc4[i] = __ldg(kg + i);
-        vc4[i] = __ldg(vg + i);
+        for (int i = 0; i < D / 64; ++i) {
+          ksf4[i] = __ldg(reinterpret_cast<const uint32_t*>(p.k_sf + row * (D / 16)) + i);
+          vsf4[i] = __ldg(reinterpret_cast<const uint32_t*>(p.v_sf + row * (D / 16)) + i);
+        }
+        const uint32_t* kc = reinterpret_cast<const uint32_t*>(kc4);
+        const uint32_t* vc = reinterpret_cast<const uint32_t*>(vc4);
+#pragma unroll
+        for (int blk = 0; blk < D / 16; ++blk) {
+          const uint32_t s8k = (ksf4[blk / 4] >> (8 * (blk % 4))) & 0xFFu;
+          const uint32_t s8v = (vsf4[blk / 4] >> (8 * (blk % 4))) & 0xFFu;
+          dk[2 * blk] = dequant8_f16(kc[2 * blk], s8k);
+          dk[2 * blk + 1] = dequant8_f16(kc[2 * blk + 1], s8k);
+          dv[2 * blk] = dequant8_f16(vc[2 * blk], s8v);
+          dv[2 * blk + 1] = dequant8_f16(vc[2 * blk + 1], s8v);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) dk[i] = dv[i] = make_uint4(0u, 0u, 0u, 0u);
       }
+    }
+    __syncwarp();  // every lane's rows are staged
+
+    // ---- S = Q K^T for the 32 keys (4 n-tiles of 8 keys, D/16 k-steps)
+    float sacc[MT][4][4];
 #pragma unroll
-      for (int i = 0; i < D / 64; ++i) {
-        ksf4[i] = __ldg(reinterpret_cast<const uint32_t*>(p.k_sf + row * (D / 16)) + i);
-        vsf4[i] = __ldg(reinterpret_cast<const uint32_t*>(p.v_sf + row * (D / 16)) + i);
-      }
-      uint8_t* dst = svr + lane * kVRow<D>;
+    for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-      for (int i = 0; i < D / 32; ++i) reinterpret_cast<uint4*>(dst)[i] = vc4[i];
+      for (int j = 0; j < 4; ++j)
 #pragma unroll
-      for (int i = 0; i < D / 64; ++i) reinterpret_cast<uint32_t*>(dst + D / 2)[i] = vsf4[i];
-      const uint32_t* kc = reinterpret_cast<const uint32_t*>(kc4);
+        for (int e = 0; e < 4; ++e) sacc[mt][j][e] = 0.0f;
 #pragma unroll
-      for (int blk = 0; blk < D / 16; ++blk) {
-        const float sv = e4m3_value((ksf4[blk / 4] >> (8 * (blk % 4))) & 0xFFu);
+    for (int j = 0; j < 4; ++j) {
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float kx[8];
-          dequant8_f32(kc[2 * blk + half], sv, kx);
-          const int d0 = blk * 16 + half * 8;
+      for (int s2 = 0; s2 < D / 32; ++s2) {
+        uint32_t bq[4];  // k-steps 2 s2 and 2 s2 + 1 of keys 8j .. 8j+7
+        ldsm_x4(sk_addr + (8 * j + lane % 8) * kS + (32 * s2 + 8 * (lane / 8)) * 2, bq);
 #pragma unroll
-          for (int r = 0; r < RMAX; ++r) {
-            if (r < R) {
-              const float4 qa = *reinterpret_cast<const float4*>(sq + r * D + d0);
-              const float4 qb = *reinterpret_cast<const float4*>(sq + r * D + d0 + 4);
-              s[r] = fmaf(qa.x, kx[0], s[r]);
-              s[r] = fmaf(qa.y, kx[1], s[r]);
-              s[r] = fmaf(qa.z, kx[2], s[r]);
-              s[r] = fmaf(qa.w, kx[3], s[r]);
-              s[r] = fmaf(qb.x, kx[4], s[r]);
-              s[r] = fmaf(qb.y, kx[5], s[r]);
-              s[r] = fmaf(qb.z, kx[6], s[r]);
-              s[r] = fmaf(qb.w, kx[7], s[r]);
-            }
-          }
+        for (int mt = 0; mt < MT; ++mt) {
+          mma16816(sacc[mt][j], qa[mt][2 * s2], bq[0], bq[1]);
+          mma16816(sacc[mt][j], qa[mt][2 * s2 + 1], bq[2], bq[3]);
         }
       }
     }
-    // ---- causal mask, online softmax (row statistics are warp-uniform)
-    float pr[RMAX];
+
+    // ---- causal mask and online softmax; rows r0 = 16 mt + lane/4 (h = 0)
+    // and r0 + 8 (h = 1), keys kb + 8j + 2(lane%4) + e
 #pragma unroll
-    for (int r = 0; r < RMAX; ++r) {
-      if (r < R) {
-        const bool vis = kvalid && key <= delta + r / G;
-        const float sr = vis ? s[r] : -INFINITY;
-        const float m_new = fmaxf(m[r], warp_max(sr));
-        const float alpha = m_new == -INFINITY ? 1.0f : ex2_approx(m[r] - m_new);
-        pr[r] = vis ? ex2_approx(sr - m_new) : 0.0f;
-        l[r] = l[r] * alpha + pr[r];
+    for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
-        for (int e = 0; e < kDpl; ++e) o[r][e] *= alpha;
-        m[r] = m_new;
-      } else {
-        pr[r] = 0.0f;
+      for (int h = 0; h < 2; ++h) {
+        const int r = 16 * mt + lane / 4 + 8 * h;
+        const int lim = r < R ? min(k1 - 1, delta + r / G) : -1;  // last visible key
+        float mx = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int key = kb + 8 * j + 2 * (lane % 4) + e;
+            const float x = key <= lim ? sacc[mt][j][2 * h + e] * ssc : -INFINITY;
+            sacc[mt][j][2 * h + e] = x;
+            mx = fmaxf(mx, x);
+          }
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+        const float m_new = fmaxf(mrow[mt][h], mx);
+        const float alpha = m_new == -INFINITY ? 1.0f : ex2_approx(mrow[mt][h] - m_new);
+        float psum = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float x = sacc[mt][j][2 * h + e];
+            const float pv = x == -INFINITY ? 0.0f : ex2_approx(x - m_new);
+            sacc[mt][j][2 * h + e] = pv;
+            psum += pv;
+          }
+        lrow[mt][h] = lrow[mt][h] * alpha + psum;
+        mrow[mt][h] = m_new;
+#pragma unroll
+        for (int nd = 0; nd < D / 8; ++nd) {
+          o[mt][nd][2 * h] *= alpha;
+          o[mt][nd][2 * h + 1] *= alpha;
+        }
       }
     }
-    // ---- O += P V: this lane's columns of each key's V row
-    __syncwarp();  // every lane's V row is staged
-    const int nk = min(32, k1 - kb);
-#pragma unroll 4
-    for (int kk = 0; kk < nk; ++kk) {
-      const uint8_t* vrow = svr + kk * kVRow<D>;
-      const uint8_t* vc = vrow + lane * (kDpl / 2);
-      const float sv = e4m3_value(vrow[D / 2 + (lane * kDpl) / 16]);
-      float vx[kDpl];
-      if constexpr (kDpl == 4) {
-        const uint32_t two = *reinterpret_cast<const uint16_t*>(vc);
-        uint32_t h[4];
-        e2m1x8_to_f16x2(two, h);
-        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&h[0]));
-        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&h[1]));
-        vx[0] = f0.x * sv;
-        vx[1] = f0.y * sv;
-        vx[2] = f1.x * sv;
-        vx[3] = f1.y * sv;
-      } else {
-        const uint32_t one = *vc;
-        uint32_t h[4];
-        e2m1x8_to_f16x2(one, h);
-        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&h[0]));
-        vx[0] = f0.x * sv;
-        vx[1] = f0.y * sv;
+
+    // ---- O += P V (k-steps of 16 keys, n-tiles of 8 columns)
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      uint32_t pa[MT][4];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        pa[mt][0] = f16x2_of(sacc[mt][2 * kk][0], sacc[mt][2 * kk][1]);
+        pa[mt][1] = f16x2_of(sacc[mt][2 * kk][2], sacc[mt][2 * kk][3]);
+        pa[mt][2] = f16x2_of(sacc[mt][2 * kk + 1][0], sacc[mt][2 * kk + 1][1]);
+        pa[mt][3] = f16x2_of(sacc[mt][2 * kk + 1][2], sacc[mt][2 * kk + 1][3]);
       }
 #pragma unroll
-      for (int r = 0; r < RMAX; ++r) {
-        if (r < R) {
-          const float pk = __shfl_sync(0xFFFFFFFFu, pr[r], kk);
+      for (int nd2 = 0; nd2 < D / 16; ++nd2) {
+        uint32_t bv[4];  // n-tiles 2 nd2 and 2 nd2 + 1, keys 16 kk .. 16 kk + 15
+        const int m = lane / 8;
+        ldsm_x4_t(sv_addr + (16 * kk + 8 * (m & 1) + lane % 8) * kS + (16 * nd2 + 8 * (m >> 1)) * 2,
+                  bv);
 #pragma unroll
-          for (int e = 0; e < kDpl; ++e) o[r][e] = fmaf(pk, vx[e], o[r][e]);
+        for (int mt = 0; mt < MT; ++mt) {
+          mma16816(o[mt][2 * nd2], pa[mt], bv[0], bv[1]);
+          mma16816(o[mt][2 * nd2 + 1], pa[mt], bv[2], bv[3]);
         }
       }
     }
   }
+
   // ---- results: the whole sequence in this unit, or a partial slot
 #pragma unroll
-  for (int r = 0; r < RMAX; ++r) {
-    if (r < R) {
-      const float lr = warp_sum(l[r]);
-      const int t = r / G, g = r % G;
-      if (slot < 0) {
-        const int64_t orow = static_cast<int64_t>(qo_start + t) * p.num_qo_heads + hk * G + g;
-        const float inv = vs / lr;
-        __nv_bfloat16* dst = p.out + orow * D + lane * kDpl;
+  for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
-        for (int e = 0; e < kDpl; e += 2)
-          *reinterpret_cast<__nv_bfloat162*>(dst + e) =
-              __floats2bfloat162_rn(o[r][e] * inv, o[r][e + 1] * inv);
-        if (p.lse && lane == 0) p.lse[orow] = (m[r] + log2f(lr)) * 0.6931471805599453f;
+    for (int h = 0; h < 2; ++h) {
+      float lsum = lrow[mt][h];
+      lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 1);
+      lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 2);
+      const int r = 16 * mt + lane / 4 + 8 * h;
+      if (r >= R) continue;
+      const int col = 2 * (lane % 4);
+      if (slot < 0) {
+        const int64_t orow =
+            static_cast<int64_t>(qo_start + r / G) * p.num_qo_heads + hk * G + r % G;
+        const float inv = vs / lsum;
+        __nv_bfloat16* dst = p.out + orow * D + col;
+#pragma unroll
+        for (int nd = 0; nd < D / 8; ++nd)
+          *reinterpret_cast<__nv_bfloat162*>(dst + 8 * nd) =
+              __floats2bfloat162_rn(o[mt][nd][2 * h] * inv, o[mt][nd][2 * h + 1] * inv);
+        if (p.lse && lane % 4 == 0)
+          p.lse[orow] = (mrow[mt][h] + log2f(lsum)) * 0.6931471805599453f;
       } else {
         float* dst = p.part + (static_cast<int64_t>(slot) * p.rows + r) * (D + 2);
 #pragma unroll
-        for (int e = 0; e < kDpl; ++e) dst[lane * kDpl + e] = o[r][e];
-        if (lane == 0) {
-          dst[D] = m[r];
-          dst[D + 1] = lr;
+        for (int nd = 0; nd < D / 8; ++nd) {
+          dst[8 * nd + col] = o[mt][nd][2 * h];
+          dst[8 * nd + col + 1] = o[mt][nd][2 * h + 1];
+        }
+        if (lane % 4 == 0) {
+          dst[D] = mrow[mt][h];
+          dst[D + 1] = lsum;
         }
       }
     }
@@ -323,11 +410,10 @@ __global__ void __launch_bounds__(128) nvfp4_decode_merge_kernel(const DecodePar
   if (p.lse && lane == 0) p.lse[orow] = (M + log2f(L)) * 0.6931471805599453f;
 }
 
-template <int D, int RMAX>
+template <int D, int MT>
 fi_status launch_decode_impl(const DecodeParams& p, cudaStream_t stream) {
-  const int smem = kDecWarps * RMAX * D * static_cast<int>(sizeof(float)) +
-                   kDecWarps * 32 * kVRow<D>;
-  auto kern = nvfp4_decode_kernel<D, RMAX>;
+  const int smem = kDecWarps * 2 * 32 * kRowStride<D>;
+  auto kern = nvfp4_decode_kernel<D, MT>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
     return FI_ERR_CUDA;
@@ -374,9 +460,9 @@ fi_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.sm_scale = P.sm_scale;
   p.status = a.status;
   const int D = P.head_dim;
-  if (P.dec_rows <= 8)
-    return D == 128 ? launch_decode_impl<128, 8>(p, stream) : launch_decode_impl<64, 8>(p, stream);
-  return D == 128 ? launch_decode_impl<128, 32>(p, stream) : launch_decode_impl<64, 32>(p, stream);
+  if (P.dec_rows <= 16)
+    return D == 128 ? launch_decode_impl<128, 1>(p, stream) : launch_decode_impl<64, 1>(p, stream);
+  return D == 128 ? launch_decode_impl<128, 2>(p, stream) : launch_decode_impl<64, 2>(p, stream);
 }
 
 }  // namespace fi
