@@ -104,8 +104,27 @@ __global__ void __launch_bounds__(kAppendThreads, kCtasPerSm)
   constexpr int kTpr = kBlocks / BPT;  // threads per (token, tensor, head) row
   constexpr int kTokPerCta = kAppendThreads / kTpr;
   __shared__ float4 tab[128];
-  // Inputs may come from the previous grid of the stream (programmatic
-  // dependent launch): wait for it, then let the next grid start launching.
+  const int64_t step = static_cast<int64_t>(gridDim.x) * kTokPerCta;
+  {
+    // While the previous grid of the stream finishes (programmatic dependent
+    // launch), pull this CTA's K or V row segments into L2: the tokens
+    // blockIdx.x * kTokPerCta + r + k * step of (tensor, head) blockIdx.y.
+    // Only kernel parameters are read here, and a prefetch cannot change what
+    // the loads after the wait see.
+    const int Hp = p.num_kv_heads;
+    const int tp = static_cast<int>(blockIdx.y) >= Hp ? 1 : 0;
+    const __nv_bfloat16* src = (tp ? p.v : p.k) + (static_cast<int>(blockIdx.y) - tp * Hp) * D;
+    const int64_t ts = tp ? p.v_tok_stride : p.k_tok_stride;
+    if (((reinterpret_cast<uintptr_t>(src) | static_cast<uintptr_t>(ts * 2)) & 15u) == 0) {
+      constexpr int kRowsPerPass = kAppendThreads / kTokPerCta;
+      for (int64_t tok = static_cast<int64_t>(blockIdx.x) * kTokPerCta + threadIdx.x % kTokPerCta +
+                         (threadIdx.x / kTokPerCta) * step;
+           tok < p.num_tokens; tok += kRowsPerPass * step)
+        prefetch_l2_bulk(src + tok * ts, D * 2);
+    }
+  }
+  // Inputs may come from the previous grid of the stream: wait for it, then
+  // let the next grid start launching.
   grid_dep_wait();
   grid_dep_launch();
 
@@ -138,7 +157,6 @@ __global__ void __launch_bounds__(kAppendThreads, kCtasPerSm)
   const uint32_t pmask = (1u << p.log2_page_size) - 1u;
   const uint64_t num_slots = static_cast<uint64_t>(p.num_slots);
   const bool report_oob = t == 0 && h == 0 && j == 0;  // one report per token
-  const int64_t step = static_cast<int64_t>(gridDim.x) * kTokPerCta;
   int64_t tok = static_cast<int64_t>(blockIdx.x) * kTokPerCta + threadIdx.x / kTpr;
   // Persistent over token groups: the next group's slot and values are
   // loaded before the current group is quantized and stored, so every thread
