@@ -8,9 +8,10 @@
 //
 // Decode rows are few (G * qo_len per KV head) and every key is read once, so
 // the work is HBM-bound.  One warp owns one unit = (sequence, KV head, chunk
-// of keys) and takes its keys 32 at a time: each lane dequantizes its own
-// key's K and V rows into exact fp16 rows in shared memory (E2M1 x E4M3 fits
-// fp16), then the warp computes S = Q K^T and O += P V with m16n8k16
+// of keys) and takes its keys 32 at a time: each lane copies its own key's
+// raw K and V rows (codes and block scales) into a two-step ring in shared
+// memory two steps ahead (cp.async), dequantizes them into exact fp16 rows
+// (E2M1 x E4M3 fits fp16), then the warp computes S = Q K^T and O += P V with m16n8k16
 // warp-level MMAs (fp16 in, fp32 accumulators; Q in registers, scaled by a
 // power of two into fp16 range), the online softmax running on the
 // accumulator fragments.  A sequence whose keys span several chunks writes
@@ -25,7 +26,8 @@ namespace fi {
 
 namespace {
 
-constexpr int kDecWarps = 4;  // warps (units) per CTA
+constexpr int kDecWarps = 4;   // warps (units) per CTA
+constexpr int kDecStages = 2;  // raw rows in flight per warp: this step's and the next
 
 struct DecodeParams {
   const __nv_bfloat16* q;
@@ -54,22 +56,6 @@ __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
   return v;
-}
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-  return v;
-}
-
-// Cache row of key `key` of sequence b, KV head hk (page checked).
-__device__ __forceinline__ int64_t key_row(const DecodeParams& p, const int32_t* pt, int key,
-                                           int hk) {
-  int page = __ldg(pt + key / p.page_size);
-  if (page < 0 || page >= p.num_pages) {
-    atomicOr(p.status, FI_DEV_PAGE_OOB);
-    page = 0;
-  }
-  return (static_cast<int64_t>(page) * p.num_kv_heads + hk) * p.page_size + key % p.page_size;
 }
 
 // m16n8k16 MMA with fp16 inputs and fp32 accumulators (the warp-level tensor
@@ -102,12 +88,21 @@ __device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
 // 8x8 matrix load fall on distinct banks.
 template <int D>
 constexpr int kRowStride = D * 2 + 16;
+// Bytes of one lane's raw rows in the ring: K codes, V codes, K scales, V
+// scales (D/2, D/2, D/16, D/16), padded to a multiple of 16.
+template <int D>
+constexpr int kLaneRaw = (D + D / 8 + 15) / 16 * 16;
+template <int D>
+constexpr int decode_smem_bytes() {
+  return kDecWarps * (2 * 32 * kRowStride<D> + kDecStages * 32 * kLaneRaw<D>);
+}
 
 // MT: 16-row MMA tiles per unit (rows G * qo_len <= 16 MT).
 template <int D, int MT>
-__global__ void __launch_bounds__(32 * kDecWarps, MT == 1 ? 3 : 2)
+__global__ void __launch_bounds__(32 * kDecWarps, 2)
     nvfp4_decode_kernel(const DecodeParams p) {
   constexpr int kS = kRowStride<D>;
+  constexpr int kLR = kLaneRaw<D>;
   extern __shared__ __align__(16) uint8_t dsm[];
   grid_dep_wait();  // Q and the cache may come from the previous grid
   grid_dep_launch();
@@ -129,6 +124,8 @@ __global__ void __launch_bounds__(32 * kDecWarps, MT == 1 ? 3 : 2)
   uint8_t* sk = dsm + warp * 2 * 32 * kS;  // this warp's 32 staged K rows, then V rows
   uint8_t* sv = sk + 32 * kS;
   const uint32_t sk_addr = smem_u32(sk), sv_addr = smem_u32(sv);
+  // this warp's raw ring: stage st, lane l at (st * 32 + l) * kLR
+  uint8_t* raw = dsm + kDecWarps * 2 * 32 * kS + warp * kDecStages * 32 * kLR;
   const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.pt_stride;
   auto q_ptr = [&](int r) {  // row r = token r / G, head hk * G + r % G
     return p.q + (static_cast<int64_t>(qo_start + r / G) * p.num_qo_heads + hk * G + r % G) * D;
@@ -197,28 +194,65 @@ __global__ void __launch_bounds__(32 * kDecWarps, MT == 1 ? 3 : 2)
       for (int e = 0; e < 4; ++e) o[mt][nd][e] = 0.0f;
   }
 
-  for (int kb = k0; kb < k1; kb += 32) {
+  // Raw rows of key kbs + lane into ring stage st (one commit group per call,
+  // empty past the chunk).  The page id comes from the previous call, so the
+  // page-table read is one step ahead of the copies that need it.
+  auto page_of = [&](int key) { return key < k1 ? __ldg(pt + key / p.page_size) : 0; };
+  int page_next = page_of(k0 + lane);
+  auto issue = [&](int kbs, int st) {
+    const int key = kbs + lane;
+    int page = page_next;
+    page_next = page_of(key + 32);
+    if (key < k1) {
+      if (page < 0 || page >= p.num_pages) {
+        atomicOr(p.status, FI_DEV_PAGE_OOB);
+        page = 0;
+      }
+      const int64_t row =
+          (static_cast<int64_t>(page) * p.num_kv_heads + hk) * p.page_size + key % p.page_size;
+      uint8_t* dst = raw + (st * 32 + lane) * kLR;
+      const uint8_t* kg = p.k_data + row * (D / 2);
+      const uint8_t* vg = p.v_data + row * (D / 2);
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) {
+        cp_async16(dst + 16 * i, kg + 16 * i);
+        cp_async16(dst + D / 2 + 16 * i, vg + 16 * i);
+      }
+      if constexpr (D == 128) {
+        cp_async8(dst + D, p.k_sf + row * (D / 16));
+        cp_async8(dst + D + D / 16, p.v_sf + row * (D / 16));
+      } else {
+        cp_async4(dst + D, p.k_sf + row * (D / 16));
+        cp_async4(dst + D + D / 16, p.v_sf + row * (D / 16));
+      }
+    }
+    cp_async_commit();
+  };
+  issue(k0, 0);
+  issue(k0 + 32, 1);
+
+  int st = 0;
+  for (int kb = k0; kb < k1; kb += 32, st ^= 1) {
     // ---- stage this lane's key: K and V rows as exact fp16 (zeros past k1)
-    __syncwarp();  // the previous batch's rows have been read
+    cp_async_wait<1>();  // this lane's raw rows of this step have landed
+    __syncwarp();        // the previous batch's rows have been read
     {
       uint4* dk = reinterpret_cast<uint4*>(sk + lane * kS);
       uint4* dv = reinterpret_cast<uint4*>(sv + lane * kS);
       const int key = kb + lane;
       if (key < k1) {
-        const int64_t row = key_row(p, pt, key, hk);
-        const uint4* kg = reinterpret_cast<const uint4*>(p.k_data + row * (D / 2));
-        const uint4* vg = reinterpret_cast<const uint4*>(p.v_data + row * (D / 2));
+        const uint8_t* src = raw + (st * 32 + lane) * kLR;
         uint4 kc4[D / 32], vc4[D / 32];
         uint32_t ksf4[D / 64], vsf4[D / 64];
 #pragma unroll
         for (int i = 0; i < D / 32; ++i) {
-          kc4[i] = __ldg(kg + i);
-          vc4[i] = __ldg(vg + i);
+          kc4[i] = reinterpret_cast<const uint4*>(src)[i];
+          vc4[i] = reinterpret_cast<const uint4*>(src + D / 2)[i];
         }
 #pragma unroll
         for (int i = 0; i < D / 64; ++i) {
-          ksf4[i] = __ldg(reinterpret_cast<const uint32_t*>(p.k_sf + row * (D / 16)) + i);
-          vsf4[i] = __ldg(reinterpret_cast<const uint32_t*>(p.v_sf + row * (D / 16)) + i);
+          ksf4[i] = reinterpret_cast<const uint32_t*>(src + D)[i];
+          vsf4[i] = reinterpret_cast<const uint32_t*>(src + D + D / 16)[i];
         }
         const uint32_t* kc = reinterpret_cast<const uint32_t*>(kc4);
         const uint32_t* vc = reinterpret_cast<const uint32_t*>(vc4);
@@ -237,6 +271,8 @@ __global__ void __launch_bounds__(32 * kDecWarps, MT == 1 ? 3 : 2)
       }
     }
     __syncwarp();  // every lane's rows are staged
+    // the raw stage just read takes the rows of the step after next
+    issue(kb + 64, st);
 
     // ---- S = Q K^T for the 32 keys (4 n-tiles of 8 keys, D/16 k-steps)
     float sacc[MT][4][4];
@@ -328,6 +364,8 @@ __global__ void __launch_bounds__(32 * kDecWarps, MT == 1 ? 3 : 2)
     }
   }
 
+  cp_async_wait<0>();  // (every copy was consumed; nothing is left in flight)
+
   // ---- results: the whole sequence in this unit, or a partial slot
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
@@ -412,7 +450,7 @@ __global__ void __launch_bounds__(128) nvfp4_decode_merge_kernel(const DecodePar
 
 template <int D, int MT>
 fi_status launch_decode_impl(const DecodeParams& p, cudaStream_t stream) {
-  const int smem = kDecWarps * 2 * 32 * kRowStride<D>;
+  const int smem = decode_smem_bytes<D>();
   auto kern = nvfp4_decode_kernel<D, MT>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
