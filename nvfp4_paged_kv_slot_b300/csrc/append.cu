@@ -28,6 +28,9 @@ namespace {
 
 constexpr int kAppendThreads = 256;
 constexpr int kCtasPerSm = 3;  // resident CTAs per SM the persistent grid aims for
+// Passes of the direct kernel whose input rows are pulled into L2 before the
+// grid-dependency wait (measured: 2 beats 1, 3 and all).
+constexpr int kPrefetchPasses = 2;
 constexpr int kDirectBlocksPerThread = 2;
 
 // Staged kernel: 16 consumer warps and one producer warp; stages of about
@@ -107,19 +110,22 @@ __global__ void __launch_bounds__(kAppendThreads, kCtasPerSm)
   const int64_t step = static_cast<int64_t>(gridDim.x) * kTokPerCta;
   {
     // While the previous grid of the stream finishes (programmatic dependent
-    // launch), pull this CTA's K or V row segments into L2: the tokens
-    // blockIdx.x * kTokPerCta + r + k * step of (tensor, head) blockIdx.y.
-    // Only kernel parameters are read here, and a prefetch cannot change what
-    // the loads after the wait see.
+    // launch), pull the K or V row segments of this CTA's first
+    // kPrefetchPasses passes into L2: the tokens blockIdx.x * kTokPerCta + r
+    // + k * step, k < kPrefetchPasses, of (tensor, head) blockIdx.y.  Only
+    // kernel parameters are read here, and a prefetch cannot change what the
+    // loads after the wait see.  (Prefetching every pass queued the whole
+    // input ahead of the first real loads and was slower.)
     const int Hp = p.num_kv_heads;
     const int tp = static_cast<int>(blockIdx.y) >= Hp ? 1 : 0;
     const __nv_bfloat16* src = (tp ? p.v : p.k) + (static_cast<int>(blockIdx.y) - tp * Hp) * D;
     const int64_t ts = tp ? p.v_tok_stride : p.k_tok_stride;
     if (((reinterpret_cast<uintptr_t>(src) | static_cast<uintptr_t>(ts * 2)) & 15u) == 0) {
       constexpr int kRowsPerPass = kAppendThreads / kTokPerCta;
-      for (int64_t tok = static_cast<int64_t>(blockIdx.x) * kTokPerCta + threadIdx.x % kTokPerCta +
-                         (threadIdx.x / kTokPerCta) * step;
-           tok < p.num_tokens; tok += kRowsPerPass * step)
+      const int64_t first = static_cast<int64_t>(blockIdx.x) * kTokPerCta;
+      const int64_t end = min(p.num_tokens, first + kPrefetchPasses * step);
+      for (int64_t tok = first + threadIdx.x % kTokPerCta + (threadIdx.x / kTokPerCta) * step;
+           tok < end; tok += kRowsPerPass * step)
         prefetch_l2_bulk(src + tok * ts, D * 2);
     }
   }
