@@ -266,6 +266,22 @@ fi_status fi_prefill_plan_host(const int32_t* qo_indptr_host, const int32_t* kv_
                                const fi_plan_options* opts, fi_plan_info* info,
                                int32_t* work_out, int64_t work_capacity);
 
+/* Host-only decode planning, for inspection and tests (the decision
+ * fi_decode_plan makes for the same arguments on a GPU with `num_sms` SMs):
+ * fills `info`, *chunk_out (keys per unit: the smallest power of two from
+ * 256 to 16384 that keeps the units at most 32 per SM) and *num_merges_out,
+ * and, when the pointers are non-NULL, up to `unit_capacity` units as 4 int32
+ * each (sequence, KV head, chunk index, partial slot or -1 when the sequence
+ * has one chunk) in launch order, and up to `merge_capacity` merge items as 4
+ * int32 each (sequence, KV head, first partial slot, number of chunks).
+ * Makes no CUDA call.  Errors as fi_decode_plan. */
+fi_status fi_decode_plan_host(const int32_t* qo_indptr_host, const int32_t* kv_indptr_host,
+                              int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
+                              int32_t head_dim, int32_t page_size, int32_t num_sms,
+                              fi_plan_info* info, int32_t* chunk_out, int64_t* num_merges_out,
+                              int32_t* units_out, int64_t unit_capacity, int32_t* merges_out,
+                              int64_t merge_capacity);
+
 /* Plans and runs the causal prefill in one call without allocating memory
  * (no cudaMalloc, no host heap), for callers that cannot allocate while they
  * run — a serving engine that reserves all device memory for its KV cache up

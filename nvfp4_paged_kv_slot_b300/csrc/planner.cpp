@@ -324,6 +324,36 @@ fi_status plan_decode_host(const int32_t* qo_indptr, const int32_t* kv_indptr, i
 
 }  // namespace fi
 
+extern "C" fi_status fi_decode_plan_host(const int32_t* qo_indptr_host,
+                                         const int32_t* kv_indptr_host, int32_t batch,
+                                         int32_t num_qo_heads, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t page_size, int32_t num_sms,
+                                         fi_plan_info* info, int32_t* chunk_out,
+                                         int64_t* num_merges_out, int32_t* units_out,
+                                         int64_t unit_capacity, int32_t* merges_out,
+                                         int64_t merge_capacity) {
+  if (!info || !chunk_out || !num_merges_out || num_sms <= 0 ||
+      (units_out && unit_capacity < 0) || (merges_out && merge_capacity < 0))
+    return FI_ERR_INVALID_ARGUMENT;
+  fi::HostPlan P;
+  const fi_status st = fi::plan_decode_host(qo_indptr_host, kv_indptr_host, batch, num_qo_heads,
+                                            num_kv_heads, head_dim, page_size, 0.0f, num_sms, &P);
+  if (st != FI_OK) return st;
+  *info = P.info;
+  *chunk_out = P.dec_chunk;
+  const int64_t merges = static_cast<int64_t>(P.dec_merges.size() / 4);
+  *num_merges_out = merges;
+  if (units_out) {
+    const int64_t n = std::min<int64_t>(unit_capacity, P.info.num_units);
+    std::memcpy(units_out, P.dec_units.data(), static_cast<size_t>(n) * 4 * sizeof(int32_t));
+  }
+  if (merges_out) {
+    const int64_t n = std::min<int64_t>(merge_capacity, merges);
+    std::memcpy(merges_out, P.dec_merges.data(), static_cast<size_t>(n) * 4 * sizeof(int32_t));
+  }
+  return FI_OK;
+}
+
 extern "C" fi_status fi_prefill_plan_host(const int32_t* qo_indptr_host,
                                           const int32_t* kv_indptr_host, int32_t batch,
                                           int32_t num_qo_heads, int32_t num_kv_heads,

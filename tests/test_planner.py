@@ -206,3 +206,90 @@ def test_balanced_ragged_plan_bounds():
     slots = info["num_ctas"] // info["ctas_per_unit"]
     costs = [int(w[3]) + 1 for w in work]
     assert max(costs) <= info["max_slot_tiles"] <= sum(costs) / slots + max(costs)
+
+
+# ---------------------------------------------------------------- decode plans
+# The decode plan of the PR #5043 page (max_kv_len from one reduction over the
+# lengths) with this library's split: units (sequence, KV head, chunk of keys),
+# the chunk the smallest power of two from 256 to 16384 that keeps at most 32
+# units per SM, one partial slot per chunk and one merge per multi-chunk
+# (sequence, KV head).
+
+def _decode_plan(qo_lens, kv_lens, hq, hk, num_sms=148, d=128, ps=16):
+    return fi.fi_decode_plan_host(fi.indptr_from_lens(qo_lens), fi.indptr_from_lens(kv_lens),
+                                  hq, hk, d, ps, num_sms=num_sms)
+
+
+def _check_decode_cover(qo_lens, kv_lens, hk, chunk, units, merges):
+    """Every (sequence, KV head) with queries is split into ceil(kv / chunk) units
+    that cover its keys once; multi-chunk ones own consecutive partial slots and
+    one merge item, single-chunk ones write directly (slot -1)."""
+    expect = [(b, h) for b in range(len(kv_lens)) if qo_lens[b] > 0 for h in range(hk)]
+    seen = {}
+    for b, h, c, slot in units.tolist():
+        seen.setdefault((b, h), []).append((c, slot))
+    assert sorted(seen) == expect
+    merge_of = {(b, h): (first, n) for b, h, first, n in merges.tolist()}
+    next_slot = 0
+    for (b, h) in expect:                       # units and merges in (sequence, head) order
+        n = -(-kv_lens[b] // chunk)
+        got = seen[(b, h)]
+        assert [c for c, _ in got] == list(range(n))
+        if n == 1:
+            assert got[0][1] == -1 and (b, h) not in merge_of
+        else:
+            assert merge_of[(b, h)] == (next_slot, n)
+            assert [s for _, s in got] == list(range(next_slot, next_slot + n))
+            next_slot += n
+
+
+def test_decode_plan_of_the_decode_workload():
+    import workloads as W
+    sp = W.spec("decode")
+    info, chunk, units, merges = _decode_plan(sp.qo_lens, sp.seq_lens, 32, 8)
+    # 128 x 8 (sequence, head) pairs of 4096 keys on 148 SMs: 32 units per SM
+    # allow 4736 units, so chunks of 1024 keys (4096 units); 512 would give 8192.
+    assert chunk == 1024 and info["num_units"] == 4096 and merges.shape == (1024, 4)
+    assert info["max_qo_len"] == 1 and info["max_kv_len"] == 4096 and info["is_uniform"] == 1
+    _check_decode_cover(sp.qo_lens, sp.seq_lens, 8, chunk, units, merges)
+
+
+@pytest.mark.parametrize("num_sms,want_chunk", [(148, 256), (1, 512), (200000, 256)])
+def test_decode_chunk_is_the_smallest_power_of_two_that_fits(num_sms, want_chunk):
+    qo, kv = [1, 1, 2], [100, 300, 5000]
+    info, chunk, units, merges = _decode_plan(qo, kv, 8, 2, num_sms=num_sms)
+    assert chunk == want_chunk
+    # 256 keys: (1 + 2 + 20) chunks x 2 heads = 46 units, above 32 for one SM;
+    # 512 keys: (1 + 1 + 10) x 2 = 24
+    assert info["num_units"] == {256: 46, 512: 24}[chunk]
+    _check_decode_cover(qo, kv, 2, chunk, units, merges)
+
+
+def test_decode_chunk_stops_at_16384():
+    # one SM cannot hold 1024 units whatever the chunk: the chunk stops at 16384
+    info, chunk, units, merges = _decode_plan([1] * 128, [4096] * 128, 32, 8, num_sms=1)
+    assert chunk == 16384 and info["num_units"] == 1024 and merges.shape[0] == 0
+    assert (units[:, 3] == -1).all()
+
+
+def test_decode_plan_skips_sequences_without_queries():
+    qo, kv = [0, 2, 0, 1], [50, 700, 9, 3000]
+    info, chunk, units, merges = _decode_plan(qo, kv, 4, 2)
+    assert set(units[:, 0].tolist()) == {1, 3}
+    _check_decode_cover(qo, kv, 2, chunk, units, merges)
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(qo=[9], kv=[20]), fi.FI_ERR_UNSUPPORTED),           # more than 8 query tokens
+    (dict(qo=[5], kv=[20], hq=32, hk=4), fi.FI_ERR_UNSUPPORTED),  # G * qo_len = 40 > 32 rows
+    (dict(qo=[5], kv=[4]), fi.FI_ERR_INVALID_ARGUMENT),      # qo_len > kv_len
+    (dict(d=96), fi.FI_ERR_UNSUPPORTED),
+    (dict(ps=8), fi.FI_ERR_UNSUPPORTED),
+    (dict(num_sms=0), fi.FI_ERR_INVALID_ARGUMENT),
+])
+def test_decode_plan_rejects(args, code):
+    with pytest.raises(fi.FiError) as e:
+        _decode_plan(args.get("qo", [1]), args.get("kv", [16]), args.get("hq", 8),
+                     args.get("hk", 2), num_sms=args.get("num_sms", 148), d=args.get("d", 128),
+                     ps=args.get("ps", 16))
+    assert e.value.status == code
