@@ -10,11 +10,12 @@
 // the work is HBM-bound.  One warp owns one unit = (sequence, KV head, chunk
 // of keys) and takes its keys 32 at a time: each lane copies its own key's
 // raw K and V rows (codes and block scales) into a two-step ring in shared
-// memory two steps ahead (cp.async), dequantizes them into exact fp16 rows
-// (E2M1 x E4M3 fits fp16), then the warp computes S = Q K^T and O += P V with m16n8k16
-// warp-level MMAs (fp16 in, fp32 accumulators; Q in registers, scaled by a
-// power of two into fp16 range), the online softmax running on the
-// accumulator fragments.  A sequence whose keys span several chunks writes
+// memory two steps ahead (cp.async) and dequantizes its V row into an exact
+// fp16 row (E2M1 x E4M3 fits fp16); the warp computes S = Q K^T with K's MMA
+// fragments converted straight from the raw codes in the ring, and O += P V
+// from the staged V rows, with m16n8k16 warp-level MMAs (fp16 in, fp32
+// accumulators; Q in registers, scaled by a power of two into fp16 range),
+// the online softmax running on the accumulator fragments.  A sequence whose keys span several chunks writes
 // unnormalized partial results (row max, row sum, O) that a merge kernel
 // combines.
 #include <algorithm>
@@ -69,11 +70,6 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
 __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -84,8 +80,8 @@ __device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Bytes of one staged K or V row (fp16), padded so that the eight rows of an
-// 8x8 matrix load fall on distinct banks.
+// Bytes of one staged V row (fp16), padded so that the eight rows of an 8x8
+// matrix load fall on distinct banks.
 template <int D>
 constexpr int kRowStride = D * 2 + 16;
 // Bytes of one lane's raw rows in the ring: K codes, V codes, K scales, V
@@ -94,12 +90,12 @@ template <int D>
 constexpr int kLaneRaw = (D + D / 8 + 15) / 16 * 16;
 template <int D>
 constexpr int decode_smem_bytes() {
-  return kDecWarps * (2 * 32 * kRowStride<D> + kDecStages * 32 * kLaneRaw<D>);
+  return kDecWarps * (32 * kRowStride<D> + kDecStages * 32 * kLaneRaw<D>);
 }
 
 // MT: 16-row MMA tiles per unit (rows G * qo_len <= 16 MT).
 template <int D, int MT>
-__global__ void __launch_bounds__(32 * kDecWarps, 2)
+__global__ void __launch_bounds__(32 * kDecWarps, MT == 1 ? 3 : 2)
     nvfp4_decode_kernel(const DecodeParams p) {
   constexpr int kS = kRowStride<D>;
   constexpr int kLR = kLaneRaw<D>;
@@ -121,11 +117,10 @@ __global__ void __launch_bounds__(32 * kDecWarps, 2)
   const int k0 = c * p.chunk;
   const int k1 = min(k0 + p.chunk, kv_len);
   const float ks = __ldg(p.k_scale), vs = __ldg(p.v_scale);
-  uint8_t* sk = dsm + warp * 2 * 32 * kS;  // this warp's 32 staged K rows, then V rows
-  uint8_t* sv = sk + 32 * kS;
-  const uint32_t sk_addr = smem_u32(sk), sv_addr = smem_u32(sv);
-  // this warp's raw ring: stage st, lane l at (st * 32 + l) * kLR
-  uint8_t* raw = dsm + kDecWarps * 2 * 32 * kS + warp * kDecStages * 32 * kLR;
+  uint8_t* sv = dsm + warp * 32 * kS;  // this warp's 32 staged V rows
+  const uint32_t sv_addr = smem_u32(sv);
+  // this warp's raw ring: stage st, key (lane) l at (st * 32 + l) * kLR
+  uint8_t* raw = dsm + kDecWarps * 32 * kS + warp * kDecStages * 32 * kLR;
   const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.pt_stride;
   auto q_ptr = [&](int r) {  // row r = token r / G, head hk * G + r % G
     return p.q + (static_cast<int64_t>(qo_start + r / G) * p.num_qo_heads + hk * G + r % G) * D;
@@ -233,48 +228,40 @@ __global__ void __launch_bounds__(32 * kDecWarps, 2)
 
   int st = 0;
   for (int kb = k0; kb < k1; kb += 32, st ^= 1) {
-    // ---- stage this lane's key: K and V rows as exact fp16 (zeros past k1)
+    // ---- stage this lane's key: its V row as exact fp16 (zeros past k1)
     cp_async_wait<1>();  // this lane's raw rows of this step have landed
-    __syncwarp();        // the previous batch's rows have been read
+    __syncwarp();        // ... and every lane's; the previous batch's V rows have been read
     {
-      uint4* dk = reinterpret_cast<uint4*>(sk + lane * kS);
       uint4* dv = reinterpret_cast<uint4*>(sv + lane * kS);
       const int key = kb + lane;
       if (key < k1) {
         const uint8_t* src = raw + (st * 32 + lane) * kLR;
-        uint4 kc4[D / 32], vc4[D / 32];
-        uint32_t ksf4[D / 64], vsf4[D / 64];
+        uint4 vc4[D / 32];
+        uint32_t vsf4[D / 64];
 #pragma unroll
-        for (int i = 0; i < D / 32; ++i) {
-          kc4[i] = reinterpret_cast<const uint4*>(src)[i];
-          vc4[i] = reinterpret_cast<const uint4*>(src + D / 2)[i];
-        }
+        for (int i = 0; i < D / 32; ++i) vc4[i] = reinterpret_cast<const uint4*>(src + D / 2)[i];
 #pragma unroll
-        for (int i = 0; i < D / 64; ++i) {
-          ksf4[i] = reinterpret_cast<const uint32_t*>(src + D)[i];
+        for (int i = 0; i < D / 64; ++i)
           vsf4[i] = reinterpret_cast<const uint32_t*>(src + D + D / 16)[i];
-        }
-        const uint32_t* kc = reinterpret_cast<const uint32_t*>(kc4);
         const uint32_t* vc = reinterpret_cast<const uint32_t*>(vc4);
 #pragma unroll
         for (int blk = 0; blk < D / 16; ++blk) {
-          const uint32_t s8k = (ksf4[blk / 4] >> (8 * (blk % 4))) & 0xFFu;
           const uint32_t s8v = (vsf4[blk / 4] >> (8 * (blk % 4))) & 0xFFu;
-          dk[2 * blk] = dequant8_f16(kc[2 * blk], s8k);
-          dk[2 * blk + 1] = dequant8_f16(kc[2 * blk + 1], s8k);
           dv[2 * blk] = dequant8_f16(vc[2 * blk], s8v);
           dv[2 * blk + 1] = dequant8_f16(vc[2 * blk + 1], s8v);
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < D / 8; ++i) dk[i] = dv[i] = make_uint4(0u, 0u, 0u, 0u);
+        for (int i = 0; i < D / 8; ++i) dv[i] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
-    __syncwarp();  // every lane's rows are staged
-    // the raw stage just read takes the rows of the step after next
-    issue(kb + 64, st);
 
-    // ---- S = Q K^T for the 32 keys (4 n-tiles of 8 keys, D/16 k-steps)
+    // ---- S = Q K^T for the 32 keys (4 n-tiles of 8 keys, D/16 k-steps).  The
+    // B fragment of n-tile j, k-step t (dims 16t .. 16t+15 = scale block t)
+    // holds, in lane l, key 8j + l/4 at dims 16t + 2(l%4) + {0, 1} and
+    // {8, 9} more: byte l%4 of code words 4(t/2) + 2(t%2) and the word after
+    // it of that key's raw row, times the block's scale.  Keys past k1 read
+    // stale ring bytes; their logits are replaced by -inf below.
     float sacc[MT][4][4];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
@@ -282,19 +269,43 @@ __global__ void __launch_bounds__(32 * kDecWarps, 2)
       for (int j = 0; j < 4; ++j)
 #pragma unroll
         for (int e = 0; e < 4; ++e) sacc[mt][j][e] = 0.0f;
+    const uint32_t bsel = static_cast<uint32_t>(lane % 4) | ((4u + static_cast<uint32_t>(lane % 4)) << 4);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
+      const uint8_t* kr = raw + (st * 32 + 8 * j + lane / 4) * kLR;
+      uint32_t kw[D / 8];
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) {
+        const uint4 w4 = reinterpret_cast<const uint4*>(kr)[i];
+        kw[4 * i] = w4.x;
+        kw[4 * i + 1] = w4.y;
+        kw[4 * i + 2] = w4.z;
+        kw[4 * i + 3] = w4.w;
+      }
+      uint32_t ksf[D / 64];
+#pragma unroll
+      for (int i = 0; i < D / 64; ++i) ksf[i] = reinterpret_cast<const uint32_t*>(kr + D)[i];
 #pragma unroll
       for (int s2 = 0; s2 < D / 32; ++s2) {
-        uint32_t bq[4];  // k-steps 2 s2 and 2 s2 + 1 of keys 8j .. 8j+7
-        ldsm_x4(sk_addr + (8 * j + lane % 8) * kS + (32 * s2 + 8 * (lane / 8)) * 2, bq);
+        // bytes for k-steps 2 s2 (b0, b1) and 2 s2 + 1 (b0, b1), in that order
+        const uint32_t lo = __byte_perm(kw[4 * s2], kw[4 * s2 + 1], bsel);
+        const uint32_t hi = __byte_perm(kw[4 * s2 + 2], kw[4 * s2 + 3], bsel);
+        uint32_t h[4];
+        e2m1x8_to_f16x2(__byte_perm(lo, hi, 0x5410), h);
+        const uint32_t sa = e4m3_to_f16x2_dup(ksf[s2 / 2] >> (16 * (s2 % 2)));
+        const uint32_t sb = e4m3_to_f16x2_dup(ksf[s2 / 2] >> (16 * (s2 % 2) + 8));
+        const uint32_t b0a = hmul2_u32(h[0], sa), b1a = hmul2_u32(h[1], sa);
+        const uint32_t b0b = hmul2_u32(h[2], sb), b1b = hmul2_u32(h[3], sb);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          mma16816(sacc[mt][j], qa[mt][2 * s2], bq[0], bq[1]);
-          mma16816(sacc[mt][j], qa[mt][2 * s2 + 1], bq[2], bq[3]);
+          mma16816(sacc[mt][j], qa[mt][2 * s2], b0a, b1a);
+          mma16816(sacc[mt][j], qa[mt][2 * s2 + 1], b0b, b1b);
         }
       }
     }
+    __syncwarp();  // every lane has read this stage's raw rows; V rows are staged
+    // the raw stage just read takes the rows of the step after next
+    issue(kb + 64, st);
 
     // ---- causal mask and online softmax; rows r0 = 16 mt + lane/4 (h = 0)
     // and r0 + 8 (h = 1), keys kb + 8j + 2(lane%4) + e
