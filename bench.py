@@ -179,6 +179,19 @@ class PathRunner:
         self.ctx = fi.fi_context_create()
         self.plan = fi.fi_plan_create(self.ctx)
         self.decode = bool(sp.qo_lens)
+        if self.decode:
+            # A decode step appends each sequence's newest qo_len tokens; the
+            # rest of its context is written into the cache once, here.
+            append = fi.fi_fp8_append if self.fp8 else fi.fi_nvfp4_append
+            append(self.ctx, self.k, self.v, self.cache.k_scale, self.cache.v_scale, self.slots,
+                   self.cache)
+            torch.cuda.synchronize()
+            qlens = np.diff(self.qo_indptr)
+            idx = np.concatenate([np.arange(e - q, e) for e, q in zip(self.kv_indptr[1:], qlens)])
+            idx_t = torch.from_numpy(idx.astype(np.int64)).to(device)
+            self.k = self.k.index_select(0, idx_t).contiguous()
+            self.v = self.v.index_select(0, idx_t).contiguous()
+            self.slots = self.slots.index_select(0, idx_t).contiguous()
         lens = np.diff(self.qo_indptr).tolist()
         kv_lens = np.diff(self.kv_indptr).tolist()
         self.flops = W.causal_flops(lens, kv_lens, sp.num_qo_heads, sp.head_dim)
