@@ -2,7 +2,8 @@
 causal prefill, through the C ABI of libfi_nvfp4.so.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload uniform|single|ragged] [--no-e2e] [--no-cpu-baseline]
+                    [--workload uniform|single|ragged|decode] [--kv-format nvfp4|fp8]
+                    [--no-e2e] [--no-cpu-baseline]
 
 One step is one pass of the whole path over one batch: fi_nvfp4_append of every
 token's K/V into the cache, fi_prefill_plan of the batch, fi_prefill_run.  The
@@ -84,6 +85,16 @@ def recorded_traffic(key):
         with open(os.path.join(ROOT, src), "rb") as f:
             h.update(f.read())
     return rec["dram_bytes_per_launch"] if h.hexdigest()[:16] == rec["source_sha256_16"] else None
+
+
+def newest_token_rows(qo_indptr, kv_indptr):
+    """Rows (in the kv_indptr layout) of each sequence's newest qo_len tokens: the
+    tokens a decode step appends, the rest of the context being in the cache."""
+    qlens = np.diff(np.asarray(qo_indptr))
+    ends = np.asarray(kv_indptr)[1:]
+    if len(ends) == 0:
+        return np.zeros(0, np.int64)
+    return np.concatenate([np.arange(e - q, e) for e, q in zip(ends, qlens)]).astype(np.int64)
 
 
 def append_bytes(num_tokens_written, num_tokens_skipped, num_kv_heads, head_dim, fp8=False):
@@ -186,9 +197,7 @@ class PathRunner:
             append(self.ctx, self.k, self.v, self.cache.k_scale, self.cache.v_scale, self.slots,
                    self.cache)
             torch.cuda.synchronize()
-            qlens = np.diff(self.qo_indptr)
-            idx = np.concatenate([np.arange(e - q, e) for e, q in zip(self.kv_indptr[1:], qlens)])
-            idx_t = torch.from_numpy(idx.astype(np.int64)).to(device)
+            idx_t = torch.from_numpy(newest_token_rows(self.qo_indptr, self.kv_indptr)).to(device)
             self.k = self.k.index_select(0, idx_t).contiguous()
             self.v = self.v.index_select(0, idx_t).contiguous()
             self.slots = self.slots.index_select(0, idx_t).contiguous()

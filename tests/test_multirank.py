@@ -49,3 +49,11 @@ def test_reference_arm_is_rank0_only(monkeypatch, capsys):
     args = argparse.Namespace(steps=1, warmup=0, gpus=2, workload="single")
     assert bench.run_reference(args) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_decode_step_appends_the_newest_tokens():
+    import bench
+    # sequences of 5, 3 and 4 keys with 1, 3 and 2 new query tokens
+    rows = bench.newest_token_rows([0, 1, 4, 6], [0, 5, 8, 12])
+    assert rows.tolist() == [4, 5, 6, 7, 10, 11]
+    assert bench.newest_token_rows([0], [0]).size == 0
