@@ -293,3 +293,27 @@ def test_decode_plan_rejects(args, code):
                      args.get("hk", 2), num_sms=args.get("num_sms", 148), d=args.get("d", 128),
                      ps=args.get("ps", 16))
     assert e.value.status == code
+
+
+def test_fp8_plan_counts_one_byte_per_element_in_the_l2_gate():
+    # 20 sequences of 2000 tokens, H_kv = 8, D = 128: the NVFP4 K+V bytes
+    # (72 per token and head and tensor) fit the gate 2 kv_bytes <= L2, the FP8
+    # bytes (128) do not
+    ind = fi.indptr_from_lens([2000] * 20)
+    tokens = 40000
+    nv, _ = fi.fi_prefill_plan_host(ind, ind, 32, 8, 128, 16, l2_bytes=L2, with_list=False)
+    f8, _ = fi.fi_prefill_plan_host(ind, ind, 32, 8, 128, 16, l2_bytes=L2, with_list=False,
+                                    kv_format=1)
+    assert nv["kv_bytes"] == tokens * 8 * 2 * (64 + 8)
+    assert f8["kv_bytes"] == tokens * 8 * 2 * 128
+    assert 2 * nv["kv_bytes"] <= L2 < 2 * f8["kv_bytes"]
+    assert nv["global_reverse"] == 1 and f8["global_reverse"] == 0
+    # everything else about the plan is the same
+    for k in ("num_units", "q_tiles", "head_units", "ctas_per_unit", "is_uniform"):
+        assert nv[k] == f8[k]
+
+
+def test_plan_rejects_unknown_kv_format():
+    with pytest.raises(fi.FiError) as e:
+        fi.fi_prefill_plan_host([0, 4], [0, 4], 4, 2, 64, 16, kv_format=2)
+    assert e.value.status == fi.FI_ERR_INVALID_ARGUMENT
