@@ -1,25 +1,33 @@
-"""Benchmark of the NVFP4 paged-KV hot path on B300: quantize-append -> plan ->
+"""Benchmark of the NVFP4 paged-KV hot path on B300: plan -> quantize-append ->
 causal prefill, through the C ABI of libfi_nvfp4.so.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload uniform|single|ragged|decode] [--kv-format nvfp4|fp8]
-                    [--no-e2e] [--no-cpu-baseline]
+                    [--no-e2e] [--no-cpu-baseline] [--no-extra]
 
-One step is one pass of the whole path over one batch: fi_nvfp4_append of every
-token's K/V into the cache, fi_prefill_plan of the batch, fi_prefill_run.  The
-default workload is the uniform batch: 1024 sequences of qo_len = kv_len = 1024,
-H_q = 32, H_kv = 8, head_dim = 128, page_size = 16 (synthetic N(0,1) bf16
-inputs, random page table).  `value` is the causal prefill FLOPs of a step
-divided by the measured step time (TFLOP/s); the append bandwidth of the
-8192-token append workload (cold L2: 24 rotating buffer sets captured in one
-CUDA graph) is reported beside it.
+One step is one pass of the whole path over one batch: fi_prefill_plan of the
+batch (its upload enqueued first, so that the append and the prefill are
+adjacent on the stream and the prefill is launched as the append's
+programmatic dependent), fi_nvfp4_append of every token's K/V into the cache,
+fi_prefill_run.  The default workload is the uniform batch: 1024 sequences of
+qo_len = kv_len = 1024, H_q = 32, H_kv = 8, head_dim = 128, page_size = 16
+(synthetic N(0,1) bf16 inputs, random page table).  `value` is the causal
+prefill FLOPs of a step divided by the measured step time (TFLOP/s), timed over
+K steps with no event between the kernels; a second pass of K steps with
+events around each kernel gives the per-kernel times of `roofline` and
+`append_in_step`.  The same run also measures, each in its own timed passes,
+the single 2048 x 2048 prefill, the ragged batch, the 128 x 4096 decode and the
+FP8 (E4M3) variant of the uniform batch (`workloads`), and the 8192-token
+append with cold L2 (`append_bench`: 24 rotating buffer sets captured in one
+CUDA graph).
 
 Under torchrun (N > 1) every rank runs its own independent copy of the
 workload on its own GPU (the path has no exchange step): scaling is weak and
 `value` is the FLOPs of all ranks over the slowest rank's time.
 
 --impl reference times the CPU oracle (the slow, plain C++ definition of the
-method) on a bounded sample of the same workload, on the host cores.
+method) on a fixed sample of the same workload, on the host cores; the
+`cpu_baseline` leg of our arm times the same sample.
 """
 from __future__ import annotations
 
@@ -52,8 +60,14 @@ WORKLOAD_DESC = {
     "ragged": "ragged batch: 256 sequences, qo_len=kv_len log-uniform in [128,16384], H_q=32, "
               "H_kv=8, head_dim=128, page_size=16, append + plan + causal prefill",
     "decode": "decode batch: 128 sequences x kv_len 4096, qo_len 1, H_q=32, H_kv=8, "
-              "head_dim=128, page_size=16, append + decode plan + decode",
+              "head_dim=128, page_size=16, decode plan + append of the newest token + decode",
 }
+
+# Oracle sample (both arms): sequences of the workload drawn with a fixed seed
+# until about ORACLE_TOKENS cache tokens, and at most ORACLE_ROWS of their
+# (token, query head) rows in a seeded random order.
+ORACLE_TOKENS = 8192
+ORACLE_ROWS = 1 << 18
 
 
 # ----------------------------------------------------------------- helpers
@@ -189,7 +203,7 @@ class PathRunner:
         self.lse = torch.empty(self.q.shape[:2], dtype=torch.float32, device=device)
         self.ctx = fi.fi_context_create()
         self.plan = fi.fi_plan_create(self.ctx)
-        self.decode = bool(sp.qo_lens)
+        self.decode = sp.attn == "decode"
         if self.decode:
             # A decode step appends each sequence's newest qo_len tokens; the
             # rest of its context is written into the cache once, here.
@@ -214,14 +228,10 @@ class PathRunner:
                                          fp8=self.fp8)
 
     def step(self, stream, ev=None):
+        """plan (host planning, upload enqueued) -> append -> run.  With `ev`
+        (three events) the append and the run are bracketed by events:
+        ev[0] append ev[1] run ev[2]."""
         fi, sp = self.fi, self.sp
-        if ev is not None:
-            ev[0].record(stream)
-        append = fi.fi_fp8_append if self.fp8 else fi.fi_nvfp4_append
-        append(self.ctx, self.k, self.v, self.cache.k_scale, self.cache.v_scale, self.slots,
-               self.cache, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
         if self.decode:
             fi.fi_decode_plan(self.plan, self.qo_indptr, self.kv_indptr, self.page_table,
                               sp.num_qo_heads, sp.num_kv_heads, sp.head_dim, sp.page_size,
@@ -232,14 +242,28 @@ class PathRunner:
                                sm_scale=self.d["sm_scale"], stream=stream,
                                kv_format=1 if self.fp8 else 0)
         if ev is not None:
-            ev[2].record(stream)
+            ev[0].record(stream)
+        append = fi.fi_fp8_append if self.fp8 else fi.fi_nvfp4_append
+        append(self.ctx, self.k, self.v, self.cache.k_scale, self.cache.v_scale, self.slots,
+               self.cache, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
         if self.decode:
             run = fi.fi_decode_run
         else:
             run = fi.fi_prefill_run_fp8 if self.fp8 else fi.fi_prefill_run
         run(self.plan, self.q, self.cache, self.out, self.lse, stream=stream)
         if ev is not None:
-            ev[3].record(stream)
+            ev[2].record(stream)
+
+    def launches_per_step(self):
+        """Kernels of this library one step launches: the append and the
+        attention (a decode with split sequences adds its merge kernel)."""
+        if self.decode:
+            info = self.fi.fi_plan_get_info(self.plan)
+            merges = info["num_units"] > info["batch"] * self.sp.num_kv_heads
+            return 3 if merges else 2
+        return 2
 
     def status(self):
         return self.fi.fi_device_status(self.ctx)
@@ -272,24 +296,31 @@ def aggregate_value(flops_per_rank, step_ms_max, world):
 
 
 def time_device_steps(runner, stream, steps, warmup, dist_on, device):
+    """Returns (step ms over `steps` steps with no event between the kernels,
+    per-step append ms, per-step attention ms from a second pass of `steps`
+    steps with events around each kernel)."""
     for _ in range(warmup):
         runner.step(stream)
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     barrier(dist_on)
     torch.cuda.synchronize()
     start.record(stream)
-    for i in range(steps):
-        runner.step(stream, evs[i])
+    for _ in range(steps):
+        runner.step(stream)
     end.record(stream)
     torch.cuda.synchronize()
     barrier(dist_on)
     total_ms = start.elapsed_time(end)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        runner.step(stream, evs[i])
+    torch.cuda.synchronize()
     append_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    prefill_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    return total_ms, append_ms, prefill_ms
+    attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    return total_ms, append_ms, attn_ms
 
 
 def time_e2e(runner, stream, steps, warmup):
@@ -393,18 +424,21 @@ def time_append_cold(fi, device, n_sets=24, reps=20):
 
 
 # ----------------------------------------------------------------- oracle legs
-def oracle_sample(name, budget_s, seed=0):
-    """Times the CPU oracle on a bounded sample of workload `name`: two of its
-    sequences (same per-sequence shape, freshly drawn seeded inputs) are
-    appended by the oracle into a host cache, then sampled attention rows of
-    those sequences are computed until `budget_s` seconds of attention time
-    are used.  Returns (flops, seconds, description, threads, append seconds)."""
+def oracle_sample(name, seed=0):
+    """Times the CPU oracle on a fixed sample of workload `name`: sequences
+    drawn with `seed` (same per-sequence shapes, freshly drawn seeded inputs)
+    until about ORACLE_TOKENS cache tokens, appended by the oracle into a host
+    cache (plan-free: the oracle needs none), then the attention of at most
+    ORACLE_ROWS of their (token, query head) rows in a seeded random order, in
+    chunks.  Returns a dict: flops of the sampled rows, append and attention
+    seconds, rows, threads and a description."""
     import oracle as O
     full = W.spec(name)
-    n_seqs = max(1, min(full.batch, math.ceil(32768 * full.batch / sum(full.seq_lens))))
+    n_seqs = max(1, min(full.batch, math.ceil(ORACLE_TOKENS * full.batch / sum(full.seq_lens))))
     sp = W.sample_spec(name, n_seqs, seed)
     d = W.make(sp, device="cpu")
     qo = d["qo_indptr"].numpy().astype(np.int64)
+    kv = d["kv_indptr"].numpy().astype(np.int64)
     rng = np.random.default_rng(seed)
     threads = O.max_threads()
     host = O.new_cache(d["num_pages"], sp.num_kv_heads, sp.page_size, sp.head_dim, 0)
@@ -413,53 +447,53 @@ def oracle_sample(name, budget_s, seed=0):
                   d["slot_mapping"].numpy(), host)
     t_append = time.perf_counter() - t0
     assert st == 0
-    # rows: (token, head) pairs of the sample in random order, until the budget is used
     all_rows = np.stack(np.meshgrid(np.arange(int(qo[-1])), np.arange(sp.num_qo_heads),
                                     indexing="ij"), -1).reshape(-1, 2).astype(np.int64)
     rng.shuffle(all_rows)
-    seq_of = np.searchsorted(qo, all_rows[:, 0], side="right") - 1
-    flops, t_attn, done, chunk = 0, 0.0, 0, 256
+    rows_all = all_rows[:ORACLE_ROWS]
+    seq_of = np.searchsorted(qo, rows_all[:, 0], side="right") - 1
+    i = rows_all[:, 0] - qo[seq_of]
+    visible = i + (kv[seq_of + 1] - kv[seq_of]) - (qo[seq_of + 1] - qo[seq_of]) + 1
+    flops = int(4 * sp.head_dim * visible.sum())
     qb = W.bits(d["q"])
     pt = d["page_table"].numpy()
-    while done < len(all_rows) and t_attn < budget_s:
-        rows = all_rows[done:done + chunk]
+    t_attn, chunk = 0.0, 65536
+    for c0 in range(0, len(rows_all), chunk):
         t0 = time.perf_counter()
-        O.prefill(qb, qo.astype(np.int32), qo.astype(np.int32), pt, host, sp.num_qo_heads,
-                  d["k_scale"], d["v_scale"], d["sm_scale"], rows=rows, threads=threads)
+        O.prefill(qb, qo.astype(np.int32), kv.astype(np.int32), pt, host, sp.num_qo_heads,
+                  d["k_scale"], d["v_scale"], d["sm_scale"], rows=rows_all[c0:c0 + chunk],
+                  threads=threads)
         t_attn += time.perf_counter() - t0
-        i = rows[:, 0] - qo[seq_of[done:done + chunk]]
-        flops += int(4 * sp.head_dim * (i + 1).sum())
-        done += len(rows)
-        chunk = min(chunk * 2, 8192)
-    lens_txt = str(sp.seq_lens) if len(sp.seq_lens) <= 12 else f"{len(sp.seq_lens)} x {sp.seq_lens[0]}" \
-        if len(set(sp.seq_lens)) == 1 else f"{sum(sp.seq_lens)} tokens in total"
-    desc = (f"{len(sp.seq_lens)} sequences of the workload ({lens_txt}): oracle "
-            f"append ({t_append:.2f} s) + fp64 attention of {done} sampled (token, head) rows "
-            f"({t_attn:.2f} s); TFLOP/s over the sampled rows' causal FLOPs")
-    return flops, t_attn, desc, threads, t_append
+    lens_txt = f"{len(sp.seq_lens)} x {sp.seq_lens[0]}" if len(set(sp.seq_lens)) == 1 \
+        else f"{sum(sp.seq_lens)} tokens in total"
+    desc = (f"{len(sp.seq_lens)} sequences of the workload ({lens_txt}): oracle append of "
+            f"their K/V ({t_append:.2f} s) + fp64 attention of {len(rows_all)} (token, query "
+            f"head) rows ({t_attn:.2f} s); value = the rows' causal FLOPs / (append + "
+            f"attention time)")
+    return {"flops": flops, "t_append": t_append, "t_attn": t_attn, "rows": len(rows_all),
+            "threads": threads, "desc": desc}
 
 
 def run_reference(args):
-    """--impl reference: the oracle, timed on the host cores."""
+    """--impl reference: the oracle, timed on the host cores (rank 0 only)."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
-    for _ in range(args.warmup):
-        oracle_sample(args.workload, budget / 4, seed=1)
-    tot_f, tot_t, desc, threads = 0, 0.0, "", 1
+    for i in range(args.warmup):
+        oracle_sample(args.workload, seed=100 + i)
+    tot_f, tot_t, res = 0, 0.0, None
     for i in range(args.steps):
-        f, t, desc, threads, _ = oracle_sample(args.workload, budget, seed=2 + i)
-        tot_f += f
-        tot_t += t
+        res = oracle_sample(args.workload, seed=i)
+        tot_f += res["flops"]
+        tot_t += res["t_append"] + res["t_attn"]
     value = tot_f / tot_t / 1e12
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD_DESC[args.workload], "sampled": True},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                             "sample": desc},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": res["threads"],
+                             "kind": "oracle", "sample": res["desc"]},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -467,6 +501,63 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------- main
+def kernel_names(runner):
+    """Names of the step's kernels: (append, attention)."""
+    if runner.fp8:
+        app = "fp8_append_kernel"
+    else:
+        # the library's switch to the staged kernel
+        app = "nvfp4_append_staged_kernel" if runner.tokens >= 65536 else "nvfp4_append_kernel"
+    attn = "nvfp4_decode_kernel" if runner.decode else "nvfp4_prefill_kernel"
+    return app, attn
+
+
+def measure(fi, name, device, steps, warmup, dist_on, kv_format="nvfp4", seqs=0):
+    """Builds workload `name`, checks one clean step, times it; returns the
+    runner and its numbers."""
+    runner = PathRunner(fi, name, device, seqs, kv_format=kv_format)
+    stream = torch.cuda.Stream(device=device)
+    stream.wait_stream(torch.cuda.current_stream(device))  # inputs are made on the current stream
+    # correctness guard: the step must run clean before it is timed
+    runner.step(stream)
+    st = runner.status()
+    if st != 0:
+        raise RuntimeError(f"{name}: device status {st} after the first step")
+    total_ms, append_ms, attn_ms = time_device_steps(runner, stream, steps, warmup, dist_on,
+                                                     device)
+    st = runner.status()
+    if st != 0:
+        raise RuntimeError(f"{name}: device status {st} after the timed steps")
+    return runner, stream, {"step_ms": total_ms / steps, "append_ms": statistics.mean(append_ms),
+                            "attn_ms": statistics.mean(attn_ms)}
+
+
+def attention_entry(runner, t, peaks):
+    """Per-launch numbers of the attention kernel of a measured workload."""
+    app_name, attn_name = kernel_names(runner)
+    ms = t["attn_ms"]
+    e = {"kernel": attn_name, "ms_per_launch": ms, "step_ms": t["step_ms"],
+         "tflops": runner.flops / (ms * 1e-3) / 1e12,
+         "step_tflops": runner.flops / (t["step_ms"] * 1e-3) / 1e12,
+         "flops_per_launch": runner.flops}
+    if runner.decode:
+        gbs = runner.decode_bytes / (ms * 1e-3) / 1e9
+        e.update({"bound": "hbm", "gbs": gbs, "algorithmic_bytes": runner.decode_bytes,
+                  "frac": gbs / peaks["hbm_gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s"})
+    else:
+        e.update({"bound": "tensor", "frac": e["tflops"] / peaks["bf16_tflops"],
+                  "frac_of_sustained": e["tflops"] / peaks["bf16_tflops_sustained"],
+                  "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"})
+    app_gbs = runner.append_bytes / (t["append_ms"] * 1e-3) / 1e9
+    e["append"] = {"kernel": app_name, "ms_per_launch": t["append_ms"], "gbs": app_gbs,
+                   "frac": app_gbs / peaks["hbm_gbs"], "algorithmic_bytes": runner.append_bytes}
+    return e
+
+
+EXTRA = [("single", "single", "nvfp4"), ("ragged", "ragged", "nvfp4"),
+         ("decode", "decode", "nvfp4"), ("fp8_uniform", "uniform", "fp8")]
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -480,12 +571,16 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-append-bench", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the other workloads (single, ragged, decode, fp8)")
+    ap.add_argument("--extra-steps", type=int, default=10)
     ap.add_argument("--seqs", type=int, default=0,
                     help="use only the first N sequences of the workload (profiling cases)")
     ap.add_argument("--only", choices=["all", "append"], default="all",
                     help="append: run only the cold-L2 append measurement")
     args = ap.parse_args()
+    if args.steps < 1 or args.warmup < 0:
+        raise SystemExit("--steps >= 1 and --warmup >= 0")
     if args.impl == "reference":
         return run_reference(args)
 
@@ -508,30 +603,33 @@ def main():
                           "us_warm_l2": a["warm_ms"] * 1e3, "frac": gbs / peaks["hbm_gbs"],
                           "status": a["status"]}), flush=True)
         return 0 if a["status"] == 0 else 1
-    runner = PathRunner(fi, args.workload, device, args.seqs, kv_format=args.kv_format)
-    stream = torch.cuda.Stream(device=device)
-    stream.wait_stream(torch.cuda.current_stream(device))  # inputs are made on the current stream
-    # correctness guard: the step must run clean before it is timed
-    runner.step(stream)
-    st = runner.status()
-    if st != 0:
-        raise RuntimeError(f"device status {st} after the first step")
 
     clocks = ClockSampler(local_rank)
     clocks.start()
-    total_ms, append_ms, prefill_ms = time_device_steps(runner, stream, args.steps, args.warmup,
-                                                        dist_on, device)
+    runner, stream, t = measure(fi, args.workload, device, args.steps, args.warmup, dist_on,
+                                kv_format=args.kv_format, seqs=args.seqs)
     clk = clocks.stop()
-    st = runner.status()
-    if st != 0:
-        raise RuntimeError(f"device status {st} after the timed steps")
-    step_ms = max_over_ranks(total_ms / args.steps, dist_on, device)
+    step_ms = max_over_ranks(t["step_ms"], dist_on, device)
     value = aggregate_value(runner.flops, step_ms, world)
-    pf_ms = statistics.mean(prefill_ms)
-    ap_ms = statistics.mean(append_ms)
-    pf_tflops = runner.flops / (pf_ms * 1e-3) / 1e12
-    peak_sus = peaks["bf16_tflops_sustained"]
-    peak_burst = peaks["bf16_tflops"]
+    head = attention_entry(runner, t, peaks)
+    full_uniform = args.workload == "uniform" and not args.seqs and not runner.fp8
+    traffic = recorded_traffic("prefill_uniform") if full_uniform else None
+    if runner.decode:
+        roofline = {"bound": "hbm", "achieved": head["gbs"], "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": head["frac"], "traffic": None,
+                    "kernel": head["kernel"], "algorithmic_bytes": runner.decode_bytes,
+                    "ms_per_launch": head["ms_per_launch"],
+                    "peak_kind": f"HBM copy ({peaks['source']})"}
+    else:
+        roofline = {"bound": "tensor", "achieved": head["tflops"], "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": head["frac"], "traffic": traffic,
+                    "kernel": head["kernel"], "flops_per_launch": runner.flops,
+                    "ms_per_launch": head["ms_per_launch"],
+                    "peak_kind": f"bf16 dense burst ({peaks['source']})",
+                    "peak_sustained": peaks["bf16_tflops_sustained"],
+                    "frac_of_sustained": head["frac_of_sustained"]}
+    append_in_step = dict(head["append"])
+    append_in_step["traffic"] = recorded_traffic("append_uniform") if full_uniform else None
 
     e2e = None
     if not args.no_e2e:
@@ -540,6 +638,28 @@ def main():
         e2e = {"value": aggregate_value(runner.flops, e2e_s * 1e3, world), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": args.e2e_steps, "ms_per_step": e2e_s * 1e3}
+    launches = runner.launches_per_step() * args.steps
+    tokens = runner.tokens
+    runner.close()
+    del runner, stream
+    torch.cuda.empty_cache()
+
+    extra = {}
+    if not args.no_extra and not args.seqs and args.workload == "uniform" and \
+            args.kv_format == "nvfp4":
+        for key, name, fmt in EXTRA:
+            c2 = ClockSampler(local_rank)
+            c2.start()
+            r2, s2, t2 = measure(fi, name, device, args.extra_steps, 3, dist_on, kv_format=fmt)
+            ck = c2.stop()
+            e = attention_entry(r2, t2, peaks)
+            e["workload"] = WORKLOAD_DESC[name] + (" [FP8 (E4M3) paged KV]" if fmt == "fp8" else "")
+            e["steps"] = args.extra_steps
+            e["clocks"] = {"sm_mhz": ck["sm_mhz"], "reasons": ck["reasons"]}
+            extra[key] = e
+            r2.close()
+            del r2, s2
+            torch.cuda.empty_cache()
 
     app = None
     if not args.no_append_bench and rank == 0:
@@ -558,55 +678,35 @@ def main():
                "status": a["status"]}
 
     cpu = None
-    if not args.no_cpu_baseline and rank == 0 and world == 1 and not runner.fp8:
-        f, t, desc, threads, _ = oracle_sample(args.workload, args.cpu_budget)
-        cpu = {"value": f / t / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": desc}
+    if not args.no_cpu_baseline and rank == 0 and world == 1 and args.kv_format == "nvfp4":
+        r = oracle_sample(args.workload, seed=0)
+        cpu = {"value": r["flops"] / (r["t_append"] + r["t_attn"]) / 1e12, "unit": UNIT,
+               "cores": r["threads"], "kind": "oracle", "sample": r["desc"],
+               "attention_only_tflops": r["flops"] / r["t_attn"] / 1e12}
 
-    runner_append_gbs = runner.append_bytes / (ap_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD_DESC[args.workload] +
                    (f" (first {args.seqs} sequences only)" if args.seqs else "") +
-                   (" [FP8 (E4M3) paged KV variant]" if runner.fp8 else ""),
+                   (" [FP8 (E4M3) paged KV variant]" if args.kv_format == "fp8" else ""),
                    "kv_format": args.kv_format,
-                   "tokens": runner.tokens,
-                   "flops_per_step": runner.flops,
+                   "tokens": tokens,
+                   "flops_per_step": head["flops_per_launch"],
                    "l2": "inputs larger than L2 (Q 8.6 GB, KV cache 1.2 GB per step)"
-                   if args.workload == "uniform" else "see workload",
+                   if args.workload == "uniform" and not args.seqs else "see workload",
+                   "step": "plan (upload) -> append -> prefill, no event between the kernels",
                    "parallelism": f"replicas x{world} (independent shards, no collective)"},
-        "roofline": {"bound": "hbm", "achieved": runner.decode_bytes / (pf_ms * 1e-3) / 1e9,
-                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": runner.decode_bytes / (pf_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                     "traffic": None, "kernel": "nvfp4_decode_kernel",
-                     "algorithmic_bytes": runner.decode_bytes, "tflops": pf_tflops,
-                     "ms_per_launch": pf_ms} if runner.decode else
-                    {"bound": "tensor", "achieved": pf_tflops, "peak": peak_sus,
-                     "unit": "TFLOP/s", "frac": pf_tflops / peak_sus,
-                     "traffic": recorded_traffic("prefill_uniform")
-                     if args.workload == "uniform" and not args.seqs and not runner.fp8 else None,
-                     "kernel": "nvfp4_prefill_kernel", "peak_kind":
-                     f"bf16 dense sustained ({peaks['source']})",
-                     "frac_of_burst_peak": pf_tflops / peak_burst,
-                     "ms_per_launch": pf_ms},
-        "append_in_step": {"ms_per_launch": ap_ms, "gbs": runner_append_gbs,
-                           "frac": runner_append_gbs / peaks["hbm_gbs"],
-                           "kernel": ("fp8_append_kernel" if runner.fp8 else
-                                      # the library's switch to the staged kernel
-                                      "nvfp4_append_staged_kernel" if runner.tokens >= 65536
-                                      else "nvfp4_append_kernel"),
-                           "traffic": recorded_traffic("append_uniform")
-                           if args.workload == "uniform" and not args.seqs and not runner.fp8
-                           else None},
+        "roofline": roofline,
+        "append_in_step": append_in_step,
+        "workloads": extra or None,
         "append_bench": app,
         "clocks": clk,
         "e2e": e2e,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": launches,
         "cpu_baseline": cpu,
     }
-    runner.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist_on:

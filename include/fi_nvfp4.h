@@ -297,11 +297,14 @@ fi_status fi_decode_plan_host(const int32_t* qo_indptr_host, const int32_t* kv_i
  * (units = sum over sequences of ceil(qo_len / 128) times the head units);
  * larger calls return FI_ERR_SCRATCH_TOO_SMALL and enqueue nothing.  Every
  * call shares the array: calls that overlap on the GPU (on different streams)
- * race.  The host arrays are copied with cudaMemcpyAsync from pageable memory,
- * which waits for the stream's earlier work, so calls on one stream are
- * ordered.  The first call on a device looks up the array's device address;
- * make that first call before any stream capture.  Ragged work units are taken
- * in sequence order with the heaviest q-tile of each sequence first. */
+ * race; calls on one stream are ordered by the stream (each call's copies into
+ * the array run after the previous call's kernel).  The indptr arrays are
+ * copied with cudaMemcpyAsync: from pageable memory they have been read when
+ * the call returns; page-locked ones are read when the stream reaches the
+ * copy, so they must stay unchanged until then.  The first call on a device
+ * looks up the array's device address; make that first call before any stream
+ * capture.  Ragged work units are taken in sequence order with the heaviest
+ * q-tile of each sequence first. */
 fi_status fi_prefill_noalloc(const int32_t* qo_indptr_host, const int32_t* kv_indptr_host,
                              int32_t batch, const int32_t* page_table_dev,
                              int32_t page_table_stride, int32_t num_qo_heads,

@@ -63,6 +63,21 @@ int32_t fi_diag_repack_tile(const uint8_t* raw, int32_t head_dim, int32_t is_v, 
 int32_t fi_diag_umma(int32_t mode, const void* a, const void* b, float* c, int32_t* status,
                      void* stream);
 
+/* Makes a bounded pipeline wait run out, with the library's own wait code: a
+ * one-CTA kernel whose warps wait on an mbarrier that nothing arrives at.
+ * Warp 0 holds tensor memory, has a 4096-byte bulk copy (copy_src -> shared
+ * memory) in flight and waits with the limit `timeout_ns` (1 ns .. 1 s); the
+ * other warps wait with the prefill's 2 s limit and give up through the CTA's
+ * abort flag as soon as warp 0's wait has run out.  Warp 0 then waits
+ * (bounded) for its copy, every thread meets, the tensor memory is freed and
+ * the kernel returns.  Effects: `status` (device int32) gets FI_DEV_WAIT_TIMEOUT
+ * (16) with atomicOr; copy_out (device, 4096 bytes) receives the copied bytes;
+ * report (device, 4 x uint64): [0] ns warp 0 waited, [1] ns warp 1 waited,
+ * [2] waits that gave up (66), [3] 1 if the copy completed.  copy_src and
+ * copy_out 16-byte aligned. */
+int32_t fi_diag_wait_timeout(uint64_t timeout_ns, const uint8_t* copy_src, uint8_t* copy_out,
+                             int32_t* status, unsigned long long* report, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

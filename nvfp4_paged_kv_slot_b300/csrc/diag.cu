@@ -4,6 +4,7 @@
 
 #include <mutex>
 
+#include "fi_nvfp4.h"
 #include "fi_nvfp4_diag.h"
 #include "nvfp4.cuh"
 
@@ -201,6 +202,80 @@ __global__ void __launch_bounds__(128, 1) umma_probe_kernel(const __grid_constan
   if (warp == 0) tmem_dealloc(tbase, 256);
 }
 
+// A pipeline that stops: the waits of the library's kernels (mbar_wait with
+// an AbortState) on an mbarrier that nothing arrives at.  Warp 0 holds tensor
+// memory and has a bulk copy in flight, as the prefill's roles do, and waits
+// with the caller's limit; warp 1 (one thread) and warps 2-3 (every thread)
+// wait on the same barrier with the prefill's own 2 s limit and must give up
+// as soon as warp 0's wait has set the CTA's abort flag.  Then warp 0 drains
+// its copy (a bounded wait on the copy's barrier, as the prefill's load warp
+// does when it aborts), every thread meets, and the tensor memory is freed.
+// report[0]: ns warp 0 waited; [1]: ns warp 1 waited; [2]: waits that gave up
+// (66 expected: 1 + 1 + 64); [3]: 1 if the drained copy completed;
+// copy_out: the copied bytes, read back from shared memory after the drain.
+constexpr int kProbeCopyBytes = 4096;
+constexpr uint64_t kPipelineTimeoutNs = 2000000000ull;  // the prefill's limit
+constexpr uint64_t kDrainNs = 100000000ull;
+
+__global__ void __launch_bounds__(128, 1)
+    wait_timeout_probe_kernel(uint64_t timeout_ns, const uint8_t* copy_src, uint8_t* copy_out,
+                              int32_t* status, unsigned long long* report) {
+  __shared__ __align__(128) uint8_t buf[kProbeCopyBytes];
+  __shared__ uint64_t never, copy_done;
+  __shared__ uint32_t tslot;
+  __shared__ int abort_flag;
+  __shared__ unsigned gave_up;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    mbar_init(&never, 1);
+    mbar_init(&copy_done, 1);
+    abort_flag = 0;
+    gave_up = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tslot, 32);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tslot;
+  const AbortState ab_short{&abort_flag, status, timeout_ns, FI_DEV_WAIT_TIMEOUT};
+  const AbortState ab_long{&abort_flag, status, kPipelineTimeoutNs, FI_DEV_WAIT_TIMEOUT};
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&copy_done, kProbeCopyBytes);
+      bulk_g2s(buf, copy_src, kProbeCopyBytes, &copy_done);
+      const uint64_t t0 = global_timer_ns();
+      const bool ok = mbar_wait(&never, 0, ab_short);
+      report[0] = global_timer_ns() - t0;
+      if (!ok) atomicAdd(&gave_up, 1u);
+      volatile int drain_flag = 0;
+      const AbortState drain_ab{&drain_flag, nullptr, kDrainNs, 0};
+      report[3] = mbar_wait(&copy_done, 0, drain_ab) ? 1ull : 0ull;
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint64_t t0 = global_timer_ns();
+      const bool ok = mbar_wait(&never, 0, ab_long);
+      report[1] = global_timer_ns() - t0;
+      if (!ok) atomicAdd(&gave_up, 1u);
+    }
+    __syncwarp();
+  } else {
+    if (!mbar_wait(&never, 0, ab_long)) atomicAdd(&gave_up, 1u);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  for (int i = threadIdx.x; i < kProbeCopyBytes / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(copy_out)[i] = reinterpret_cast<const uint4*>(buf)[i];
+  if (threadIdx.x == 0) report[2] = gave_up;
+  if (warp == 0) tmem_dealloc(tbase, 32);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_once;
 
@@ -306,6 +381,16 @@ int32_t fi_diag_umma(int32_t mode, const void* a, const void* b, float* c, int32
                            smem) != cudaSuccess)
     return 4;
   fi::umma_probe_kernel<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(p);
+  return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}
+
+int32_t fi_diag_wait_timeout(uint64_t timeout_ns, const uint8_t* copy_src, uint8_t* copy_out,
+                             int32_t* status, unsigned long long* report, void* stream) {
+  if (!copy_src || !copy_out || !status || !report || !fi::a16(copy_src) || !fi::a16(copy_out) ||
+      timeout_ns == 0 || timeout_ns > 1000000000ull)
+    return 1;
+  fi::wait_timeout_probe_kernel<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+      timeout_ns, copy_src, copy_out, status, report);
   return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }
 

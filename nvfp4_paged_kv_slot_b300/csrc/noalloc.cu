@@ -149,10 +149,13 @@ extern "C" fi_status fi_prefill_noalloc(const int32_t* qo_indptr_host,
   fi_status st = scratch_address(&scratch);
   if (st != FI_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // Copies from pageable host memory: each waits for the stream's earlier
-  // work and returns once the source has been staged, so the host buffers
-  // below may be reused at once and an earlier call's kernel on this stream
-  // has finished reading the scratch before it is overwritten.
+  // The copies and the kernel are enqueued on `stream`, so stream order puts
+  // every copy after the stream's earlier work (an earlier call's kernel has
+  // finished reading the scratch) and before this call's kernel.  The work
+  // list is staged in a stack buffer: pageable memory, whose copy has read
+  // the source when cudaMemcpyAsync returns, so the buffer may be refilled at
+  // once.  The caller's indptr arrays are read when the stream reaches their
+  // copies if they are page-locked (the header says so).
   if (!status_dev && cudaMemsetAsync(scratch, 0, kStatusWords * sizeof(int32_t), s) != cudaSuccess)
     return FI_ERR_CUDA;
   if (cudaMemcpyAsync(scratch + off_qo, qo_indptr_host, nb * sizeof(int32_t),

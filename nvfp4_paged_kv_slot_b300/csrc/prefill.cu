@@ -17,9 +17,9 @@
 //   warp 3        idle
 //   WG 1..NQ      softmax, one warpgroup per Q tile, one thread per query row:
 //                 the row of S in registers (one tensor-memory read), online
-//                 softmax in fp32 (base 2, paired fp32 arithmetic, exp2 split
-//                 between the MUFU unit and an FMA-pipe polynomial), P written
-//                 back to tensor memory over S as fp16, lazy O rescale, epilogue
+//                 softmax in fp32 (base 2, paired fp32 arithmetic, exp2 on the
+//                 MUFU unit), P written back to tensor memory over S as fp16,
+//                 lazy O rescale, epilogue
 //   last WG       repack: raw FP4 tile -> exact 16-bit tile in the swizzled
 //                 layout the tensor cores read (K as bf16, V as fp16)
 // The NQ Q tiles of a CTA are NQ query heads of one GQA group at the same
@@ -27,6 +27,7 @@
 // Tensor memory: S_i at column 128 i, O_i after all S.  Registers are moved
 // to the softmax warpgroups with setmaxnreg.  All waits are bounded.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 
 #include "internal.h"
@@ -41,17 +42,15 @@ constexpr uint64_t kDrainNs = 100000000ull;     // 0.1 s per wait while aborting
 // The running max is moved (and O rescaled) only when it grows by more than
 // 2^kLazyRescale, so P stays below 2^kLazyRescale (exact range for fp16 P).
 constexpr float kLazyRescale = 8.0f;
-// Outside the diagonal tiles, element pairs k (0..31 per half row) with
-// (k & kPolyMask) == kPolyMask take exp2 on the FMA pipe, the others on the
-// MUFU unit.  On B300 the MUFU unit keeps up (measured: every pair on MUFU is
-// 4% faster than one pair in four on the FMA pipe), so the mask selects none.
-constexpr int kPolyMask = 64;
 // Threads of the repack role: the last warpgroup.  (Adding warps 2-3 was
 // measured slower: they share the schedulers of two softmax warps.)
 constexpr int kRepackThreads = 128;
+// Devices whose cluster occupancy is cached by the launcher.
+constexpr int kMaxDevices = 64;
 
 struct PrefillParams {
   CUtensorMap tmap_q;  // 3-D view of q: (head_dim, num_qo_heads, total_qo)
+  const __nv_bfloat16* q;  // the same memory (L2 prefetch before the grid wait)
   const uint8_t* k_data;
   const uint8_t* v_data;
   const uint8_t* k_sf;
@@ -213,31 +212,6 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// 2^x for a pair of fp32 arguments x <= 2^7, on the FMA and integer pipes
-// instead of the MUFU unit: x = n + f with n = round(x), read from the low
-// mantissa bits of x + 1.5 * 2^23, and f = x - n in [-1/2, 1/2]; 2^f by a
-// degree-3 polynomial fitted to the relative error on [-1/2, 1/2]
-// (coefficients derived by csrc/exp2_poly_fit.py; max relative error 7.5e-5,
-// below the 2^-11 rounding of the fp16 P it feeds); 2^n by adding n to the
-// exponent field.  Arguments are clamped at -120 (2^-120 is zero in fp16 P).
-__device__ __forceinline__ uint64_t exp2_fma_x2(uint64_t x2) {
-  float x0, x1;
-  f2_unpack(x2, x0, x1);
-  const uint64_t xc = f2_pack(fmaxf(x0, -120.0f), fmaxf(x1, -120.0f));
-  const uint64_t magic = f2_pack(12582912.0f, 12582912.0f);
-  const uint64_t t = f2_add(xc, magic);
-  const uint64_t f = f2_sub(xc, f2_sub(t, magic));
-  uint64_t q = f2_fma(f2_pack(0.055171623826026917f, 0.055171623826026917f), f,
-                      f2_pack(0.2426111251115799f, 0.2426111251115799f));
-  q = f2_fma(q, f, f2_pack(0.6932609677314758f, 0.6932609677314758f));
-  q = f2_fma(q, f, f2_pack(0.9999280571937561f, 0.9999280571937561f));
-  float q0, q1, t0, t1;
-  f2_unpack(q, q0, q1);
-  f2_unpack(t, t0, t1);
-  return f2_pack(__uint_as_float(__float_as_uint(q0) + (__float_as_uint(t0) << 23)),
-                 __uint_as_float(__float_as_uint(q1) + (__float_as_uint(t1) << 23)));
-}
-
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -321,9 +295,27 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR, KVF>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const AbortState ab{abort_flag, p.status, kTimeoutNs, FI_DEV_WAIT_TIMEOUT};
-  // Everything above overlaps the previous grid of the stream when this one
-  // is launched as its programmatic dependent; every input (Q, the cache
-  // the append wrote, the plan, the page table) is read after this wait.
+  // Everything up to grid_dep_wait overlaps the previous grid of the stream
+  // when this one is launched as its programmatic dependent (the prefetch
+  // before the wait of the FlashInfer PR #8210 page, "FlashInfer: sm_107a
+  // 아키텍처를 위한 Fused Decode List Scorer 프리페칭 최적화").  The Q rows and
+  // the page-table row of this CTA's first unit are pulled into L2 here: a
+  // prefetch writes nothing and L2 stays coherent with the previous grid's
+  // writes, so results cannot change.  Finding the first unit reads only the
+  // plan's memory, which no kernel writes (its copy completed before the
+  // previous grid started).  Every input is read after the wait.
+  if (warp == 2) {
+    const UnitCursor uc = unit_first(p, u0, ustride);
+    if (uc.unit >= 0) {
+      const Unit w = decode_unit(p, uc.unit, heads_per_unit, head_off);
+      const int rows = min(kTileQ, w.qo_len - w.qt * kTileQ);
+      const __nv_bfloat16* q0 =
+          p.q + (static_cast<int64_t>(w.qo_start + w.qt * kTileQ) * p.num_qo_heads + w.hq0) * D;
+      for (int r = lane; r < rows; r += 32)
+        prefetch_l2_bulk(q0 + static_cast<int64_t>(r) * p.num_qo_heads * D, NQ * D * 2);
+      if (lane == 0) prefetch_l2_line(p.page_table + static_cast<int64_t>(w.b) * p.pt_stride);
+    }
+  }
   grid_dep_wait();
   grid_dep_launch();
 
@@ -695,14 +687,9 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR, KVF>::kThreads, 1)
             const uint64_t x2 =
                 f2_fma(f2_pack(__uint_as_float(sv[2 * k]), __uint_as_float(sv[2 * k + 1])),
                        scale2, negm2);
-            uint64_t p2;
-            if (!masked && (k & kPolyMask) == kPolyMask) {
-              p2 = exp2_fma_x2(x2);
-            } else {
-              float x0, x1;
-              f2_unpack(x2, x0, x1);
-              p2 = f2_pack(ex2(x0), ex2(x1));
-            }
+            float x0, x1;
+            f2_unpack(x2, x0, x1);
+            const uint64_t p2 = f2_pack(ex2(x0), ex2(x1));
             acc[k & 3] = f2_add(acc[k & 3], p2);
             float p0, p1;
             f2_unpack(p2, p0, p1);
@@ -801,22 +788,30 @@ fi_status launch_impl(const PrefillParams& p, int grid, cudaStream_t stream) {
   cl[0].val.clusterDim.x = 2;
   cl[0].val.clusterDim.y = 1;
   cl[0].val.clusterDim.z = 1;
-  // as many pairs as can be resident at once (persistent), at most one per unit
-  static int max_clusters = 0;
-  if (max_clusters == 0) {
+  // As many pairs as can be resident at once (persistent), at most one per
+  // unit.  The occupancy query is cached per device (0 = not yet known); a
+  // race between host threads only repeats the same query.
+  static std::atomic<int> max_clusters[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FI_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FI_ERR_UNSUPPORTED;
+  int n_clusters = max_clusters[dev].load(std::memory_order_relaxed);
+  if (n_clusters == 0) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FI_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * 74);
+    cfg.gridDim = dim3(2 * std::max(sms / 2, 1));
     cfg.blockDim = dim3(L::kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = cl;
     cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0)
+    if (cudaOccupancyMaxActiveClusters(&n_clusters, kern, &cfg) != cudaSuccess || n_clusters <= 0)
       return FI_ERR_CUDA;
-    max_clusters = n;
+    max_clusters[dev].store(n_clusters, std::memory_order_relaxed);
   }
-  const int pairs = std::max(1, std::min(grid / 2, max_clusters));
+  const int pairs = std::max(1, std::min(grid / 2, n_clusters));
   return launch_pdl(kern, dim3(2 * pairs), dim3(L::kThreads), smem, stream, p, cl, 1);
 }
 
@@ -848,6 +843,7 @@ fi_status launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
                                  static_cast<uint64_t>(D) * 2,
                                  static_cast<uint64_t>(P.num_qo_heads) * D * 2, 64, 1, kTileQ))
     return FI_ERR_CUDA;
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.k_data = a.cache.k_data;
   p.v_data = a.cache.v_data;
   p.k_sf = a.cache.k_sf;

@@ -115,3 +115,13 @@ def test_decode_equals_prefill_path_on_the_same_inputs():
     assert (lse_d - lse_p).abs().max().item() <= 1e-3
     m.fi_plan_destroy(plan)
     m.fi_context_destroy(ctx)
+
+
+def test_decode_page_id_out_of_range_flagged():
+    """A page-table entry outside [0, num_pages) is read as page 0 and flagged
+    with FI_DEV_PAGE_OOB (the run neither faults nor reads outside the cache)."""
+    d = device_inputs("decode_small")
+    d["page_table"][3, 2] = 1 << 20
+    d["page_table"][4, 0] = -5
+    _, _, _, status, _ = _run_decode(d)
+    assert status & fi().FI_DEV_PAGE_OOB

@@ -4,10 +4,14 @@ before touching memory.  Kernels adjacent in one stream, eagerly and in a CUDA
 graph, must give the same bytes as the same calls separated by a host sync,
 including a prefill followed by an append that overwrites the cache the
 prefill reads."""
+import numpy as np
 import pytest
 import torch
 
-from gpu_util import device_inputs, fi, gpu_cache
+import oracle as O
+import workloads as W
+from gpu_util import (assert_within_tolerance, compare_attention, device_inputs, fi, gpu_cache,
+                      oracle_attention, oracle_cache)
 
 pytestmark = pytest.mark.gpu
 
@@ -62,6 +66,18 @@ def test_adjacent_append_and_prefill_equal_synced_calls(name):
     assert torch.equal(out2, ref2)
     for name_t in ("k_data", "v_data", "k_sf", "v_sf"):
         assert torch.equal(getattr(c, name_t), getattr(c2, name_t))
+    # and both prefills against the oracle: the first on the cache of the
+    # first append, the second on the cache both appends leave
+    h = d["host"]
+    host = oracle_cache(d)
+    ref_out, _ = oracle_attention(d, host)
+    assert_within_tolerance(compare_attention(out1, None, ref_out, None))
+    assert O.append(W.bits(k2), W.bits(v2), d["k_scale"], d["v_scale"],
+                    h["slot_mapping"].numpy(), host) == 0
+    for name_t in ("k_data", "v_data", "k_sf", "v_sf"):
+        assert np.array_equal(getattr(c, name_t).cpu().numpy(), host[name_t]), name_t
+    ref_out2, _ = oracle_attention(d, host)
+    assert_within_tolerance(compare_attention(out2, None, ref_out2, None))
     assert m.fi_device_status(ctx) == 0
     m.fi_plan_destroy(plan)
     m.fi_context_destroy(ctx)

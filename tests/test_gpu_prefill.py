@@ -46,6 +46,28 @@ def test_prefill_single_cta_path_for_groups_of_four(name, schedule):
     assert_within_tolerance(compare_attention(pair_out, pair_lse, ref_out, ref_lse))
 
 
+@pytest.mark.parametrize("name", ["offset_small", "offset_gqa3_d64", "offset_uniform_small"])
+@pytest.mark.parametrize("schedule", [0, 1, 2])
+@pytest.mark.parametrize("cta_pairs", [0, 1])
+def test_prefill_bottom_right_causal_matches_oracle(name, schedule, cta_pairs):
+    """qo_len < kv_len: query row i of a sequence sees keys j <= i + kv_len -
+    qo_len (the newest qo_len tokens query the whole cache), including a
+    sequence with no query rows inside a ragged batch, on the arithmetic
+    (uniform) and list (ragged) tile decodings, every schedule, and both the
+    CTA-pair and single-CTA kernels."""
+    d = device_inputs(name)
+    sp = d["spec"]
+    out, lse, cache, status, info = run_path(d, schedule=schedule, cta_pairs=cta_pairs)
+    assert status == 0
+    assert info["is_uniform"] == (len(set(sp.seq_lens)) == 1 and len(set(sp.qo_lens)) == 1)
+    if sp.group % 4 == 0:
+        assert info["ctas_per_unit"] == (1 if cta_pairs else 2)
+    ref_out, ref_lse = oracle_attention(d, oracle_cache(d))
+    res = compare_attention(out, lse, ref_out, ref_lse)
+    print(name, schedule, cta_pairs, info, res)
+    assert_within_tolerance(res)
+
+
 def test_prefill_single_sequence_2048_sampled():
     d = device_inputs("single")
     out, lse, cache, status, info = run_path(d)

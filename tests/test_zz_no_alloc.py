@@ -1,5 +1,6 @@
-"""fi_prefill_noalloc, the prefill entry point that allocates no memory, checked
-against the regular plan + run path through the C ABI.
+"""fi_prefill_noalloc, the prefill entry point that allocates no memory, through
+the C ABI: every call is checked against the fp64 oracle and against the
+regular plan + run path on the same inputs.
 
 Some callers cannot allocate while they run: a serving engine that reserves
 all device memory for its KV cache up front and forbids allocation while it
@@ -15,7 +16,9 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_util import (OUT_MAX_ABS, OUT_MEAN_ABS, LSE_MAX_ABS, device_inputs, fi, gpu_cache)
+from gpu_util import (OUT_MAX_ABS, OUT_MEAN_ABS, LSE_MAX_ABS, assert_within_tolerance,
+                      compare_attention, device_inputs, fi, gpu_cache, oracle_attention,
+                      oracle_cache, sample_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -24,6 +27,15 @@ pytestmark = pytest.mark.gpu
 def _need_gpu():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
+
+
+def _append(m, d):
+    cache = gpu_cache(d)
+    ctx = m.fi_context_create()
+    m.fi_nvfp4_append(ctx, d["k"], d["v"], cache.k_scale, cache.v_scale, d["slot_mapping"], cache)
+    assert m.fi_device_status(ctx) == 0
+    m.fi_context_destroy(ctx)
+    return cache
 
 
 def _regular(m, d, cache):
@@ -42,9 +54,9 @@ def _regular(m, d, cache):
     return out, lse
 
 
-def _noalloc(m, d, cache):
+def _noalloc(m, d, cache, with_status=True):
     """Calls the C entry point directly (ctypes), with caller-owned outputs and
-    a caller-owned status word."""
+    a caller-owned status word (or none: the bits are then discarded)."""
     sp = d["spec"]
     qo = np.ascontiguousarray(d["host"]["qo_indptr"].numpy(), dtype=np.int32)
     kv = np.ascontiguousarray(d["host"]["kv_indptr"].numpy(), dtype=np.int32)
@@ -57,7 +69,8 @@ def _noalloc(m, d, cache):
                                   d["page_table"].data_ptr(), d["page_table"].stride(0),
                                   sp.num_qo_heads, sp.num_kv_heads, sp.head_dim, sp.page_size,
                                   float(d["sm_scale"]), d["q"].data_ptr(), C.byref(cc),
-                                  out.data_ptr(), lse.data_ptr(), status.data_ptr(), stream)
+                                  out.data_ptr(), lse.data_ptr(),
+                                  status.data_ptr() if with_status else None, stream)
     assert rc == m.FI_OK, m.lib.fi_status_string(rc).decode()
     torch.cuda.synchronize()
     assert int(status.item()) == 0
@@ -70,21 +83,42 @@ def _close(a, b, la, lb):
     assert float((la - lb).abs().max()) <= LSE_MAX_ABS
 
 
-def test_noalloc_matches_plan_and_run_on_two_calls_in_a_row():
-    """Two consecutive calls with different batches (ragged, then uniform):
-    the second call must not see anything the first left in the shared scratch."""
+def test_noalloc_matches_oracle_and_plan_and_run_on_calls_in_a_row():
+    """Consecutive calls with different batches (ragged, uniform, then newest
+    tokens over a longer cache with a sequence that has no query rows): no call
+    may see anything an earlier one left in the shared scratch."""
     m = fi()
-    for name in ("ragged_small", "uniform_small"):
+    for name in ("ragged_small", "uniform_small", "offset_small"):
         d = device_inputs(name)
-        cache = gpu_cache(d)
-        ctx = m.fi_context_create()
-        m.fi_nvfp4_append(ctx, d["k"], d["v"], cache.k_scale, cache.v_scale,
-                          d["slot_mapping"], cache)
-        assert m.fi_device_status(ctx) == 0
-        m.fi_context_destroy(ctx)
-        ref_out, ref_lse = _regular(m, d, cache)
+        cache = _append(m, d)
         out, lse = _noalloc(m, d, cache)
-        _close(out, ref_out, lse, ref_lse)
+        ref_out, ref_lse = oracle_attention(d, oracle_cache(d))
+        assert_within_tolerance(compare_attention(out, lse, ref_out, ref_lse))
+        reg_out, reg_lse = _regular(m, d, cache)
+        _close(out, reg_out, lse, reg_lse)
+
+
+def test_noalloc_many_units_without_a_status_word():
+    """2292 ragged work units: the list is staged to the scratch in pieces of
+    1024 units (two full pieces and a tail, at growing offsets).  The first call
+    passes no status word (the bits go to the scratch and are discarded), the
+    second one does; both agree with plan + run on every row and with the
+    oracle on sampled rows."""
+    m = fi()
+    d = device_inputs("many_units")
+    sp = d["spec"]
+    qo = d["host"]["qo_indptr"].numpy()
+    units = sum(-(-int(qo[b + 1] - qo[b]) // 128) for b in range(len(qo) - 1)) * \
+        sp.num_kv_heads * (sp.group // 2)
+    assert units > 2 * 1024
+    cache = _append(m, d)
+    reg_out, reg_lse = _regular(m, d, cache)
+    rows = sample_rows(d, 2000, seed=11)
+    ref_out, ref_lse = oracle_attention(d, oracle_cache(d), rows=rows)
+    for with_status in (False, True):
+        out, lse = _noalloc(m, d, cache, with_status=with_status)
+        _close(out, reg_out, lse, reg_lse)
+        assert_within_tolerance(compare_attention(out, lse, ref_out, ref_lse, rows=rows))
 
 
 def test_noalloc_rejects_batches_beyond_its_scratch():

@@ -39,7 +39,8 @@ class Spec:
     page_size: int
     num_qo_heads: int = 0          # 0: append-only workload
     seq_lens: list = field(default_factory=list)   # kv_len per sequence (qo_len too, unless qo_lens)
-    qo_lens: list = field(default_factory=list)    # decode: the newest qo_len tokens query
+    qo_lens: list = field(default_factory=list)    # the newest qo_len tokens query (else all)
+    attn: str = "prefill"          # attention the workload feeds: "prefill" or "decode"
     append_tokens: int = 0         # append-only workloads
     num_pages: int = 0             # append-only workloads
     skip_fraction: float = 0.0     # fraction of slots set to -1 (append-only)
@@ -95,19 +96,37 @@ def spec(name: str) -> Spec:
     # Decode: the newest 1..8 tokens of each sequence query its whole cache.
     if name == "decode":
         return Spec("decode", 10000, num_kv_heads=8, head_dim=128, page_size=16,
-                    num_qo_heads=32, seq_lens=[4096] * 128, qo_lens=[1] * 128)
+                    num_qo_heads=32, seq_lens=[4096] * 128, qo_lens=[1] * 128, attn="decode")
     if name == "decode_small":
         return Spec("decode_small", 11000, num_kv_heads=2, head_dim=128, page_size=16,
-                    num_qo_heads=8, seq_lens=[1, 40, 300, 1000, 5000], qo_lens=[1] * 5)
+                    num_qo_heads=8, seq_lens=[1, 40, 300, 1000, 5000], qo_lens=[1] * 5, attn="decode")
     if name == "decode_spec_small":
         return Spec("decode_spec_small", 12000, num_kv_heads=2, head_dim=128, page_size=16,
-                    num_qo_heads=8, seq_lens=[8, 130, 700, 2600], qo_lens=[1, 3, 8, 2])
+                    num_qo_heads=8, seq_lens=[8, 130, 700, 2600], qo_lens=[1, 3, 8, 2], attn="decode")
     if name == "decode_d64":
         return Spec("decode_d64", 13000, num_kv_heads=4, head_dim=64, page_size=32,
-                    num_qo_heads=8, seq_lens=[257, 1500, 90], qo_lens=[1, 2, 1])
+                    num_qo_heads=8, seq_lens=[257, 1500, 90], qo_lens=[1, 2, 1], attn="decode")
     if name == "uniform_small":
         return Spec("uniform_small", 7000, num_kv_heads=2, head_dim=128, page_size=16,
                     num_qo_heads=8, seq_lens=[384] * 6)
+    # Prefill of the newest qo_len tokens of each sequence over a longer cache
+    # (bottom-right causal alignment), with a sequence that has no query rows
+    # inside a non-empty ragged batch; GQA 4 (CTA pairs) and 3 (one head per CTA).
+    if name == "offset_small":
+        return Spec("offset_small", 14000, num_kv_heads=2, head_dim=128, page_size=16,
+                    num_qo_heads=8, seq_lens=[300, 130, 64, 900], qo_lens=[1, 130, 0, 257])
+    if name == "offset_gqa3_d64":
+        return Spec("offset_gqa3_d64", 15000, num_kv_heads=2, head_dim=64, page_size=32,
+                    num_qo_heads=6, seq_lens=[200, 77, 1000, 129], qo_lens=[200, 0, 129, 5])
+    # The same offset for every sequence: the uniform (arithmetic) tile decoding
+    # with qo_len < kv_len.
+    if name == "offset_uniform_small":
+        return Spec("offset_uniform_small", 16000, num_kv_heads=2, head_dim=128, page_size=16,
+                    num_qo_heads=8, seq_lens=[600] * 4, qo_lens=[200] * 4)
+    # Many ragged work units (more than a thousand q-tiles x head units).
+    if name == "many_units":
+        return Spec("many_units", 17000, num_kv_heads=2, head_dim=128, page_size=16,
+                    num_qo_heads=8, seq_lens=ragged_lengths(128, 1, 4000, 17000))
     raise KeyError(name)
 
 
@@ -120,7 +139,8 @@ def sample_spec(name: str, n_seqs: int, seed: int = 0) -> Spec:
     return Spec(f"{name}_sample{seed}", sp.seed + 100 + seed, num_kv_heads=sp.num_kv_heads,
                 head_dim=sp.head_dim, page_size=sp.page_size, num_qo_heads=sp.num_qo_heads,
                 seq_lens=[sp.seq_lens[i] for i in sorted(idx)],
-                qo_lens=[sp.qo_lens[i] for i in sorted(idx)] if sp.qo_lens else [])
+                qo_lens=[sp.qo_lens[i] for i in sorted(idx)] if sp.qo_lens else [],
+                attn=sp.attn)
 
 
 def _bf16_normal(shape, gen, device, outlier_p=0.0, outlier_scale=20.0):
