@@ -117,6 +117,7 @@ struct Layout {
   static constexpr int kRegRepack = 64;
   static constexpr int kRegSoftmax = NQ == 2 ? 160 : 232;
   static_assert(kOffStg % 1024 == 0 && kStg % 1024 == 0, "swizzled tiles need 1 KB alignment");
+  static_assert(kAlloc <= 232448, "at most 227 KB of shared memory per CTA");
   static_assert(kRaw % 16 == 0 && kOffRaw % 16 == 0, "bulk copies need 16 B alignment");
 };
 
@@ -535,6 +536,9 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR, KVF>::kThreads, 1)
             tc_fence_after();
             issue_pv_half(i, ss_v, 1, true);
             if (i == NQ - 1) release_stg(ss_v);
+            // O_i of this unit is complete once this PV is: the epilogue of
+            // head i need not wait for the other heads' last PVs
+            if (!more) mma_commit(o_full + i);
             if (more) {
               if (i == 0) {
                 ss_k = stg_k % L::kStgStages;
@@ -552,7 +556,6 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR, KVF>::kThreads, 1)
           }
         }
         if (!ok) break;
-        for (int i = 0; i < NQ; ++i) mma_commit(o_full + i);
       }
       // Every MMA this thread issued has completed once `drain` arrives.
       mma_commit(drain);
