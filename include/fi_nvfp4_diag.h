@@ -63,6 +63,18 @@ int32_t fi_diag_repack_tile(const uint8_t* raw, int32_t head_dim, int32_t is_v, 
 int32_t fi_diag_umma(int32_t mode, const void* a, const void* b, float* c, int32_t* status,
                      void* stream);
 
+/* One M=256 x N=128 x K=128 tcgen05 MMA issued for a pair of CTAs (one
+ * 2-CTA cluster, cta_group::2), fp32 result c [256][128]:
+ *   mode 0: c = A * B^T, A bf16 [256][128] K-major (CTA r holds rows
+ *           128r..128r+127), B bf16 [128 N][128 K] K-major, N rows split
+ *           64 per CTA (as the paired prefill's S = Q K^T);
+ *   mode 1: c = A * B, A fp16 [256][128 K] K-major, B fp16 [128 K][128 N]
+ *           MN-major, N columns split 64 per CTA (as its O = P V).
+ * tmem_addrs (device, 2 x uint32): the tensor-memory base address each CTA
+ * was allocated.  `status` gets bit 16 if a wait ran out of time. */
+int32_t fi_diag_umma_pair(int32_t mode, const void* a, const void* b, float* c, int32_t* status,
+                          uint32_t* tmem_addrs, void* stream);
+
 /* Makes a bounded pipeline wait run out, with the library's own wait code: a
  * one-CTA kernel whose warps wait on an mbarrier that nothing arrives at.
  * Warp 0 holds tensor memory, has a 4096-byte bulk copy (copy_src -> shared

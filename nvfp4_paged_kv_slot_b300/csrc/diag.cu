@@ -276,6 +276,104 @@ __global__ void __launch_bounds__(128, 1)
   if (warp == 0) tmem_dealloc(tbase, 32);
 }
 
+// One M=256 N=128 K=128 MMA over a CTA pair (cta_group::2), as the paired
+// prefill issues them.  CTA r stages rows 128 r .. 128 r + 127 of A (K-major,
+// bf16 in mode 0, fp16 in mode 1) and its half of B: mode 0 (S = Q K^T) rows
+// 64 r .. 64 r + 63 of B [128 N][128 K] (K-major, 64-row column blocks of
+// 8 KB); mode 1 (O = P V) columns 64 r .. 64 r + 63 of B [128 K][128 N]
+// (MN-major, one 16 KB block).  The even CTA issues the MMAs and a commit to
+// both CTAs' barriers; each CTA reads its 128 rows of D.  tmem_addrs[r]: the
+// tensor-memory base each CTA was given.
+struct UmmaPairParams {
+  const uint16_t* a;
+  const uint16_t* b;
+  float* c;
+  int32_t* status;
+  uint32_t* tmem_addrs;
+  int mode;
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
+    umma_pair_probe_kernel(const __grid_constant__ UmmaPairParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sa = smem;
+  uint8_t* sb = smem + 32768;
+  uint64_t* bar_mma = reinterpret_cast<uint64_t*>(smem + 49152);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_mma + 1);
+  int* abort_flag = reinterpret_cast<int*>(tslot + 1);
+  const uint32_t rank = cluster_ctarank();
+  const int tid = threadIdx.x;
+  const int warp = tid / 32;
+  if (tid == 0) {
+    mbar_init(bar_mma, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc_pair(tslot, 256);
+    tmem_relinquish_pair();
+  }
+  // row tid of this CTA's half of A
+  const uint16_t* arow = p.a + (128 * rank + tid) * 128;
+  for (int c = 0; c < 16; ++c)
+    *reinterpret_cast<uint4*>(sa + sw128_offset(tid, c)) = *reinterpret_cast<const uint4*>(arow + 8 * c);
+  if (p.mode == 0) {
+    if (tid < 64) {
+      const uint16_t* brow = p.b + (64 * rank + tid) * 128;
+      for (int c = 0; c < 16; ++c)
+        *reinterpret_cast<uint4*>(sb + (c >> 3) * 8192 + tid * 128 + (((c & 7) ^ (tid & 7)) << 4)) =
+            *reinterpret_cast<const uint4*>(brow + 8 * c);
+    }
+  } else {
+    const uint16_t* brow = p.b + tid * 128 + 64 * rank;
+    for (int c = 0; c < 8; ++c)
+      *reinterpret_cast<uint4*>(sb + sw128_offset(tid, c)) = *reinterpret_cast<const uint4*>(brow + 8 * c);
+  }
+  fence_proxy_async_cluster();
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tbase = *tslot;
+  if (tid == 0) p.tmem_addrs[rank] = tbase;
+  const AbortState ab{abort_flag, p.status, kProbeTimeoutNs, 1 << 16};
+  if (rank == 0 && tid == 0) {
+    const uint32_t a_addr = smem_u32(sa), b_addr = smem_u32(sb);
+    if (p.mode == 0) {
+      constexpr uint32_t idesc = idesc_f16(1, 0, 0, 256, 128);
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t a_off = (kk >> 2) * 16384 + (kk & 3) * 32;
+        const uint32_t b_off = (kk >> 2) * 8192 + (kk & 3) * 32;
+        mma_ss_pair(tbase, smem_desc_sw128(a_addr + a_off, 16, 1024),
+                    smem_desc_sw128(b_addr + b_off, 16, 1024), idesc, kk > 0);
+      }
+    } else {
+      constexpr uint32_t idesc = idesc_f16(0, 0, 1, 256, 128);
+      for (int s = 0; s < 8; ++s) {
+        const uint32_t a_off = (s >> 2) * 16384 + (s & 3) * 32;
+        mma_ss_pair(tbase, smem_desc_sw128(a_addr + a_off, 16, 1024),
+                    smem_desc_sw128(b_addr + s * 2048, 16384, 1024), idesc, s > 0);
+      }
+    }
+    mma_commit_pair(bar_mma, 3);
+  }
+  __syncwarp();
+  mbar_wait(bar_mma, 0, ab);
+  tc_fence_after();
+  const uint32_t lane_base = tbase + ((static_cast<uint32_t>(warp) * 32) << 16);
+  for (int c = 0; c < 4; ++c) {
+    uint32_t v[32];
+    tmem_ld32(lane_base + c * 32, v);
+    for (int k = 0; k < 32; ++k)
+      p.c[(128 * rank + tid) * 128 + c * 32 + k] = __uint_as_float(v[k]);
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc_pair(tbase, 256);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_once;
 
@@ -381,6 +479,26 @@ int32_t fi_diag_umma(int32_t mode, const void* a, const void* b, float* c, int32
                            smem) != cudaSuccess)
     return 4;
   fi::umma_probe_kernel<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(p);
+  return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}
+
+int32_t fi_diag_umma_pair(int32_t mode, const void* a, const void* b, float* c, int32_t* status,
+                          uint32_t* tmem_addrs, void* stream) {
+  if ((mode != 0 && mode != 1) || !a || !b || !c || !status || !tmem_addrs || !fi::a16(a) ||
+      !fi::a16(b))
+    return 1;
+  fi::UmmaPairParams p;
+  p.a = static_cast<const uint16_t*>(a);
+  p.b = static_cast<const uint16_t*>(b);
+  p.c = c;
+  p.status = status;
+  p.tmem_addrs = tmem_addrs;
+  p.mode = mode;
+  const int smem = 49152 + 64 + 1024;
+  if (cudaFuncSetAttribute(fi::umma_pair_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem) != cudaSuccess)
+    return 4;
+  fi::umma_pair_probe_kernel<<<2, 128, smem, static_cast<cudaStream_t>(stream)>>>(p);
   return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }
 

@@ -15,7 +15,7 @@ if not LIB_PATH.exists():
 lib = C.CDLL(str(LIB_PATH))
 
 EXPORTED = ("fi_diag_codec_span", "fi_diag_quantize_blocks", "fi_diag_div_check",
-            "fi_diag_repack_tile", "fi_diag_umma", "fi_diag_wait_timeout")
+            "fi_diag_repack_tile", "fi_diag_umma", "fi_diag_wait_timeout", "fi_diag_umma_pair")
 
 _vp = C.c_void_p
 lib.fi_diag_codec_span.argtypes = [C.c_uint32, C.c_uint64, _vp, _vp, _vp]
@@ -24,6 +24,7 @@ lib.fi_diag_div_check.argtypes = [_vp, C.c_int32, _vp, _vp, _vp]
 lib.fi_diag_repack_tile.argtypes = [_vp, C.c_int32, C.c_int32, C.c_int32, _vp, _vp]
 lib.fi_diag_umma.argtypes = [C.c_int32, _vp, _vp, _vp, _vp, _vp]
 lib.fi_diag_wait_timeout.argtypes = [C.c_uint64, _vp, _vp, _vp, _vp, _vp]
+lib.fi_diag_umma_pair.argtypes = [C.c_int32, _vp, _vp, _vp, _vp, _vp, _vp]
 for _n in EXPORTED:
     getattr(lib, _n).restype = C.c_int32
 
@@ -68,3 +69,8 @@ def wait_timeout(timeout_ns: int, copy_src, copy_out, status, report):
     _ok(lib.fi_diag_wait_timeout(int(timeout_ns), copy_src.data_ptr(), copy_out.data_ptr(),
                                  status.data_ptr(), report.data_ptr(), _s()),
         "fi_diag_wait_timeout")
+
+
+def umma_pair(mode: int, a, b, c, status, tmem_addrs):
+    _ok(lib.fi_diag_umma_pair(mode, a.data_ptr(), b.data_ptr(), c.data_ptr(), status.data_ptr(),
+                              tmem_addrs.data_ptr(), _s()), "fi_diag_umma_pair")

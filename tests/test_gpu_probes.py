@@ -165,3 +165,25 @@ def test_tcgen05_layouts(diag, mode):
     want = (a.double() @ b.double().T) if mode == 0 else (a.double() @ b.double())
     err = (c.cpu().double() - want).abs().max().item()
     assert err < 1e-3, f"mode {mode}: max err {err}"
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_tcgen05_pair_mma_layouts(diag, mode):
+    """The 2-CTA MMA (cta_group::2, M = 256) of the paired prefill: A split by
+    rows between the CTAs, B split by N (K-major rows for S = Q K^T, MN-major
+    columns for O = P V); each CTA's tensor memory holds its 128 rows of the
+    exact product (fp64 reference)."""
+    g = torch.Generator().manual_seed(10 + mode)
+    dt = torch.bfloat16 if mode == 0 else torch.float16
+    a = (torch.randn((256, 128), generator=g) * 0.5).to(dt)
+    b = (torch.randn((128, 128), generator=g) * 0.5).to(dt)
+    c = torch.empty((256, 128), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    addrs = torch.full((2,), -1, dtype=torch.int32, device="cuda")
+    diag.umma_pair(mode, a.cuda(), b.cuda(), c, st, addrs)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert addrs[0].item() == addrs[1].item(), addrs.tolist()
+    want = (a.double() @ b.double().T) if mode == 0 else (a.double() @ b.double())
+    err = (c.cpu().double() - want).abs().max().item()
+    assert err < 1e-3, f"mode {mode}: max err {err}"
