@@ -415,6 +415,383 @@ __global__ void __launch_bounds__(32 * kDecWarps, MT == 1 ? 3 : 2)
   }
 }
 
+// ---- transposed form, for up to 16 rows per unit -------------------------
+// With few rows the row dimension is better placed on the MMA's n side (8
+// rows per n-tile) than on its 16-row m side: S^T = K Q^T takes keys as m,
+// O^T = V^T P^T takes head dimensions as m.  That halves the MMAs and the
+// accumulators of the form above, and both K and V fragments come straight
+// from the raw codes, so no dequantized copy of V is staged.
+//
+// The contraction index of each MMA may be permuted freely as long as both
+// operands agree, and the m index of O^T may be permuted as long as the
+// epilogue undoes it; both are chosen so that every lane converts contiguous
+// code bytes:
+//  * S^T, k-step s, lane (g = lane/4, t = lane%4): the A fragment's column
+//    pairs are code bytes t*D/8 + 2s (k = 2t, 2t+1) and t*D/8 + 2s + 1 (k =
+//    2t+8, 2t+9) of keys g and g+8 of the m-tile; Q's B fragment takes the
+//    same head dimensions, d = t*D/4 + 4s .. t*D/4 + 4s + 3, of row g.
+//  * O^T, m-tile i: row g of the tile is head dimension 2(g*D/16 + i), row
+//    g+8 the one after it, so a lane converts code bytes g*D/16 .. g*D/16 +
+//    D/16 - 1 of each key it touches; a pair of keys is merged nibble-wise
+//    into E2M1 pairs that hold one dimension of both keys.
+//  * The keys of the PV k-step are the S^T m-tile's rows in order; P^T's B
+//    fragment is the S^T accumulator packed to fp16 and transposed 8x8 by
+//    movmatrix.
+// Raw stage of one warp (32 keys, key = lane of the copy): K codes (D/2
+// bytes a key, unpadded: a quarter-warp reads 128 contiguous bytes), K
+// scales (D/16 bytes a key), V rows (D/2 codes, D/16 scales, padded to 80
+// or 48 bytes so that the 8-byte or 4-byte reads of a half-warp or warp hit
+// distinct banks).
+constexpr int kTWarps = 4;   // warps (units) per CTA
+constexpr int kTStages = 2;  // raw stages per warp: this step's and the next
+
+template <int D>
+constexpr int kTVRow = D == 128 ? 80 : 48;
+template <int D>
+constexpr int kTStage = 32 * (D / 2 + D / 16 + kTVRow<D>);
+template <int D>
+constexpr int decode_t_smem_bytes() {
+  return kTWarps * kTStages * kTStage<D>;
+}
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
+}
+
+// NT: 8-row n-tiles per unit (rows G * qo_len <= 8 NT).
+template <int D, int NT>
+__global__ void __launch_bounds__(32 * kTWarps, NT == 1 ? 4 : 3)
+    nvfp4_decode_t_kernel(const DecodeParams p) {
+  constexpr int kStage = kTStage<D>;
+  constexpr int kVR = kTVRow<D>;
+  constexpr int kKsf = 32 * (D / 2);         // K scales within a stage
+  constexpr int kV = 32 * (D / 2 + D / 16);  // V rows within a stage
+  constexpr int kKW = D / 32;                // code words of a key a lane converts for S^T
+  constexpr int kVW = D / 64;                // code words of a key a lane converts for O^T
+  extern __shared__ __align__(16) uint8_t dsm[];
+  grid_dep_wait();  // Q and the cache may come from the previous grid
+  grid_dep_launch();
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int g = lane / 4, t = lane % 4;
+  const int u = blockIdx.x * kTWarps + warp;
+  if (u >= p.num_units) return;  // no block-wide barrier below
+  const int4 w = __ldg(p.units + u);
+  const int b = w.x, hk = w.y, c = w.z, slot = w.w;
+  const int qo_start = __ldg(p.qo_indptr + b);
+  const int qo_len = __ldg(p.qo_indptr + b + 1) - qo_start;
+  const int kv_len = __ldg(p.kv_indptr + b + 1) - __ldg(p.kv_indptr + b);
+  const int G = p.group;
+  const int R = G * qo_len;  // <= 8 NT (the dispatch guarantees it)
+  const int delta = kv_len - qo_len;
+  const int k0 = c * p.chunk;
+  const int k1 = min(k0 + p.chunk, kv_len);
+  const float ks = __ldg(p.k_scale), vs = __ldg(p.v_scale);
+  uint8_t* ring = dsm + warp * kTStages * kStage;
+  const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.pt_stride;
+  auto q_ptr = [&](int r) {  // row r = token r / G, head hk * G + r % G
+    return p.q + (static_cast<int64_t>(qo_start + r / G) * p.num_qo_heads + hk * G + r % G) * D;
+  };
+
+  // Q^T as fp16 B fragments, scaled as in the form above (a power of two
+  // brings every |value| below 2^14; the logits are multiplied back).
+  const float qs = p.sm_scale * ks * 1.4426950408889634f;
+  float qmax = 0.0f;
+  for (int i = lane; i < R * (D / 8); i += 32) {
+    float x[8];
+    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(q_ptr(i / (D / 8)) + (i % (D / 8)) * 8)), x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) qmax = fmaxf(qmax, fabsf(x[e]));
+  }
+  qmax = warp_max(qmax) * qs;
+  const int qe = qmax > 0.0f ? ilogbf(qmax) - 13 : 0;
+  const float qsc = ldexpf(qs, -qe);
+  const float ssc = ldexpf(1.0f, qe);
+  uint32_t qb[NT][D / 16][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int r = 8 * nt + g;
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) {
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = 0.0f;
+      if (r < R) bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(q_ptr(r) + t * (D / 4)) + i), x);
+      qb[nt][2 * i][0] = f16x2_of(x[0] * qsc, x[1] * qsc);
+      qb[nt][2 * i][1] = f16x2_of(x[2] * qsc, x[3] * qsc);
+      qb[nt][2 * i + 1][0] = f16x2_of(x[4] * qsc, x[5] * qsc);
+      qb[nt][2 * i + 1][1] = f16x2_of(x[6] * qsc, x[7] * qsc);
+    }
+  }
+
+  // O^T accumulators (m-tile i, n-tile nt), and per lane the running max and
+  // sum of rows 8 nt + 2t + e.  The max is raised lazily: only when a step's
+  // max exceeds it by more than 8 (in log2 units), so exponentials stay at
+  // most 2^8 and the rescale of O is rare.
+  float o[D / 16][NT][4];
+  float mrun[NT][2], lrun[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      mrun[nt][e] = -INFINITY;
+      lrun[nt][e] = 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[i][nt][e] = 0.0f;
+  }
+
+  // Raw rows of key kbs + lane into stage st (one commit group per call).  A
+  // key past the chunk gets zero V scales, so its stale V codes weigh 0.
+  auto page_of = [&](int key) { return key < k1 ? __ldg(pt + key / p.page_size) : 0; };
+  int page_next = page_of(k0 + lane);
+  auto issue = [&](int kbs, int st) {
+    const int key = kbs + lane;
+    int page = page_next;
+    page_next = page_of(key + 32);
+    uint8_t* s = ring + st * kStage;
+    if (key < k1) {
+      if (page < 0 || page >= p.num_pages) {
+        atomicOr(p.status, FI_DEV_PAGE_OOB);
+        page = 0;
+      }
+      const int64_t row =
+          (static_cast<int64_t>(page) * p.num_kv_heads + hk) * p.page_size + key % p.page_size;
+      const uint8_t* kg = p.k_data + row * (D / 2);
+      const uint8_t* vg = p.v_data + row * (D / 2);
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) {
+        cp_async16(s + lane * (D / 2) + 16 * i, kg + 16 * i);
+        cp_async16(s + kV + lane * kVR + 16 * i, vg + 16 * i);
+      }
+      if constexpr (D == 128) {
+        cp_async8(s + kKsf + lane * 8, p.k_sf + row * 8);
+        cp_async8(s + kV + lane * kVR + 64, p.v_sf + row * 8);
+      } else {
+        cp_async4(s + kKsf + lane * 4, p.k_sf + row * 4);
+        cp_async4(s + kV + lane * kVR + 32, p.v_sf + row * 4);
+      }
+    } else {
+      if constexpr (D == 128)
+        *reinterpret_cast<uint2*>(s + kV + lane * kVR + 64) = make_uint2(0u, 0u);
+      else
+        *reinterpret_cast<uint32_t*>(s + kV + lane * kVR + 32) = 0u;
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int i = 0; i < kTStages - 1; ++i) issue(k0 + 32 * i, i);
+
+  int st = 0;
+  for (int kb = k0; kb < k1; kb += 32) {
+    __syncwarp();  // every lane is done with the stage read in the previous step
+    issue(kb + 32 * (kTStages - 1), st == 0 ? kTStages - 1 : st - 1);
+    cp_async_wait<kTStages - 1>();  // this lane's rows of this step have landed
+    __syncwarp();                   // ... and every lane's
+    const uint8_t* sb = ring + st * kStage;
+
+    // ---- S^T = K Q^T: m-tiles of keys 0-15 and 16-31.  Keys past k1 read
+    // stale bytes; their logits are replaced by -inf below.
+    float sacc[2][NT][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = 0.0f;
+      const int ka = 16 * mt + g, kz = ka + 8;
+      uint32_t ca[kKW], cz[kKW];
+      uint32_t sfa, sfz;
+      if constexpr (D == 128) {
+        const uint4 xa = *reinterpret_cast<const uint4*>(sb + ka * 64 + 16 * t);
+        const uint4 xz = *reinterpret_cast<const uint4*>(sb + kz * 64 + 16 * t);
+        ca[0] = xa.x; ca[1] = xa.y; ca[2] = xa.z; ca[3] = xa.w;
+        cz[0] = xz.x; cz[1] = xz.y; cz[2] = xz.z; cz[3] = xz.w;
+        sfa = *reinterpret_cast<const uint16_t*>(sb + kKsf + ka * 8 + 2 * t);
+        sfz = *reinterpret_cast<const uint16_t*>(sb + kKsf + kz * 8 + 2 * t);
+      } else {
+        const uint2 xa = *reinterpret_cast<const uint2*>(sb + ka * 32 + 8 * t);
+        const uint2 xz = *reinterpret_cast<const uint2*>(sb + kz * 32 + 8 * t);
+        ca[0] = xa.x; ca[1] = xa.y;
+        cz[0] = xz.x; cz[1] = xz.y;
+        sfa = sb[kKsf + ka * 4 + t];
+        sfz = sb[kKsf + kz * 4 + t];
+      }
+#pragma unroll
+      for (int i = 0; i < kKW; ++i) {
+        // code word i: bytes 4i .. 4i+3 of the lane's range = k-steps 2i, 2i+1;
+        // its scale block is the lane's first (bytes 0-7) or second (8-15)
+        const uint32_t sa = e4m3_to_f16x2_dup(sfa >> (8 * (i / 2)));
+        const uint32_t sz = e4m3_to_f16x2_dup(sfz >> (8 * (i / 2)));
+        uint32_t ha[4], hz[4];
+        e2m1x8_to_f16x2(ca[i], ha);
+        e2m1x8_to_f16x2(cz[i], hz);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t a[4];
+          a[0] = hmul2_u32(ha[2 * h], sa);
+          a[1] = hmul2_u32(hz[2 * h], sz);
+          a[2] = hmul2_u32(ha[2 * h + 1], sa);
+          a[3] = hmul2_u32(hz[2 * h + 1], sz);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            mma16816(sacc[mt][nt], a, qb[nt][2 * i + h][0], qb[nt][2 * i + h][1]);
+        }
+      }
+    }
+
+    // ---- causal mask and online softmax; lane holds rows 8 nt + 2t + e of
+    // keys kb + 16 mt + g + 8 h (accumulator element 2h + e)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int r = 8 * nt + 2 * t + e;
+        const int lim = r < R ? min(k1 - 1, delta + r / G) : -1;  // last visible key
+        float mx = -INFINITY;
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int key = kb + 16 * mt + g + 8 * h;
+            const float x = key <= lim ? sacc[mt][nt][2 * h + e] * ssc : -INFINITY;
+            sacc[mt][nt][2 * h + e] = x;
+            mx = fmaxf(mx, x);
+          }
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
+        if (mx > mrun[nt][e] + 8.0f) {
+          const float alpha = ex2_approx(mrun[nt][e] - mx);  // 0 while mrun is -inf
+          lrun[nt][e] *= alpha;
+#pragma unroll
+          for (int i = 0; i < D / 16; ++i) {
+            o[i][nt][e] *= alpha;
+            o[i][nt][2 + e] *= alpha;
+          }
+          mrun[nt][e] = mx;
+        }
+        float psum = 0.0f;
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float x = sacc[mt][nt][2 * h + e];
+            const float pv = x == -INFINITY ? 0.0f : ex2_approx(x - mrun[nt][e]);
+            sacc[mt][nt][2 * h + e] = pv;
+            psum += pv;
+          }
+        lrun[nt][e] += psum;
+      }
+    }
+
+    // ---- O^T += V^T P^T, k-steps of keys 0-15 and 16-31
+    const uint8_t* vb = sb + kV;
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      uint32_t pb[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        pb[nt][0] = movmatrix_t(f16x2_of(sacc[kk][nt][0], sacc[kk][nt][1]));
+        pb[nt][1] = movmatrix_t(f16x2_of(sacc[kk][nt][2], sacc[kk][nt][3]));
+      }
+      const int kA = 16 * kk + 2 * t;  // keys kA, kA+1 (k = 2t, 2t+1) and kA+8, kA+9
+      uint32_t va[kVW], vb1[kVW], vc[kVW], vd[kVW];
+      uint32_t sab, scd;
+      if constexpr (D == 128) {
+        const uint2 x0 = *reinterpret_cast<const uint2*>(vb + kA * kVR + 8 * g);
+        const uint2 x1 = *reinterpret_cast<const uint2*>(vb + (kA + 1) * kVR + 8 * g);
+        const uint2 x2 = *reinterpret_cast<const uint2*>(vb + (kA + 8) * kVR + 8 * g);
+        const uint2 x3 = *reinterpret_cast<const uint2*>(vb + (kA + 9) * kVR + 8 * g);
+        va[0] = x0.x; va[1] = x0.y; vb1[0] = x1.x; vb1[1] = x1.y;
+        vc[0] = x2.x; vc[1] = x2.y; vd[0] = x3.x; vd[1] = x3.y;
+        sab = vb[kA * kVR + 64 + g] | (vb[(kA + 1) * kVR + 64 + g] << 8);
+        scd = vb[(kA + 8) * kVR + 64 + g] | (vb[(kA + 9) * kVR + 64 + g] << 8);
+      } else {
+        va[0] = *reinterpret_cast<const uint32_t*>(vb + kA * kVR + 4 * g);
+        vb1[0] = *reinterpret_cast<const uint32_t*>(vb + (kA + 1) * kVR + 4 * g);
+        vc[0] = *reinterpret_cast<const uint32_t*>(vb + (kA + 8) * kVR + 4 * g);
+        vd[0] = *reinterpret_cast<const uint32_t*>(vb + (kA + 9) * kVR + 4 * g);
+        sab = vb[kA * kVR + 32 + g / 2] | (vb[(kA + 1) * kVR + 32 + g / 2] << 8);
+        scd = vb[(kA + 8) * kVR + 32 + g / 2] | (vb[(kA + 9) * kVR + 32 + g / 2] << 8);
+      }
+      const uint32_t s01 = e4m3x2_to_f16x2(sab), s89 = e4m3x2_to_f16x2(scd);
+#pragma unroll
+      for (int j = 0; j < kVW; ++j) {
+        // byte i of a word: low nibbles of the two keys (head dimension
+        // 2(g D/16 + 4j + i)), then their high nibbles (the next dimension)
+        const uint32_t lo01 = (va[j] & 0x0F0F0F0Fu) | ((vb1[j] << 4) & 0xF0F0F0F0u);
+        const uint32_t hi01 = ((va[j] >> 4) & 0x0F0F0F0Fu) | (vb1[j] & 0xF0F0F0F0u);
+        const uint32_t lo89 = (vc[j] & 0x0F0F0F0Fu) | ((vd[j] << 4) & 0xF0F0F0F0u);
+        const uint32_t hi89 = ((vc[j] >> 4) & 0x0F0F0F0Fu) | (vd[j] & 0xF0F0F0F0u);
+        uint32_t l01[4], h01[4], l89[4], h89[4];
+        e2m1x8_to_f16x2(lo01, l01);
+        e2m1x8_to_f16x2(hi01, h01);
+        e2m1x8_to_f16x2(lo89, l89);
+        e2m1x8_to_f16x2(hi89, h89);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t a[4];
+          a[0] = hmul2_u32(l01[i], s01);
+          a[1] = hmul2_u32(h01[i], s01);
+          a[2] = hmul2_u32(l89[i], s89);
+          a[3] = hmul2_u32(h89[i], s89);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma16816(o[4 * j + i][nt], a, pb[nt][0], pb[nt][1]);
+        }
+      }
+    }
+    st = st == kTStages - 1 ? 0 : st + 1;
+  }
+
+  cp_async_wait<0>();  // (the copies past the chunk are empty groups; none is left in flight)
+
+  // ---- results: lane holds head dimensions g D/8 .. g D/8 + D/8 - 1 of rows
+  // 8 nt + 2t + e (m-tile i gives dimensions g D/8 + 2i and the one after)
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float lsum = lrun[nt][e];
+      lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 4);
+      lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 8);
+      lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 16);
+      const int r = 8 * nt + 2 * t + e;
+      if (r >= R) continue;
+      const int d0 = g * (D / 8);
+      if (slot < 0) {
+        const int64_t orow =
+            static_cast<int64_t>(qo_start + r / G) * p.num_qo_heads + hk * G + r % G;
+        const float inv = vs / lsum;
+        uint32_t packed[D / 16];
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) {
+          const __nv_bfloat162 v2 = __floats2bfloat162_rn(o[i][nt][e] * inv, o[i][nt][2 + e] * inv);
+          packed[i] = *reinterpret_cast<const uint32_t*>(&v2);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D + d0);
+#pragma unroll
+        for (int i = 0; i < D / 64; ++i)
+          dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+        if (p.lse && g == 0) p.lse[orow] = (mrun[nt][e] + log2f(lsum)) * 0.6931471805599453f;
+      } else {
+        float* dst = p.part + (static_cast<int64_t>(slot) * p.rows + r) * (D + 2);
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i)
+          *reinterpret_cast<float2*>(dst + d0 + 2 * i) = make_float2(o[i][nt][e], o[i][nt][2 + e]);
+        if (g == 0) {
+          dst[D] = mrun[nt][e];
+          dst[D + 1] = lsum;
+        }
+      }
+    }
+  }
+}
+
 // One warp per (merge item, row): combines the item's partial slots
 //   M = max m_i,  L = sum l_i 2^(m_i - M),  O = sum O_i 2^(m_i - M) / L,
 // scaled by v_scale, and lse = (M + log2 L) ln 2.
@@ -474,6 +851,21 @@ fi_status launch_decode_impl(const DecodeParams& p, cudaStream_t stream) {
   return launch_pdl(nvfp4_decode_merge_kernel<D>, dim3(mgrid), dim3(128), 0, stream, p);
 }
 
+template <int D, int NT>
+fi_status launch_decode_t_impl(const DecodeParams& p, cudaStream_t stream) {
+  const int smem = decode_t_smem_bytes<D>();
+  auto kern = nvfp4_decode_t_kernel<D, NT>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+      cudaSuccess)
+    return FI_ERR_CUDA;
+  const unsigned grid = static_cast<unsigned>((p.num_units + kTWarps - 1) / kTWarps);
+  fi_status st = launch_pdl(kern, dim3(grid), dim3(32 * kTWarps), smem, stream, p);
+  if (st != FI_OK || p.num_merges == 0) return st;
+  const int64_t warps = static_cast<int64_t>(p.num_merges) * p.rows;
+  const unsigned mgrid = static_cast<unsigned>((warps + 3) / 4);
+  return launch_pdl(nvfp4_decode_merge_kernel<D>, dim3(mgrid), dim3(128), 0, stream, p);
+}
+
 }  // namespace
 
 fi_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
@@ -509,8 +901,10 @@ fi_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.sm_scale = P.sm_scale;
   p.status = a.status;
   const int D = P.head_dim;
+  if (P.dec_rows <= 8)
+    return D == 128 ? launch_decode_t_impl<128, 1>(p, stream) : launch_decode_t_impl<64, 1>(p, stream);
   if (P.dec_rows <= 16)
-    return D == 128 ? launch_decode_impl<128, 1>(p, stream) : launch_decode_impl<64, 1>(p, stream);
+    return D == 128 ? launch_decode_t_impl<128, 2>(p, stream) : launch_decode_t_impl<64, 2>(p, stream);
   return D == 128 ? launch_decode_impl<128, 2>(p, stream) : launch_decode_impl<64, 2>(p, stream);
 }
 

@@ -106,6 +106,15 @@ def spec(name: str) -> Spec:
     if name == "decode_d64":
         return Spec("decode_d64", 13000, num_kv_heads=4, head_dim=64, page_size=32,
                     num_qo_heads=8, seq_lens=[257, 1500, 90], qo_lens=[1, 2, 1], attn="decode")
+    # Decode with 9..16 rows per KV head (GQA 8 with two-token steps; GQA 6
+    # at head_dim 64 with a 1-key sequence and a sequence split into chunks).
+    if name == "decode_g8":
+        return Spec("decode_g8", 13100, num_kv_heads=2, head_dim=128, page_size=16,
+                    num_qo_heads=16, seq_lens=[33, 700, 3000, 64], qo_lens=[1, 2, 2, 1],
+                    attn="decode")
+    if name == "decode_g6_d64":
+        return Spec("decode_g6_d64", 13200, num_kv_heads=2, head_dim=64, page_size=64,
+                    num_qo_heads=12, seq_lens=[1, 2049, 400], qo_lens=[1, 2, 2], attn="decode")
     if name == "uniform_small":
         return Spec("uniform_small", 7000, num_kv_heads=2, head_dim=128, page_size=16,
                     num_qo_heads=8, seq_lens=[384] * 6)
