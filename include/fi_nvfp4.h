@@ -203,12 +203,12 @@ fi_status fi_prefill_run(const fi_plan* plan, const void* q_dev, const fi_nvfp4_
  * comes from one reduction over the lengths).  Same arguments and causal rule
  * as fi_prefill_plan; every sequence has qo_len <= 8 and
  * (num_qo_heads / num_kv_heads) * qo_len <= 32, else FI_ERR_UNSUPPORTED.  The
- * keys of a sequence are split into chunks (a power of two, 256 .. 16384,
- * chosen from the batch); a sequence with several chunks is merged by a second
- * kernel.  The plan owns a device buffer for the chunks' partial results,
- * grown (after synchronizing `stream`) when a plan needs more; otherwise it
- * behaves as fi_prefill_plan.  fi_plan_get_info reports the units (sequence,
- * kv head, chunk) in num_units. */
+ * keys of all (sequence, KV head) pairs are split evenly over the warps the
+ * decode kernel keeps resident (fi_decode_plan_host gives the rule); a pair
+ * split across warps is merged by a second kernel.  The plan owns a device
+ * buffer for the pieces' partial results, grown (after synchronizing
+ * `stream`) when a plan needs more; otherwise it behaves as fi_prefill_plan.
+ * fi_plan_get_info reports the pieces in num_units. */
 fi_status fi_decode_plan(fi_plan* plan, const int32_t* qo_indptr_host,
                          const int32_t* kv_indptr_host, int32_t batch,
                          const int32_t* page_table_dev, int32_t page_table_stride,
@@ -267,20 +267,30 @@ fi_status fi_prefill_plan_host(const int32_t* qo_indptr_host, const int32_t* kv_
                                int32_t* work_out, int64_t work_capacity);
 
 /* Host-only decode planning, for inspection and tests (the decision
- * fi_decode_plan makes for the same arguments on a GPU with `num_sms` SMs):
- * fills `info`, *chunk_out (keys per unit: the smallest power of two from
- * 256 to 16384 that keeps the units at most 32 per SM) and *num_merges_out,
- * and, when the pointers are non-NULL, up to `unit_capacity` units as 4 int32
- * each (sequence, KV head, chunk index, partial slot or -1 when the sequence
- * has one chunk) in launch order, and up to `merge_capacity` merge items as 4
- * int32 each (sequence, KV head, first partial slot, number of chunks).
- * Makes no CUDA call.  Errors as fi_decode_plan. */
+ * fi_decode_plan makes for the same arguments on a GPU with `num_sms` SMs).
+ * The keys of every (sequence, KV head) pair with queries are taken in steps
+ * of 32, laid end to end in (sequence, head) order and cut into W runs of
+ * equal length (to one step), one per warp of the decode kernel: W is the
+ * number of warps the kernel keeps resident on num_sms SMs (16 per SM up to 8
+ * rows G * max qo_len, 12 up to 16, 8 above), or fewer so that a warp takes at
+ * least 8 steps.  A run becomes one piece per pair it touches; a pair cut into
+ * several pieces writes one partial result per piece and is merged.
+ *   Fills `info` (num_units = pieces, num_ctas = ceil(W / 4)), *num_warps_out
+ * = W and *num_merges_out, and, when the pointers are non-NULL: up to
+ * `unit_capacity` pieces as 4 int32 each (sequence * num_kv_heads + KV head,
+ * first key, end key (exclusive), partial slot or -1 for a pair in one piece)
+ * in (sequence, head, key) order; up to `merge_capacity` merge items as 4
+ * int32 each (sequence, KV head, first partial slot, pieces); up to
+ * `warp_off_capacity` of the W + 1 offsets, warp w running pieces
+ * warp_off[w] .. warp_off[w + 1] - 1.  Makes no CUDA call.  Errors as
+ * fi_decode_plan. */
 fi_status fi_decode_plan_host(const int32_t* qo_indptr_host, const int32_t* kv_indptr_host,
                               int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
                               int32_t head_dim, int32_t page_size, int32_t num_sms,
-                              fi_plan_info* info, int32_t* chunk_out, int64_t* num_merges_out,
+                              fi_plan_info* info, int32_t* num_warps_out, int64_t* num_merges_out,
                               int32_t* units_out, int64_t unit_capacity, int32_t* merges_out,
-                              int64_t merge_capacity);
+                              int64_t merge_capacity, int32_t* warp_off_out,
+                              int64_t warp_off_capacity);
 
 /* Plans and runs the causal prefill in one call without allocating memory
  * (no cudaMalloc, no host heap), for callers that cannot allocate while they

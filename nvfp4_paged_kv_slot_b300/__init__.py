@@ -97,7 +97,7 @@ _sigs = {
                              C.POINTER(fi_plan_options), C.POINTER(fi_plan_info), _vp, _i64],
     "fi_decode_plan_host": [_vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                             C.POINTER(fi_plan_info), C.POINTER(_i32), C.POINTER(_i64), _vp, _i64,
-                            _vp, _i64],
+                            _vp, _i64, _vp, _i64],
     "fi_device_status": [_vp, _vp, C.POINTER(_i32), _i32],
     "fi_prefill_noalloc": [_vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _f32, _vp,
                            C.POINTER(fi_nvfp4_cache), _vp, _vp, _vp, _vp],
@@ -369,22 +369,24 @@ def fi_prefill_plan_host(qo_indptr, kv_indptr, num_qo_heads, num_kv_heads, head_
 
 def fi_decode_plan_host(qo_indptr, kv_indptr, num_qo_heads, num_kv_heads, head_dim, page_size,
                         num_sms=148):
-    """Host-only decode planning (no CUDA): returns (info dict, chunk, units [n][4] int32,
-    merges [m][4] int32)."""
+    """Host-only decode planning (no CUDA): returns (info dict, number of warps W,
+    pieces [n][4] int32, merges [m][4] int32, warp offsets [W + 1] int32)."""
     qo = _host_i32(qo_indptr)
     kv = _host_i32(kv_indptr)
     info = fi_plan_info()
-    chunk = C.c_int32()
+    warps = C.c_int32()
     merges = C.c_int64()
     args = (qo.ctypes.data, kv.ctypes.data, qo.size - 1, num_qo_heads, num_kv_heads, head_dim,
-            page_size, num_sms, C.byref(info), C.byref(chunk), C.byref(merges))
-    _check(lib.fi_decode_plan_host(*args, None, 0, None, 0), "fi_decode_plan_host")
+            page_size, num_sms, C.byref(info), C.byref(warps), C.byref(merges))
+    _check(lib.fi_decode_plan_host(*args, None, 0, None, 0, None, 0), "fi_decode_plan_host")
     units = np.zeros((info.num_units, 4), np.int32)
     mlist = np.zeros((merges.value, 4), np.int32)
+    off = np.zeros(warps.value + 1, np.int32)
     _check(lib.fi_decode_plan_host(*args, units.ctypes.data if units.size else None,
                                    info.num_units, mlist.ctypes.data if mlist.size else None,
-                                   merges.value), "fi_decode_plan_host")
-    return info.as_dict(), chunk.value, units, mlist
+                                   merges.value, off.ctypes.data, off.size),
+           "fi_decode_plan_host")
+    return info.as_dict(), warps.value, units, mlist, off
 
 
 def fi_device_status(ctx, stream=None, reset=True) -> int:

@@ -279,12 +279,12 @@ fi_status upload_plan(fi_plan* plan, const int32_t* qo_indptr_host,
   if (!plan->host.work.empty())
     std::memcpy(h + plan->off_work, plan->host.work.data(),
                 plan->host.work.size() * sizeof(int32_t));
-  if (!plan->host.slot_units.empty()) {
+  if (!plan->host.slot_units.empty())
     std::memcpy(h + plan->off_slot_units, plan->host.slot_units.data(),
                 plan->host.slot_units.size() * sizeof(int32_t));
+  if (!plan->host.slot_begin.empty())
     std::memcpy(h + plan->off_slot_begin, plan->host.slot_begin.data(),
                 plan->host.slot_begin.size() * sizeof(int32_t));
-  }
   if (cudaMemcpyAsync(plan->dev, h, words * sizeof(int32_t), cudaMemcpyHostToDevice, s) !=
       cudaSuccess)
     return FI_ERR_CUDA;
@@ -342,10 +342,11 @@ fi_status fi_decode_plan(fi_plan* plan, const int32_t* qo_indptr_host,
     return FI_ERR_INVALID_ARGUMENT;
   plan->page_table = page_table_dev;
   plan->page_table_stride = page_table_stride;
-  // the units and merges travel in the work-list and slot-unit regions
+  // the pieces, merges and warp offsets travel in the work-list, slot-unit
+  // and slot-begin regions
   P.work = P.dec_units;
   P.slot_units = P.dec_merges;
-  P.slot_begin.clear();
+  P.slot_begin = P.dec_warp_off;
   const size_t need = static_cast<size_t>(P.dec_parts) * P.dec_rows * (head_dim + 2);
   if (need > plan->part_floats) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -378,6 +379,7 @@ fi_status fi_decode_run(const fi_plan* plan, const void* q_dev, const fi_nvfp4_c
   a.kv_indptr_dev = plan->dev + plan->off_kv;
   a.units_dev = plan->dev + plan->off_work;
   a.merges_dev = plan->dev + plan->off_slot_units;
+  a.warp_off_dev = plan->dev + plan->off_slot_begin;
   a.part = plan->part;
   a.page_table = plan->page_table;
   a.page_table_stride = plan->page_table_stride;
@@ -475,6 +477,6 @@ const char* fi_status_string(fi_status status) {
   }
 }
 
-int32_t fi_version(void) { return 100; }
+int32_t fi_version(void) { return 200; }
 
 }  // extern "C"

@@ -27,7 +27,7 @@ namespace fi {
 
 namespace {
 
-constexpr int kDecWarps = 4;   // warps (units) per CTA
+constexpr int kDecWarps = 4;   // warps per CTA
 constexpr int kDecStages = 2;  // raw rows in flight per warp: this step's and the next
 
 struct DecodeParams {
@@ -44,11 +44,12 @@ struct DecodeParams {
   const int32_t* kv_indptr;
   const int32_t* page_table;
   int64_t pt_stride;
-  const int4* units;   // (sequence, kv head, chunk, partial slot or -1)
+  const int4* units;   // pieces (sequence * H_kv + kv head, first key, end key, slot or -1)
   const int4* merges;  // (sequence, kv head, first partial slot, chunks)
   float* part;         // partial slots: [slot][rows][D + 2] = O, then m, l
-  int32_t num_units, num_merges, num_qo_heads, num_kv_heads, group, page_size, num_pages;
-  int32_t chunk, rows;  // keys per chunk; partial rows per slot (G * max qo_len)
+  const int32_t* warp_off;  // warp w runs pieces warp_off[w] .. warp_off[w + 1] - 1
+  int32_t num_warps, num_merges, num_qo_heads, num_kv_heads, group, page_size, num_pages;
+  int32_t rows;  // partial rows per slot (G * max qo_len)
   float sm_scale;
   int32_t* status;
 };
@@ -104,311 +105,315 @@ __global__ void __launch_bounds__(32 * kDecWarps, MT == 1 ? 3 : 2)
   grid_dep_launch();
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int u = blockIdx.x * kDecWarps + warp;
-  if (u >= p.num_units) return;  // no block-wide barrier below
-  const int4 w = __ldg(p.units + u);
-  const int b = w.x, hk = w.y, c = w.z, slot = w.w;
-  const int qo_start = __ldg(p.qo_indptr + b);
-  const int qo_len = __ldg(p.qo_indptr + b + 1) - qo_start;
-  const int kv_len = __ldg(p.kv_indptr + b + 1) - __ldg(p.kv_indptr + b);
-  const int G = p.group;
-  const int R = G * qo_len;  // <= 16 MT (the planner guarantees it)
-  const int delta = kv_len - qo_len;
-  const int k0 = c * p.chunk;
-  const int k1 = min(k0 + p.chunk, kv_len);
-  const float ks = __ldg(p.k_scale), vs = __ldg(p.v_scale);
-  uint8_t* sv = dsm + warp * 32 * kS;  // this warp's 32 staged V rows
-  const uint32_t sv_addr = smem_u32(sv);
-  // this warp's raw ring: stage st, key (lane) l at (st * 32 + l) * kLR
-  uint8_t* raw = dsm + kDecWarps * 32 * kS + warp * kDecStages * 32 * kLR;
-  const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.pt_stride;
-  auto q_ptr = [&](int r) {  // row r = token r / G, head hk * G + r % G
-    return p.q + (static_cast<int64_t>(qo_start + r / G) * p.num_qo_heads + hk * G + r % G) * D;
-  };
+  const int wid = blockIdx.x * kDecWarps + warp;
+  if (wid >= p.num_warps) return;  // no block-wide barrier below
+  const int u_end = __ldg(p.warp_off + wid + 1);
+  for (int u = __ldg(p.warp_off + wid); u < u_end; ++u) {
+    __syncwarp();  // every lane is done with the previous piece's ring
+    const int4 w = __ldg(p.units + u);
+    const int b = w.x / p.num_kv_heads, hk = w.x - b * p.num_kv_heads, slot = w.w;
+    const int qo_start = __ldg(p.qo_indptr + b);
+    const int qo_len = __ldg(p.qo_indptr + b + 1) - qo_start;
+    const int kv_len = __ldg(p.kv_indptr + b + 1) - __ldg(p.kv_indptr + b);
+    const int G = p.group;
+    const int R = G * qo_len;  // <= 16 MT (the planner guarantees it)
+    const int delta = kv_len - qo_len;
+    const int k0 = w.y;  // the piece's keys: k0 .. k1 - 1
+    const int k1 = w.z;
+    const float ks = __ldg(p.k_scale), vs = __ldg(p.v_scale);
+    uint8_t* sv = dsm + warp * 32 * kS;  // this warp's 32 staged V rows
+    const uint32_t sv_addr = smem_u32(sv);
+    // this warp's raw ring: stage st, key (lane) l at (st * 32 + l) * kLR
+    uint8_t* raw = dsm + kDecWarps * 32 * kS + warp * kDecStages * 32 * kLR;
+    const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.pt_stride;
+    auto q_ptr = [&](int r) {  // row r = token r / G, head hk * G + r % G
+      return p.q + (static_cast<int64_t>(qo_start + r / G) * p.num_qo_heads + hk * G + r % G) * D;
+    };
 
-  // Q as fp16 A fragments: Q * sm_scale * k_scale * log2 e * 2^-e with e
-  // chosen so that every |value| < 2^14 (a power of two: exact); the logits
-  // are multiplied back by 2^e.
-  const float qs = p.sm_scale * ks * 1.4426950408889634f;
-  float qmax = 0.0f;
-  for (int i = lane; i < R * (D / 8); i += 32) {
-    float x[8];
-    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(q_ptr(i / (D / 8)) + (i % (D / 8)) * 8)), x);
+    // Q as fp16 A fragments: Q * sm_scale * k_scale * log2 e * 2^-e with e
+    // chosen so that every |value| < 2^14 (a power of two: exact); the logits
+    // are multiplied back by 2^e.
+    const float qs = p.sm_scale * ks * 1.4426950408889634f;
+    float qmax = 0.0f;
+    for (int i = lane; i < R * (D / 8); i += 32) {
+      float x[8];
+      bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(q_ptr(i / (D / 8)) + (i % (D / 8)) * 8)), x);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) qmax = fmaxf(qmax, fabsf(x[e]));
-  }
-  qmax = warp_max(qmax) * qs;
-  const int qe = qmax > 0.0f ? ilogbf(qmax) - 13 : 0;
-  const float qsc = ldexpf(qs, -qe);
-  const float ssc = ldexpf(1.0f, qe);
-  uint32_t qa[MT][D / 16][4];
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
-    const int r0 = 16 * mt + lane / 4, r1 = r0 + 8;
-#pragma unroll
-    for (int s = 0; s < D / 16; ++s) {
-      const int d0 = 16 * s + 2 * (lane % 4);
-      float v[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) v[k] = 0.0f;
-      if (r0 < R) {
-        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(q_ptr(r0) + d0);
-        const __nv_bfloat162 bb = *reinterpret_cast<const __nv_bfloat162*>(q_ptr(r0) + d0 + 8);
-        v[0] = __low2float(a) * qsc;
-        v[1] = __high2float(a) * qsc;
-        v[4] = __low2float(bb) * qsc;
-        v[5] = __high2float(bb) * qsc;
-      }
-      if (r1 < R) {
-        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(q_ptr(r1) + d0);
-        const __nv_bfloat162 bb = *reinterpret_cast<const __nv_bfloat162*>(q_ptr(r1) + d0 + 8);
-        v[2] = __low2float(a) * qsc;
-        v[3] = __high2float(a) * qsc;
-        v[6] = __low2float(bb) * qsc;
-        v[7] = __high2float(bb) * qsc;
-      }
-      qa[mt][s][0] = f16x2_of(v[0], v[1]);
-      qa[mt][s][1] = f16x2_of(v[2], v[3]);
-      qa[mt][s][2] = f16x2_of(v[4], v[5]);
-      qa[mt][s][3] = f16x2_of(v[6], v[7]);
+      for (int e = 0; e < 8; ++e) qmax = fmaxf(qmax, fabsf(x[e]));
     }
-  }
-
-  float o[MT][D / 8][4];
-  float mrow[MT][2], lrow[MT][2];
+    qmax = warp_max(qmax) * qs;
+    const int qe = qmax > 0.0f ? ilogbf(qmax) - 13 : 0;
+    const float qsc = ldexpf(qs, -qe);
+    const float ssc = ldexpf(1.0f, qe);
+    uint32_t qa[MT][D / 16][4];
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
+    for (int mt = 0; mt < MT; ++mt) {
+      const int r0 = 16 * mt + lane / 4, r1 = r0 + 8;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      mrow[mt][h] = -INFINITY;
-      lrow[mt][h] = 0.0f;
-    }
+      for (int s = 0; s < D / 16; ++s) {
+        const int d0 = 16 * s + 2 * (lane % 4);
+        float v[8];
 #pragma unroll
-    for (int nd = 0; nd < D / 8; ++nd)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o[mt][nd][e] = 0.0f;
-  }
-
-  // Raw rows of key kbs + lane into ring stage st (one commit group per call,
-  // empty past the chunk).  The page id comes from the previous call, so the
-  // page-table read is one step ahead of the copies that need it.
-  auto page_of = [&](int key) { return key < k1 ? __ldg(pt + key / p.page_size) : 0; };
-  int page_next = page_of(k0 + lane);
-  auto issue = [&](int kbs, int st) {
-    const int key = kbs + lane;
-    int page = page_next;
-    page_next = page_of(key + 32);
-    if (key < k1) {
-      if (page < 0 || page >= p.num_pages) {
-        atomicOr(p.status, FI_DEV_PAGE_OOB);
-        page = 0;
-      }
-      const int64_t row =
-          (static_cast<int64_t>(page) * p.num_kv_heads + hk) * p.page_size + key % p.page_size;
-      uint8_t* dst = raw + (st * 32 + lane) * kLR;
-      const uint8_t* kg = p.k_data + row * (D / 2);
-      const uint8_t* vg = p.v_data + row * (D / 2);
-#pragma unroll
-      for (int i = 0; i < D / 32; ++i) {
-        cp_async16(dst + 16 * i, kg + 16 * i);
-        cp_async16(dst + D / 2 + 16 * i, vg + 16 * i);
-      }
-      if constexpr (D == 128) {
-        cp_async8(dst + D, p.k_sf + row * (D / 16));
-        cp_async8(dst + D + D / 16, p.v_sf + row * (D / 16));
-      } else {
-        cp_async4(dst + D, p.k_sf + row * (D / 16));
-        cp_async4(dst + D + D / 16, p.v_sf + row * (D / 16));
-      }
-    }
-    cp_async_commit();
-  };
-  issue(k0, 0);
-  issue(k0 + 32, 1);
-
-  int st = 0;
-  for (int kb = k0; kb < k1; kb += 32, st ^= 1) {
-    // ---- stage this lane's key: its V row as exact fp16 (zeros past k1)
-    cp_async_wait<1>();  // this lane's raw rows of this step have landed
-    __syncwarp();        // ... and every lane's; the previous batch's V rows have been read
-    {
-      uint4* dv = reinterpret_cast<uint4*>(sv + lane * kS);
-      const int key = kb + lane;
-      if (key < k1) {
-        const uint8_t* src = raw + (st * 32 + lane) * kLR;
-        uint4 vc4[D / 32];
-        uint32_t vsf4[D / 64];
-#pragma unroll
-        for (int i = 0; i < D / 32; ++i) vc4[i] = reinterpret_cast<const uint4*>(src + D / 2)[i];
-#pragma unroll
-        for (int i = 0; i < D / 64; ++i)
-          vsf4[i] = reinterpret_cast<const uint32_t*>(src + D + D / 16)[i];
-        const uint32_t* vc = reinterpret_cast<const uint32_t*>(vc4);
-#pragma unroll
-        for (int blk = 0; blk < D / 16; ++blk) {
-          const uint32_t s8v = (vsf4[blk / 4] >> (8 * (blk % 4))) & 0xFFu;
-          dv[2 * blk] = dequant8_f16(vc[2 * blk], s8v);
-          dv[2 * blk + 1] = dequant8_f16(vc[2 * blk + 1], s8v);
+        for (int k = 0; k < 8; ++k) v[k] = 0.0f;
+        if (r0 < R) {
+          const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(q_ptr(r0) + d0);
+          const __nv_bfloat162 bb = *reinterpret_cast<const __nv_bfloat162*>(q_ptr(r0) + d0 + 8);
+          v[0] = __low2float(a) * qsc;
+          v[1] = __high2float(a) * qsc;
+          v[4] = __low2float(bb) * qsc;
+          v[5] = __high2float(bb) * qsc;
         }
-      } else {
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i) dv[i] = make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
-
-    // ---- S = Q K^T for the 32 keys (4 n-tiles of 8 keys, D/16 k-steps).  The
-    // B fragment of n-tile j, k-step t (dims 16t .. 16t+15 = scale block t)
-    // holds, in lane l, key 8j + l/4 at dims 16t + 2(l%4) + {0, 1} and
-    // {8, 9} more: byte l%4 of code words 4(t/2) + 2(t%2) and the word after
-    // it of that key's raw row, times the block's scale.  Keys past k1 read
-    // stale ring bytes; their logits are replaced by -inf below.
-    float sacc[MT][4][4];
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[mt][j][e] = 0.0f;
-    const uint32_t bsel = static_cast<uint32_t>(lane % 4) | ((4u + static_cast<uint32_t>(lane % 4)) << 4);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint8_t* kr = raw + (st * 32 + 8 * j + lane / 4) * kLR;
-      uint32_t kw[D / 8];
-#pragma unroll
-      for (int i = 0; i < D / 32; ++i) {
-        const uint4 w4 = reinterpret_cast<const uint4*>(kr)[i];
-        kw[4 * i] = w4.x;
-        kw[4 * i + 1] = w4.y;
-        kw[4 * i + 2] = w4.z;
-        kw[4 * i + 3] = w4.w;
-      }
-      uint32_t ksf[D / 64];
-#pragma unroll
-      for (int i = 0; i < D / 64; ++i) ksf[i] = reinterpret_cast<const uint32_t*>(kr + D)[i];
-#pragma unroll
-      for (int s2 = 0; s2 < D / 32; ++s2) {
-        // bytes for k-steps 2 s2 (b0, b1) and 2 s2 + 1 (b0, b1), in that order
-        const uint32_t lo = __byte_perm(kw[4 * s2], kw[4 * s2 + 1], bsel);
-        const uint32_t hi = __byte_perm(kw[4 * s2 + 2], kw[4 * s2 + 3], bsel);
-        uint32_t h[4];
-        e2m1x8_to_f16x2(__byte_perm(lo, hi, 0x5410), h);
-        const uint32_t sa = e4m3_to_f16x2_dup(ksf[s2 / 2] >> (16 * (s2 % 2)));
-        const uint32_t sb = e4m3_to_f16x2_dup(ksf[s2 / 2] >> (16 * (s2 % 2) + 8));
-        const uint32_t b0a = hmul2_u32(h[0], sa), b1a = hmul2_u32(h[1], sa);
-        const uint32_t b0b = hmul2_u32(h[2], sb), b1b = hmul2_u32(h[3], sb);
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          mma16816(sacc[mt][j], qa[mt][2 * s2], b0a, b1a);
-          mma16816(sacc[mt][j], qa[mt][2 * s2 + 1], b0b, b1b);
+        if (r1 < R) {
+          const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(q_ptr(r1) + d0);
+          const __nv_bfloat162 bb = *reinterpret_cast<const __nv_bfloat162*>(q_ptr(r1) + d0 + 8);
+          v[2] = __low2float(a) * qsc;
+          v[3] = __high2float(a) * qsc;
+          v[6] = __low2float(bb) * qsc;
+          v[7] = __high2float(bb) * qsc;
         }
+        qa[mt][s][0] = f16x2_of(v[0], v[1]);
+        qa[mt][s][1] = f16x2_of(v[2], v[3]);
+        qa[mt][s][2] = f16x2_of(v[4], v[5]);
+        qa[mt][s][3] = f16x2_of(v[6], v[7]);
       }
     }
-    __syncwarp();  // every lane has read this stage's raw rows; V rows are staged
-    // the raw stage just read takes the rows of the step after next
-    issue(kb + 64, st);
 
-    // ---- causal mask and online softmax; rows r0 = 16 mt + lane/4 (h = 0)
-    // and r0 + 8 (h = 1), keys kb + 8j + 2(lane%4) + e
+    float o[MT][D / 8][4];
+    float mrow[MT][2], lrow[MT][2];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int r = 16 * mt + lane / 4 + 8 * h;
-        const int lim = r < R ? min(k1 - 1, delta + r / G) : -1;  // last visible key
-        float mx = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int key = kb + 8 * j + 2 * (lane % 4) + e;
-            const float x = key <= lim ? sacc[mt][j][2 * h + e] * ssc : -INFINITY;
-            sacc[mt][j][2 * h + e] = x;
-            mx = fmaxf(mx, x);
-          }
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
-        const float m_new = fmaxf(mrow[mt][h], mx);
-        const float alpha = m_new == -INFINITY ? 1.0f : ex2_approx(mrow[mt][h] - m_new);
-        float psum = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const float x = sacc[mt][j][2 * h + e];
-            const float pv = x == -INFINITY ? 0.0f : ex2_approx(x - m_new);
-            sacc[mt][j][2 * h + e] = pv;
-            psum += pv;
-          }
-        lrow[mt][h] = lrow[mt][h] * alpha + psum;
-        mrow[mt][h] = m_new;
-#pragma unroll
-        for (int nd = 0; nd < D / 8; ++nd) {
-          o[mt][nd][2 * h] *= alpha;
-          o[mt][nd][2 * h + 1] *= alpha;
-        }
+        mrow[mt][h] = -INFINITY;
+        lrow[mt][h] = 0.0f;
       }
+#pragma unroll
+      for (int nd = 0; nd < D / 8; ++nd)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[mt][nd][e] = 0.0f;
     }
 
-    // ---- O += P V (k-steps of 16 keys, n-tiles of 8 columns)
+    // Raw rows of key kbs + lane into ring stage st (one commit group per call,
+    // empty past the chunk).  The page id comes from the previous call, so the
+    // page-table read is one step ahead of the copies that need it.
+    auto page_of = [&](int key) { return key < k1 ? __ldg(pt + key / p.page_size) : 0; };
+    int page_next = page_of(k0 + lane);
+    auto issue = [&](int kbs, int st) {
+      const int key = kbs + lane;
+      int page = page_next;
+      page_next = page_of(key + 32);
+      if (key < k1) {
+        if (page < 0 || page >= p.num_pages) {
+          atomicOr(p.status, FI_DEV_PAGE_OOB);
+          page = 0;
+        }
+        const int64_t row =
+            (static_cast<int64_t>(page) * p.num_kv_heads + hk) * p.page_size + key % p.page_size;
+        uint8_t* dst = raw + (st * 32 + lane) * kLR;
+        const uint8_t* kg = p.k_data + row * (D / 2);
+        const uint8_t* vg = p.v_data + row * (D / 2);
 #pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-      uint32_t pa[MT][4];
+        for (int i = 0; i < D / 32; ++i) {
+          cp_async16(dst + 16 * i, kg + 16 * i);
+          cp_async16(dst + D / 2 + 16 * i, vg + 16 * i);
+        }
+        if constexpr (D == 128) {
+          cp_async8(dst + D, p.k_sf + row * (D / 16));
+          cp_async8(dst + D + D / 16, p.v_sf + row * (D / 16));
+        } else {
+          cp_async4(dst + D, p.k_sf + row * (D / 16));
+          cp_async4(dst + D + D / 16, p.v_sf + row * (D / 16));
+        }
+      }
+      cp_async_commit();
+    };
+    issue(k0, 0);
+    issue(k0 + 32, 1);
+
+    int st = 0;
+    for (int kb = k0; kb < k1; kb += 32, st ^= 1) {
+      // ---- stage this lane's key: its V row as exact fp16 (zeros past k1)
+      cp_async_wait<1>();  // this lane's raw rows of this step have landed
+      __syncwarp();        // ... and every lane's; the previous batch's V rows have been read
+      {
+        uint4* dv = reinterpret_cast<uint4*>(sv + lane * kS);
+        const int key = kb + lane;
+        if (key < k1) {
+          const uint8_t* src = raw + (st * 32 + lane) * kLR;
+          uint4 vc4[D / 32];
+          uint32_t vsf4[D / 64];
+#pragma unroll
+          for (int i = 0; i < D / 32; ++i) vc4[i] = reinterpret_cast<const uint4*>(src + D / 2)[i];
+#pragma unroll
+          for (int i = 0; i < D / 64; ++i)
+            vsf4[i] = reinterpret_cast<const uint32_t*>(src + D + D / 16)[i];
+          const uint32_t* vc = reinterpret_cast<const uint32_t*>(vc4);
+#pragma unroll
+          for (int blk = 0; blk < D / 16; ++blk) {
+            const uint32_t s8v = (vsf4[blk / 4] >> (8 * (blk % 4))) & 0xFFu;
+            dv[2 * blk] = dequant8_f16(vc[2 * blk], s8v);
+            dv[2 * blk + 1] = dequant8_f16(vc[2 * blk + 1], s8v);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < D / 8; ++i) dv[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+
+      // ---- S = Q K^T for the 32 keys (4 n-tiles of 8 keys, D/16 k-steps).  The
+      // B fragment of n-tile j, k-step t (dims 16t .. 16t+15 = scale block t)
+      // holds, in lane l, key 8j + l/4 at dims 16t + 2(l%4) + {0, 1} and
+      // {8, 9} more: byte l%4 of code words 4(t/2) + 2(t%2) and the word after
+      // it of that key's raw row, times the block's scale.  Keys past k1 read
+      // stale ring bytes; their logits are replaced by -inf below.
+      float sacc[MT][4][4];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sacc[mt][j][e] = 0.0f;
+      const uint32_t bsel = static_cast<uint32_t>(lane % 4) | ((4u + static_cast<uint32_t>(lane % 4)) << 4);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint8_t* kr = raw + (st * 32 + 8 * j + lane / 4) * kLR;
+        uint32_t kw[D / 8];
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) {
+          const uint4 w4 = reinterpret_cast<const uint4*>(kr)[i];
+          kw[4 * i] = w4.x;
+          kw[4 * i + 1] = w4.y;
+          kw[4 * i + 2] = w4.z;
+          kw[4 * i + 3] = w4.w;
+        }
+        uint32_t ksf[D / 64];
+#pragma unroll
+        for (int i = 0; i < D / 64; ++i) ksf[i] = reinterpret_cast<const uint32_t*>(kr + D)[i];
+#pragma unroll
+        for (int s2 = 0; s2 < D / 32; ++s2) {
+          // bytes for k-steps 2 s2 (b0, b1) and 2 s2 + 1 (b0, b1), in that order
+          const uint32_t lo = __byte_perm(kw[4 * s2], kw[4 * s2 + 1], bsel);
+          const uint32_t hi = __byte_perm(kw[4 * s2 + 2], kw[4 * s2 + 3], bsel);
+          uint32_t h[4];
+          e2m1x8_to_f16x2(__byte_perm(lo, hi, 0x5410), h);
+          const uint32_t sa = e4m3_to_f16x2_dup(ksf[s2 / 2] >> (16 * (s2 % 2)));
+          const uint32_t sb = e4m3_to_f16x2_dup(ksf[s2 / 2] >> (16 * (s2 % 2) + 8));
+          const uint32_t b0a = hmul2_u32(h[0], sa), b1a = hmul2_u32(h[1], sa);
+          const uint32_t b0b = hmul2_u32(h[2], sb), b1b = hmul2_u32(h[3], sb);
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            mma16816(sacc[mt][j], qa[mt][2 * s2], b0a, b1a);
+            mma16816(sacc[mt][j], qa[mt][2 * s2 + 1], b0b, b1b);
+          }
+        }
+      }
+      __syncwarp();  // every lane has read this stage's raw rows; V rows are staged
+      // the raw stage just read takes the rows of the step after next
+      issue(kb + 64, st);
+
+      // ---- causal mask and online softmax; rows r0 = 16 mt + lane/4 (h = 0)
+      // and r0 + 8 (h = 1), keys kb + 8j + 2(lane%4) + e
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
-        pa[mt][0] = f16x2_of(sacc[mt][2 * kk][0], sacc[mt][2 * kk][1]);
-        pa[mt][1] = f16x2_of(sacc[mt][2 * kk][2], sacc[mt][2 * kk][3]);
-        pa[mt][2] = f16x2_of(sacc[mt][2 * kk + 1][0], sacc[mt][2 * kk + 1][1]);
-        pa[mt][3] = f16x2_of(sacc[mt][2 * kk + 1][2], sacc[mt][2 * kk + 1][3]);
-      }
 #pragma unroll
-      for (int nd2 = 0; nd2 < D / 16; ++nd2) {
-        uint32_t bv[4];  // n-tiles 2 nd2 and 2 nd2 + 1, keys 16 kk .. 16 kk + 15
-        const int m = lane / 8;
-        ldsm_x4_t(sv_addr + (16 * kk + 8 * (m & 1) + lane % 8) * kS + (16 * nd2 + 8 * (m >> 1)) * 2,
-                  bv);
+        for (int h = 0; h < 2; ++h) {
+          const int r = 16 * mt + lane / 4 + 8 * h;
+          const int lim = r < R ? min(k1 - 1, delta + r / G) : -1;  // last visible key
+          float mx = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int key = kb + 8 * j + 2 * (lane % 4) + e;
+              const float x = key <= lim ? sacc[mt][j][2 * h + e] * ssc : -INFINITY;
+              sacc[mt][j][2 * h + e] = x;
+              mx = fmaxf(mx, x);
+            }
+          mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+          const float m_new = fmaxf(mrow[mt][h], mx);
+          const float alpha = m_new == -INFINITY ? 1.0f : ex2_approx(mrow[mt][h] - m_new);
+          float psum = 0.0f;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float x = sacc[mt][j][2 * h + e];
+              const float pv = x == -INFINITY ? 0.0f : ex2_approx(x - m_new);
+              sacc[mt][j][2 * h + e] = pv;
+              psum += pv;
+            }
+          lrow[mt][h] = lrow[mt][h] * alpha + psum;
+          mrow[mt][h] = m_new;
+#pragma unroll
+          for (int nd = 0; nd < D / 8; ++nd) {
+            o[mt][nd][2 * h] *= alpha;
+            o[mt][nd][2 * h + 1] *= alpha;
+          }
+        }
+      }
+
+      // ---- O += P V (k-steps of 16 keys, n-tiles of 8 columns)
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        uint32_t pa[MT][4];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          mma16816(o[mt][2 * nd2], pa[mt], bv[0], bv[1]);
-          mma16816(o[mt][2 * nd2 + 1], pa[mt], bv[2], bv[3]);
+          pa[mt][0] = f16x2_of(sacc[mt][2 * kk][0], sacc[mt][2 * kk][1]);
+          pa[mt][1] = f16x2_of(sacc[mt][2 * kk][2], sacc[mt][2 * kk][3]);
+          pa[mt][2] = f16x2_of(sacc[mt][2 * kk + 1][0], sacc[mt][2 * kk + 1][1]);
+          pa[mt][3] = f16x2_of(sacc[mt][2 * kk + 1][2], sacc[mt][2 * kk + 1][3]);
+        }
+#pragma unroll
+        for (int nd2 = 0; nd2 < D / 16; ++nd2) {
+          uint32_t bv[4];  // n-tiles 2 nd2 and 2 nd2 + 1, keys 16 kk .. 16 kk + 15
+          const int m = lane / 8;
+          ldsm_x4_t(sv_addr + (16 * kk + 8 * (m & 1) + lane % 8) * kS + (16 * nd2 + 8 * (m >> 1)) * 2,
+                    bv);
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            mma16816(o[mt][2 * nd2], pa[mt], bv[0], bv[1]);
+            mma16816(o[mt][2 * nd2 + 1], pa[mt], bv[2], bv[3]);
+          }
         }
       }
     }
-  }
 
-  cp_async_wait<0>();  // (every copy was consumed; nothing is left in flight)
+    cp_async_wait<0>();  // (every copy was consumed; nothing is left in flight)
 
-  // ---- results: the whole sequence in this unit, or a partial slot
+    // ---- results: the whole sequence in this unit, or a partial slot
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
+    for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      float lsum = lrow[mt][h];
-      lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 1);
-      lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 2);
-      const int r = 16 * mt + lane / 4 + 8 * h;
-      if (r >= R) continue;
-      const int col = 2 * (lane % 4);
-      if (slot < 0) {
-        const int64_t orow =
-            static_cast<int64_t>(qo_start + r / G) * p.num_qo_heads + hk * G + r % G;
-        const float inv = vs / lsum;
-        __nv_bfloat16* dst = p.out + orow * D + col;
+      for (int h = 0; h < 2; ++h) {
+        float lsum = lrow[mt][h];
+        lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 1);
+        lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 2);
+        const int r = 16 * mt + lane / 4 + 8 * h;
+        if (r >= R) continue;
+        const int col = 2 * (lane % 4);
+        if (slot < 0) {
+          const int64_t orow =
+              static_cast<int64_t>(qo_start + r / G) * p.num_qo_heads + hk * G + r % G;
+          const float inv = vs / lsum;
+          __nv_bfloat16* dst = p.out + orow * D + col;
 #pragma unroll
-        for (int nd = 0; nd < D / 8; ++nd)
-          *reinterpret_cast<__nv_bfloat162*>(dst + 8 * nd) =
-              __floats2bfloat162_rn(o[mt][nd][2 * h] * inv, o[mt][nd][2 * h + 1] * inv);
-        if (p.lse && lane % 4 == 0)
-          p.lse[orow] = (mrow[mt][h] + log2f(lsum)) * 0.6931471805599453f;
-      } else {
-        float* dst = p.part + (static_cast<int64_t>(slot) * p.rows + r) * (D + 2);
+          for (int nd = 0; nd < D / 8; ++nd)
+            *reinterpret_cast<__nv_bfloat162*>(dst + 8 * nd) =
+                __floats2bfloat162_rn(o[mt][nd][2 * h] * inv, o[mt][nd][2 * h + 1] * inv);
+          if (p.lse && lane % 4 == 0)
+            p.lse[orow] = (mrow[mt][h] + log2f(lsum)) * 0.6931471805599453f;
+        } else {
+          float* dst = p.part + (static_cast<int64_t>(slot) * p.rows + r) * (D + 2);
 #pragma unroll
-        for (int nd = 0; nd < D / 8; ++nd) {
-          dst[8 * nd + col] = o[mt][nd][2 * h];
-          dst[8 * nd + col + 1] = o[mt][nd][2 * h + 1];
-        }
-        if (lane % 4 == 0) {
-          dst[D] = mrow[mt][h];
-          dst[D + 1] = lsum;
+          for (int nd = 0; nd < D / 8; ++nd) {
+            dst[8 * nd + col] = o[mt][nd][2 * h];
+            dst[8 * nd + col + 1] = o[mt][nd][2 * h + 1];
+          }
+          if (lane % 4 == 0) {
+            dst[D] = mrow[mt][h];
+            dst[D + 1] = lsum;
+          }
         }
       }
     }
@@ -442,8 +447,14 @@ __global__ void __launch_bounds__(32 * kDecWarps, MT == 1 ? 3 : 2)
 // scales (D/16 bytes a key), V rows (D/2 codes, D/16 scales, padded to 80
 // or 48 bytes so that the 8-byte or 4-byte reads of a half-warp or warp hit
 // distinct banks).
-constexpr int kTWarps = 4;   // warps (units) per CTA
+constexpr int kTWarps = 4;   // warps per CTA
 constexpr int kTStages = 2;  // raw stages per warp: this step's and the next
+
+// The planner sizes the warp count to what is resident per SM: 4 CTAs (up to
+// 8 rows) or 3 (up to 16) of this form, 2 of the form above (above 16 rows).
+static_assert(kTWarps * 4 == decode_warps_per_sm(8) && kTWarps * 3 == decode_warps_per_sm(16) &&
+                  kDecWarps * 2 == decode_warps_per_sm(32),
+              "decode occupancy and plan disagree");
 
 template <int D>
 constexpr int kTVRow = D == 128 ? 80 : 48;
@@ -476,316 +487,338 @@ __global__ void __launch_bounds__(32 * kTWarps, NT == 1 ? 4 : 3)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int g = lane / 4, t = lane % 4;
-  const int u = blockIdx.x * kTWarps + warp;
-  if (u >= p.num_units) return;  // no block-wide barrier below
-  const int4 w = __ldg(p.units + u);
-  const int b = w.x, hk = w.y, c = w.z, slot = w.w;
-  const int qo_start = __ldg(p.qo_indptr + b);
-  const int qo_len = __ldg(p.qo_indptr + b + 1) - qo_start;
-  const int kv_len = __ldg(p.kv_indptr + b + 1) - __ldg(p.kv_indptr + b);
-  const int G = p.group;
-  const int R = G * qo_len;  // <= 8 NT (the dispatch guarantees it)
-  const int delta = kv_len - qo_len;
-  const int k0 = c * p.chunk;
-  const int k1 = min(k0 + p.chunk, kv_len);
-  const float ks = __ldg(p.k_scale), vs = __ldg(p.v_scale);
-  uint8_t* ring = dsm + warp * kTStages * kStage;
-  const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.pt_stride;
-  auto q_ptr = [&](int r) {  // row r = token r / G, head hk * G + r % G
-    return p.q + (static_cast<int64_t>(qo_start + r / G) * p.num_qo_heads + hk * G + r % G) * D;
-  };
+  const int wid = blockIdx.x * kTWarps + warp;
+  if (wid >= p.num_warps) return;  // no block-wide barrier below
+  const int u_end = __ldg(p.warp_off + wid + 1);
+  for (int u = __ldg(p.warp_off + wid); u < u_end; ++u) {
+    __syncwarp();  // every lane is done with the previous piece's ring
+    const int4 w = __ldg(p.units + u);
+    const int b = w.x / p.num_kv_heads, hk = w.x - b * p.num_kv_heads, slot = w.w;
+    const int qo_start = __ldg(p.qo_indptr + b);
+    const int qo_len = __ldg(p.qo_indptr + b + 1) - qo_start;
+    const int kv_len = __ldg(p.kv_indptr + b + 1) - __ldg(p.kv_indptr + b);
+    const int G = p.group;
+    const int R = G * qo_len;  // <= 8 NT (the dispatch guarantees it)
+    const int delta = kv_len - qo_len;
+    const int k0 = w.y;  // the piece's keys: k0 .. k1 - 1
+    const int k1 = w.z;
+    const float ks = __ldg(p.k_scale), vs = __ldg(p.v_scale);
+    uint8_t* ring = dsm + warp * kTStages * kStage;
+    const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.pt_stride;
+    auto q_ptr = [&](int r) {  // row r = token r / G, head hk * G + r % G
+      return p.q + (static_cast<int64_t>(qo_start + r / G) * p.num_qo_heads + hk * G + r % G) * D;
+    };
 
-  // Q^T as fp16 B fragments, scaled as in the form above (a power of two
-  // brings every |value| below 2^14; the logits are multiplied back).
-  const float qs = p.sm_scale * ks * 1.4426950408889634f;
-  float qmax = 0.0f;
-  for (int i = lane; i < R * (D / 8); i += 32) {
-    float x[8];
-    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(q_ptr(i / (D / 8)) + (i % (D / 8)) * 8)), x);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) qmax = fmaxf(qmax, fabsf(x[e]));
-  }
-  qmax = warp_max(qmax) * qs;
-  const int qe = qmax > 0.0f ? ilogbf(qmax) - 13 : 0;
-  const float qsc = ldexpf(qs, -qe);
-  const float ssc = ldexpf(1.0f, qe);
-  uint32_t qb[NT][D / 16][2];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int r = 8 * nt + g;
-#pragma unroll
-    for (int i = 0; i < D / 32; ++i) {
+    // Q^T as fp16 B fragments, scaled as in the form above (a power of two
+    // brings every |value| below 2^14; the logits are multiplied back).
+    const float qs = p.sm_scale * ks * 1.4426950408889634f;
+    float qmax = 0.0f;
+    for (int i = lane; i < R * (D / 8); i += 32) {
       float x[8];
+      bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(q_ptr(i / (D / 8)) + (i % (D / 8)) * 8)), x);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = 0.0f;
-      if (r < R) bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(q_ptr(r) + t * (D / 4)) + i), x);
-      qb[nt][2 * i][0] = f16x2_of(x[0] * qsc, x[1] * qsc);
-      qb[nt][2 * i][1] = f16x2_of(x[2] * qsc, x[3] * qsc);
-      qb[nt][2 * i + 1][0] = f16x2_of(x[4] * qsc, x[5] * qsc);
-      qb[nt][2 * i + 1][1] = f16x2_of(x[6] * qsc, x[7] * qsc);
+      for (int e = 0; e < 8; ++e) qmax = fmaxf(qmax, fabsf(x[e]));
     }
-  }
-
-  // O^T accumulators (m-tile i, n-tile nt), and per lane the running max and
-  // sum of rows 8 nt + 2t + e.  The max is raised lazily: only when a step's
-  // max exceeds it by more than 8 (in log2 units), so exponentials stay at
-  // most 2^8 and the rescale of O is rare.
-  float o[D / 16][NT][4];
-  float mrun[NT][2], lrun[NT][2];
+    qmax = warp_max(qmax) * qs;
+    const int qe = qmax > 0.0f ? ilogbf(qmax) - 13 : 0;
+    const float qsc = ldexpf(qs, -qe);
+    const float ssc = ldexpf(1.0f, qe);
+    uint32_t qb[NT][D / 16][2];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      mrun[nt][e] = -INFINITY;
-      lrun[nt][e] = 0.0f;
-    }
-#pragma unroll
-    for (int i = 0; i < D / 16; ++i)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o[i][nt][e] = 0.0f;
-  }
-
-  // Raw rows of key kbs + lane into stage st (one commit group per call).  A
-  // key past the chunk gets zero V scales, so its stale V codes weigh 0.
-  auto page_of = [&](int key) { return key < k1 ? __ldg(pt + key / p.page_size) : 0; };
-  int page_next = page_of(k0 + lane);
-  auto issue = [&](int kbs, int st) {
-    const int key = kbs + lane;
-    int page = page_next;
-    page_next = page_of(key + 32);
-    uint8_t* s = ring + st * kStage;
-    if (key < k1) {
-      if (page < 0 || page >= p.num_pages) {
-        atomicOr(p.status, FI_DEV_PAGE_OOB);
-        page = 0;
-      }
-      const int64_t row =
-          (static_cast<int64_t>(page) * p.num_kv_heads + hk) * p.page_size + key % p.page_size;
-      const uint8_t* kg = p.k_data + row * (D / 2);
-      const uint8_t* vg = p.v_data + row * (D / 2);
+    for (int nt = 0; nt < NT; ++nt) {
+      const int r = 8 * nt + g;
 #pragma unroll
       for (int i = 0; i < D / 32; ++i) {
-        cp_async16(s + lane * (D / 2) + 16 * i, kg + 16 * i);
-        cp_async16(s + kV + lane * kVR + 16 * i, vg + 16 * i);
-      }
-      if constexpr (D == 128) {
-        cp_async8(s + kKsf + lane * 8, p.k_sf + row * 8);
-        cp_async8(s + kV + lane * kVR + 64, p.v_sf + row * 8);
-      } else {
-        cp_async4(s + kKsf + lane * 4, p.k_sf + row * 4);
-        cp_async4(s + kV + lane * kVR + 32, p.v_sf + row * 4);
-      }
-    } else {
-      if constexpr (D == 128)
-        *reinterpret_cast<uint2*>(s + kV + lane * kVR + 64) = make_uint2(0u, 0u);
-      else
-        *reinterpret_cast<uint32_t*>(s + kV + lane * kVR + 32) = 0u;
-    }
-    cp_async_commit();
-  };
+        float x[8];
 #pragma unroll
-  for (int i = 0; i < kTStages - 1; ++i) issue(k0 + 32 * i, i);
-
-  int st = 0;
-  for (int kb = k0; kb < k1; kb += 32) {
-    __syncwarp();  // every lane is done with the stage read in the previous step
-    issue(kb + 32 * (kTStages - 1), st == 0 ? kTStages - 1 : st - 1);
-    cp_async_wait<kTStages - 1>();  // this lane's rows of this step have landed
-    __syncwarp();                   // ... and every lane's
-    const uint8_t* sb = ring + st * kStage;
-
-    // ---- S^T = K Q^T: m-tiles of keys 0-15 and 16-31.  Keys past k1 read
-    // stale bytes; their logits are replaced by -inf below.
-    float sacc[2][NT][4];
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = 0.0f;
-      const int ka = 16 * mt + g, kz = ka + 8;
-      uint32_t ca[kKW], cz[kKW];
-      uint32_t sfa, sfz;
-      if constexpr (D == 128) {
-        const uint4 xa = *reinterpret_cast<const uint4*>(sb + ka * 64 + 16 * t);
-        const uint4 xz = *reinterpret_cast<const uint4*>(sb + kz * 64 + 16 * t);
-        ca[0] = xa.x; ca[1] = xa.y; ca[2] = xa.z; ca[3] = xa.w;
-        cz[0] = xz.x; cz[1] = xz.y; cz[2] = xz.z; cz[3] = xz.w;
-        sfa = *reinterpret_cast<const uint16_t*>(sb + kKsf + ka * 8 + 2 * t);
-        sfz = *reinterpret_cast<const uint16_t*>(sb + kKsf + kz * 8 + 2 * t);
-      } else {
-        const uint2 xa = *reinterpret_cast<const uint2*>(sb + ka * 32 + 8 * t);
-        const uint2 xz = *reinterpret_cast<const uint2*>(sb + kz * 32 + 8 * t);
-        ca[0] = xa.x; ca[1] = xa.y;
-        cz[0] = xz.x; cz[1] = xz.y;
-        sfa = sb[kKsf + ka * 4 + t];
-        sfz = sb[kKsf + kz * 4 + t];
-      }
-#pragma unroll
-      for (int i = 0; i < kKW; ++i) {
-        // code word i: bytes 4i .. 4i+3 of the lane's range = k-steps 2i, 2i+1;
-        // its scale block is the lane's first (bytes 0-7) or second (8-15)
-        const uint32_t sa = e4m3_to_f16x2_dup(sfa >> (8 * (i / 2)));
-        const uint32_t sz = e4m3_to_f16x2_dup(sfz >> (8 * (i / 2)));
-        uint32_t ha[4], hz[4];
-        e2m1x8_to_f16x2(ca[i], ha);
-        e2m1x8_to_f16x2(cz[i], hz);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t a[4];
-          a[0] = hmul2_u32(ha[2 * h], sa);
-          a[1] = hmul2_u32(hz[2 * h], sz);
-          a[2] = hmul2_u32(ha[2 * h + 1], sa);
-          a[3] = hmul2_u32(hz[2 * h + 1], sz);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-            mma16816(sacc[mt][nt], a, qb[nt][2 * i + h][0], qb[nt][2 * i + h][1]);
-        }
+        for (int e = 0; e < 8; ++e) x[e] = 0.0f;
+        if (r < R)
+          bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(q_ptr(r) + t * (D / 4)) + i), x);
+        qb[nt][2 * i][0] = f16x2_of(x[0] * qsc, x[1] * qsc);
+        qb[nt][2 * i][1] = f16x2_of(x[2] * qsc, x[3] * qsc);
+        qb[nt][2 * i + 1][0] = f16x2_of(x[4] * qsc, x[5] * qsc);
+        qb[nt][2 * i + 1][1] = f16x2_of(x[6] * qsc, x[7] * qsc);
       }
     }
 
-    // ---- causal mask and online softmax; lane holds rows 8 nt + 2t + e of
-    // keys kb + 16 mt + g + 8 h (accumulator element 2h + e)
+    // O^T accumulators (m-tile i, n-tile nt), and per lane the running max and
+    // sum of rows 8 nt + 2t + e.  The max is raised lazily: only when a step's
+    // max exceeds it by more than 8 (in log2 units), so exponentials stay at
+    // most 2^8 and the rescale of O is rare.
+    float o[D / 16][NT][4];
+    float mrun[NT][2], lrun[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int r = 8 * nt + 2 * t + e;
-        const int lim = r < R ? min(k1 - 1, delta + r / G) : -1;  // last visible key
-        float mx = -INFINITY;
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int key = kb + 16 * mt + g + 8 * h;
-            const float x = key <= lim ? sacc[mt][nt][2 * h + e] * ssc : -INFINITY;
-            sacc[mt][nt][2 * h + e] = x;
-            mx = fmaxf(mx, x);
-          }
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
-        if (mx > mrun[nt][e] + 8.0f) {
-          const float alpha = ex2_approx(mrun[nt][e] - mx);  // 0 while mrun is -inf
-          lrun[nt][e] *= alpha;
-#pragma unroll
-          for (int i = 0; i < D / 16; ++i) {
-            o[i][nt][e] *= alpha;
-            o[i][nt][2 + e] *= alpha;
-          }
-          mrun[nt][e] = mx;
-        }
-        float psum = 0.0f;
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const float x = sacc[mt][nt][2 * h + e];
-            const float pv = x == -INFINITY ? 0.0f : ex2_approx(x - mrun[nt][e]);
-            sacc[mt][nt][2 * h + e] = pv;
-            psum += pv;
-          }
-        lrun[nt][e] += psum;
+        mrun[nt][e] = -INFINITY;
+        lrun[nt][e] = 0.0f;
       }
+#pragma unroll
+      for (int i = 0; i < D / 16; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[i][nt][e] = 0.0f;
     }
 
-    // ---- O^T += V^T P^T, k-steps of keys 0-15 and 16-31
-    const uint8_t* vb = sb + kV;
+    // Raw rows of key kbs + lane into stage st (one commit group per call).  A
+    // key past the chunk gets zero V scales, so its stale V codes weigh 0.
+    auto page_of = [&](int key) { return key < k1 ? __ldg(pt + key / p.page_size) : 0; };
+    int page_next = page_of(k0 + lane);
+    auto issue = [&](int kbs, int st) {
+      const int key = kbs + lane;
+      int page = page_next;
+      page_next = page_of(key + 32);
+      uint8_t* s = ring + st * kStage;
+      if (key < k1) {
+        if (page < 0 || page >= p.num_pages) {
+          atomicOr(p.status, FI_DEV_PAGE_OOB);
+          page = 0;
+        }
+        const int64_t row =
+            (static_cast<int64_t>(page) * p.num_kv_heads + hk) * p.page_size + key % p.page_size;
+        const uint8_t* kg = p.k_data + row * (D / 2);
+        const uint8_t* vg = p.v_data + row * (D / 2);
 #pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-      uint32_t pb[NT][2];
+        for (int i = 0; i < D / 32; ++i) {
+          cp_async16(s + lane * (D / 2) + 16 * i, kg + 16 * i);
+          cp_async16(s + kV + lane * kVR + 16 * i, vg + 16 * i);
+        }
+        if constexpr (D == 128) {
+          cp_async8(s + kKsf + lane * 8, p.k_sf + row * 8);
+          cp_async8(s + kV + lane * kVR + 64, p.v_sf + row * 8);
+        } else {
+          cp_async4(s + kKsf + lane * 4, p.k_sf + row * 4);
+          cp_async4(s + kV + lane * kVR + 32, p.v_sf + row * 4);
+        }
+      } else {
+        if constexpr (D == 128)
+          *reinterpret_cast<uint2*>(s + kV + lane * kVR + 64) = make_uint2(0u, 0u);
+        else
+          *reinterpret_cast<uint32_t*>(s + kV + lane * kVR + 32) = 0u;
+      }
+      cp_async_commit();
+    };
+#pragma unroll
+    for (int i = 0; i < kTStages - 1; ++i) issue(k0 + 32 * i, i);
+
+    int st = 0;
+    for (int kb = k0; kb < k1; kb += 32) {
+      __syncwarp();  // every lane is done with the stage read in the previous step
+      issue(kb + 32 * (kTStages - 1), st == 0 ? kTStages - 1 : st - 1);
+      cp_async_wait<kTStages - 1>();  // this lane's rows of this step have landed
+      __syncwarp();                   // ... and every lane's
+      const uint8_t* sb = ring + st * kStage;
+
+      // ---- S^T = K Q^T: m-tiles of keys 0-15 and 16-31.  Keys past k1 read
+      // stale bytes; their logits are replaced by -inf below.
+      float sacc[2][NT][4];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = 0.0f;
+        const int ka = 16 * mt + g, kz = ka + 8;
+        uint32_t ca[kKW], cz[kKW];
+        uint32_t sfa, sfz;
+        if constexpr (D == 128) {
+          const uint4 xa = *reinterpret_cast<const uint4*>(sb + ka * 64 + 16 * t);
+          const uint4 xz = *reinterpret_cast<const uint4*>(sb + kz * 64 + 16 * t);
+          ca[0] = xa.x; ca[1] = xa.y; ca[2] = xa.z; ca[3] = xa.w;
+          cz[0] = xz.x; cz[1] = xz.y; cz[2] = xz.z; cz[3] = xz.w;
+          sfa = *reinterpret_cast<const uint16_t*>(sb + kKsf + ka * 8 + 2 * t);
+          sfz = *reinterpret_cast<const uint16_t*>(sb + kKsf + kz * 8 + 2 * t);
+        } else {
+          const uint2 xa = *reinterpret_cast<const uint2*>(sb + ka * 32 + 8 * t);
+          const uint2 xz = *reinterpret_cast<const uint2*>(sb + kz * 32 + 8 * t);
+          ca[0] = xa.x; ca[1] = xa.y;
+          cz[0] = xz.x; cz[1] = xz.y;
+          sfa = sb[kKsf + ka * 4 + t];
+          sfz = sb[kKsf + kz * 4 + t];
+        }
+#pragma unroll
+        for (int i = 0; i < kKW; ++i) {
+          // code word i: bytes 4i .. 4i+3 of the lane's range = k-steps 2i, 2i+1;
+          // its scale block is the lane's first (bytes 0-7) or second (8-15)
+          const uint32_t sa = e4m3x2_to_f16x2(__byte_perm(sfa, 0u, i / 2 ? 0x1111u : 0x0000u));
+          const uint32_t sz = e4m3x2_to_f16x2(__byte_perm(sfz, 0u, i / 2 ? 0x1111u : 0x0000u));
+          uint32_t ha[4], hz[4];
+          e2m1x8_to_f16x2(ca[i], ha);
+          e2m1x8_to_f16x2(cz[i], hz);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t a[4];
+            a[0] = hmul2_u32(ha[2 * h], sa);
+            a[1] = hmul2_u32(hz[2 * h], sz);
+            a[2] = hmul2_u32(ha[2 * h + 1], sa);
+            a[3] = hmul2_u32(hz[2 * h + 1], sz);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma16816(sacc[mt][nt], a, qb[nt][2 * i + h][0], qb[nt][2 * i + h][1]);
+          }
+        }
+      }
+
+      // ---- causal mask and online softmax; lane holds rows 8 nt + 2t + e of
+      // keys kb + 16 mt + g + 8 h (accumulator element 2h + e).  A step whose
+      // 32 keys every row sees (row 0 sees the fewest) takes no mask; rows past
+      // R then run on zero logits, finite and never written out.
+      const bool full = kb + 31 <= min(k1 - 1, delta);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        pb[nt][0] = movmatrix_t(f16x2_of(sacc[kk][nt][0], sacc[kk][nt][1]));
-        pb[nt][1] = movmatrix_t(f16x2_of(sacc[kk][nt][2], sacc[kk][nt][3]));
-      }
-      const int kA = 16 * kk + 2 * t;  // keys kA, kA+1 (k = 2t, 2t+1) and kA+8, kA+9
-      uint32_t va[kVW], vb1[kVW], vc[kVW], vd[kVW];
-      uint32_t sab, scd;
-      if constexpr (D == 128) {
-        const uint2 x0 = *reinterpret_cast<const uint2*>(vb + kA * kVR + 8 * g);
-        const uint2 x1 = *reinterpret_cast<const uint2*>(vb + (kA + 1) * kVR + 8 * g);
-        const uint2 x2 = *reinterpret_cast<const uint2*>(vb + (kA + 8) * kVR + 8 * g);
-        const uint2 x3 = *reinterpret_cast<const uint2*>(vb + (kA + 9) * kVR + 8 * g);
-        va[0] = x0.x; va[1] = x0.y; vb1[0] = x1.x; vb1[1] = x1.y;
-        vc[0] = x2.x; vc[1] = x2.y; vd[0] = x3.x; vd[1] = x3.y;
-        sab = vb[kA * kVR + 64 + g] | (vb[(kA + 1) * kVR + 64 + g] << 8);
-        scd = vb[(kA + 8) * kVR + 64 + g] | (vb[(kA + 9) * kVR + 64 + g] << 8);
-      } else {
-        va[0] = *reinterpret_cast<const uint32_t*>(vb + kA * kVR + 4 * g);
-        vb1[0] = *reinterpret_cast<const uint32_t*>(vb + (kA + 1) * kVR + 4 * g);
-        vc[0] = *reinterpret_cast<const uint32_t*>(vb + (kA + 8) * kVR + 4 * g);
-        vd[0] = *reinterpret_cast<const uint32_t*>(vb + (kA + 9) * kVR + 4 * g);
-        sab = vb[kA * kVR + 32 + g / 2] | (vb[(kA + 1) * kVR + 32 + g / 2] << 8);
-        scd = vb[(kA + 8) * kVR + 32 + g / 2] | (vb[(kA + 9) * kVR + 32 + g / 2] << 8);
-      }
-      const uint32_t s01 = e4m3x2_to_f16x2(sab), s89 = e4m3x2_to_f16x2(scd);
 #pragma unroll
-      for (int j = 0; j < kVW; ++j) {
-        // byte i of a word: low nibbles of the two keys (head dimension
-        // 2(g D/16 + 4j + i)), then their high nibbles (the next dimension)
-        const uint32_t lo01 = (va[j] & 0x0F0F0F0Fu) | ((vb1[j] << 4) & 0xF0F0F0F0u);
-        const uint32_t hi01 = ((va[j] >> 4) & 0x0F0F0F0Fu) | (vb1[j] & 0xF0F0F0F0u);
-        const uint32_t lo89 = (vc[j] & 0x0F0F0F0Fu) | ((vd[j] << 4) & 0xF0F0F0F0u);
-        const uint32_t hi89 = ((vc[j] >> 4) & 0x0F0F0F0Fu) | (vd[j] & 0xF0F0F0F0u);
-        uint32_t l01[4], h01[4], l89[4], h89[4];
-        e2m1x8_to_f16x2(lo01, l01);
-        e2m1x8_to_f16x2(hi01, h01);
-        e2m1x8_to_f16x2(lo89, l89);
-        e2m1x8_to_f16x2(hi89, h89);
+        for (int e = 0; e < 2; ++e) {
+          float mx;
+          if (full) {
+            mx = fmaxf(fmaxf(sacc[0][nt][e], sacc[0][nt][2 + e]),
+                       fmaxf(sacc[1][nt][e], sacc[1][nt][2 + e])) * ssc;
+          } else {
+            const int r = 8 * nt + 2 * t + e;
+            const int lim = r < R ? min(k1 - 1, delta + r / G) : -1;  // last visible key
+            mx = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint32_t a[4];
-          a[0] = hmul2_u32(l01[i], s01);
-          a[1] = hmul2_u32(h01[i], s01);
-          a[2] = hmul2_u32(l89[i], s89);
-          a[3] = hmul2_u32(h89[i], s89);
+            for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma16816(o[4 * j + i][nt], a, pb[nt][0], pb[nt][1]);
+              for (int h = 0; h < 2; ++h) {
+                const int key = kb + 16 * mt + g + 8 * h;
+                const float x = key <= lim ? sacc[mt][nt][2 * h + e] * ssc : -INFINITY;
+                sacc[mt][nt][2 * h + e] = x;
+                mx = fmaxf(mx, x);
+              }
+          }
+          mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
+          if (mx > mrun[nt][e] + 8.0f) {
+            const float alpha = ex2_approx(mrun[nt][e] - mx);  // 0 while mrun is -inf
+            lrun[nt][e] *= alpha;
+#pragma unroll
+            for (int i = 0; i < D / 16; ++i) {
+              o[i][nt][e] *= alpha;
+              o[i][nt][2 + e] *= alpha;
+            }
+            mrun[nt][e] = mx;
+          }
+          const float m = mrun[nt][e];
+          float psum = 0.0f;
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const float x = sacc[mt][nt][2 * h + e];
+              float pv;
+              if (full)
+                pv = ex2_approx(fmaf(x, ssc, -m));  // x is the unscaled logit here
+              else
+                pv = x == -INFINITY ? 0.0f : ex2_approx(x - m);
+              sacc[mt][nt][2 * h + e] = pv;
+              psum += pv;
+            }
+          lrun[nt][e] += psum;
         }
       }
+
+      // ---- O^T += V^T P^T, k-steps of keys 0-15 and 16-31
+      const uint8_t* vb = sb + kV;
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        uint32_t pb[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          pb[nt][0] = movmatrix_t(f16x2_of(sacc[kk][nt][0], sacc[kk][nt][1]));
+          pb[nt][1] = movmatrix_t(f16x2_of(sacc[kk][nt][2], sacc[kk][nt][3]));
+        }
+        const int kA = 16 * kk + 2 * t;  // keys kA, kA+1 (k = 2t, 2t+1) and kA+8, kA+9
+        uint32_t va[kVW], vb1[kVW], vc[kVW], vd[kVW];
+        uint32_t sab, scd;
+        if constexpr (D == 128) {
+          const uint2 x0 = *reinterpret_cast<const uint2*>(vb + kA * kVR + 8 * g);
+          const uint2 x1 = *reinterpret_cast<const uint2*>(vb + (kA + 1) * kVR + 8 * g);
+          const uint2 x2 = *reinterpret_cast<const uint2*>(vb + (kA + 8) * kVR + 8 * g);
+          const uint2 x3 = *reinterpret_cast<const uint2*>(vb + (kA + 9) * kVR + 8 * g);
+          va[0] = x0.x; va[1] = x0.y; vb1[0] = x1.x; vb1[1] = x1.y;
+          vc[0] = x2.x; vc[1] = x2.y; vd[0] = x3.x; vd[1] = x3.y;
+          sab = vb[kA * kVR + 64 + g] | (vb[(kA + 1) * kVR + 64 + g] << 8);
+          scd = vb[(kA + 8) * kVR + 64 + g] | (vb[(kA + 9) * kVR + 64 + g] << 8);
+        } else {
+          va[0] = *reinterpret_cast<const uint32_t*>(vb + kA * kVR + 4 * g);
+          vb1[0] = *reinterpret_cast<const uint32_t*>(vb + (kA + 1) * kVR + 4 * g);
+          vc[0] = *reinterpret_cast<const uint32_t*>(vb + (kA + 8) * kVR + 4 * g);
+          vd[0] = *reinterpret_cast<const uint32_t*>(vb + (kA + 9) * kVR + 4 * g);
+          sab = vb[kA * kVR + 32 + g / 2] | (vb[(kA + 1) * kVR + 32 + g / 2] << 8);
+          scd = vb[(kA + 8) * kVR + 32 + g / 2] | (vb[(kA + 9) * kVR + 32 + g / 2] << 8);
+        }
+        const uint32_t s01 = e4m3x2_to_f16x2(sab), s89 = e4m3x2_to_f16x2(scd);
+#pragma unroll
+        for (int j = 0; j < kVW; ++j) {
+          // byte i of a word: low nibbles of the two keys (head dimension
+          // 2(g D/16 + 4j + i)), then their high nibbles (the next dimension)
+          const uint32_t lo01 = (va[j] & 0x0F0F0F0Fu) | ((vb1[j] << 4) & 0xF0F0F0F0u);
+          const uint32_t hi01 = ((va[j] >> 4) & 0x0F0F0F0Fu) | (vb1[j] & 0xF0F0F0F0u);
+          const uint32_t lo89 = (vc[j] & 0x0F0F0F0Fu) | ((vd[j] << 4) & 0xF0F0F0F0u);
+          const uint32_t hi89 = ((vc[j] >> 4) & 0x0F0F0F0Fu) | (vd[j] & 0xF0F0F0F0u);
+          uint32_t l01[4], h01[4], l89[4], h89[4];
+          e2m1x8_to_f16x2(lo01, l01);
+          e2m1x8_to_f16x2(hi01, h01);
+          e2m1x8_to_f16x2(lo89, l89);
+          e2m1x8_to_f16x2(hi89, h89);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint32_t a[4];
+            a[0] = hmul2_u32(l01[i], s01);
+            a[1] = hmul2_u32(h01[i], s01);
+            a[2] = hmul2_u32(l89[i], s89);
+            a[3] = hmul2_u32(h89[i], s89);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma16816(o[4 * j + i][nt], a, pb[nt][0], pb[nt][1]);
+          }
+        }
+      }
+      st = st == kTStages - 1 ? 0 : st + 1;
     }
-    st = st == kTStages - 1 ? 0 : st + 1;
-  }
 
-  cp_async_wait<0>();  // (the copies past the chunk are empty groups; none is left in flight)
+    cp_async_wait<0>();  // (the copies past the chunk are empty groups; none is left in flight)
 
-  // ---- results: lane holds head dimensions g D/8 .. g D/8 + D/8 - 1 of rows
-  // 8 nt + 2t + e (m-tile i gives dimensions g D/8 + 2i and the one after)
+    // ---- results: lane holds head dimensions g D/8 .. g D/8 + D/8 - 1 of rows
+    // 8 nt + 2t + e (m-tile i gives dimensions g D/8 + 2i and the one after)
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
+    for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      float lsum = lrun[nt][e];
-      lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 4);
-      lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 8);
-      lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 16);
-      const int r = 8 * nt + 2 * t + e;
-      if (r >= R) continue;
-      const int d0 = g * (D / 8);
-      if (slot < 0) {
-        const int64_t orow =
-            static_cast<int64_t>(qo_start + r / G) * p.num_qo_heads + hk * G + r % G;
-        const float inv = vs / lsum;
-        uint32_t packed[D / 16];
+      for (int e = 0; e < 2; ++e) {
+        float lsum = lrun[nt][e];
+        lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 4);
+        lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 8);
+        lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 16);
+        const int r = 8 * nt + 2 * t + e;
+        if (r >= R) continue;
+        const int d0 = g * (D / 8);
+        if (slot < 0) {
+          const int64_t orow =
+              static_cast<int64_t>(qo_start + r / G) * p.num_qo_heads + hk * G + r % G;
+          const float inv = vs / lsum;
+          uint32_t packed[D / 16];
 #pragma unroll
-        for (int i = 0; i < D / 16; ++i) {
-          const __nv_bfloat162 v2 = __floats2bfloat162_rn(o[i][nt][e] * inv, o[i][nt][2 + e] * inv);
-          packed[i] = *reinterpret_cast<const uint32_t*>(&v2);
-        }
-        uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D + d0);
+          for (int i = 0; i < D / 16; ++i) {
+            const __nv_bfloat162 v2 =
+                __floats2bfloat162_rn(o[i][nt][e] * inv, o[i][nt][2 + e] * inv);
+            packed[i] = *reinterpret_cast<const uint32_t*>(&v2);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D + d0);
 #pragma unroll
-        for (int i = 0; i < D / 64; ++i)
-          dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
-        if (p.lse && g == 0) p.lse[orow] = (mrun[nt][e] + log2f(lsum)) * 0.6931471805599453f;
-      } else {
-        float* dst = p.part + (static_cast<int64_t>(slot) * p.rows + r) * (D + 2);
+          for (int i = 0; i < D / 64; ++i)
+            dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                packed[4 * i + 3]);
+          if (p.lse && g == 0) p.lse[orow] = (mrun[nt][e] + log2f(lsum)) * 0.6931471805599453f;
+        } else {
+          float* dst = p.part + (static_cast<int64_t>(slot) * p.rows + r) * (D + 2);
 #pragma unroll
-        for (int i = 0; i < D / 16; ++i)
-          *reinterpret_cast<float2*>(dst + d0 + 2 * i) = make_float2(o[i][nt][e], o[i][nt][2 + e]);
-        if (g == 0) {
-          dst[D] = mrun[nt][e];
-          dst[D + 1] = lsum;
+          for (int i = 0; i < D / 16; ++i)
+            *reinterpret_cast<float2*>(dst + d0 + 2 * i) =
+                make_float2(o[i][nt][e], o[i][nt][2 + e]);
+          if (g == 0) {
+            dst[D] = mrun[nt][e];
+            dst[D + 1] = lsum;
+          }
         }
       }
     }
@@ -843,7 +876,7 @@ fi_status launch_decode_impl(const DecodeParams& p, cudaStream_t stream) {
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
     return FI_ERR_CUDA;
-  const unsigned grid = static_cast<unsigned>((p.num_units + kDecWarps - 1) / kDecWarps);
+  const unsigned grid = static_cast<unsigned>((p.num_warps + kDecWarps - 1) / kDecWarps);
   fi_status st = launch_pdl(kern, dim3(grid), dim3(32 * kDecWarps), smem, stream, p);
   if (st != FI_OK || p.num_merges == 0) return st;
   const int64_t warps = static_cast<int64_t>(p.num_merges) * p.rows;
@@ -858,7 +891,7 @@ fi_status launch_decode_t_impl(const DecodeParams& p, cudaStream_t stream) {
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
     return FI_ERR_CUDA;
-  const unsigned grid = static_cast<unsigned>((p.num_units + kTWarps - 1) / kTWarps);
+  const unsigned grid = static_cast<unsigned>((p.num_warps + kTWarps - 1) / kTWarps);
   fi_status st = launch_pdl(kern, dim3(grid), dim3(32 * kTWarps), smem, stream, p);
   if (st != FI_OK || p.num_merges == 0) return st;
   const int64_t warps = static_cast<int64_t>(p.num_merges) * p.rows;
@@ -888,23 +921,25 @@ fi_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.units = reinterpret_cast<const int4*>(a.units_dev);
   p.merges = reinterpret_cast<const int4*>(a.merges_dev);
   p.part = a.part;
-  if (P.info.num_units > 0x7FFFFFFF) return FI_ERR_UNSUPPORTED;
-  p.num_units = static_cast<int32_t>(P.info.num_units);
+
   p.num_merges = static_cast<int32_t>(P.dec_merges.size() / 4);
   p.num_qo_heads = P.num_qo_heads;
   p.num_kv_heads = P.num_kv_heads;
   p.group = P.group;
   p.page_size = P.page_size;
   p.num_pages = a.cache.num_pages;
-  p.chunk = P.dec_chunk;
+  p.warp_off = a.warp_off_dev;
+  p.num_warps = P.dec_warps;
   p.rows = P.dec_rows;
   p.sm_scale = P.sm_scale;
   p.status = a.status;
   const int D = P.head_dim;
   if (P.dec_rows <= 8)
-    return D == 128 ? launch_decode_t_impl<128, 1>(p, stream) : launch_decode_t_impl<64, 1>(p, stream);
+    return D == 128 ? launch_decode_t_impl<128, 1>(p, stream)
+                    : launch_decode_t_impl<64, 1>(p, stream);
   if (P.dec_rows <= 16)
-    return D == 128 ? launch_decode_t_impl<128, 2>(p, stream) : launch_decode_t_impl<64, 2>(p, stream);
+    return D == 128 ? launch_decode_t_impl<128, 2>(p, stream)
+                    : launch_decode_t_impl<64, 2>(p, stream);
   return D == 128 ? launch_decode_impl<128, 2>(p, stream) : launch_decode_impl<64, 2>(p, stream);
 }
 

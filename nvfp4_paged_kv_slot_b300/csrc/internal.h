@@ -78,19 +78,30 @@ struct HostPlan {
   // slot_begin[s + 1]).  Empty otherwise (units are dealt round-robin).
   std::vector<int32_t> slot_units;
   std::vector<int32_t> slot_begin;
-  // decode plans (fi_decode_plan): units (sequence, kv head, chunk, partial
-  // slot or -1) and merges (sequence, kv head, first slot, chunks), 4 int32
-  // each; dec_rows = G * max qo_len rows per partial slot
+  // decode plans (fi_decode_plan): pieces (sequence * H_kv + kv head, first
+  // key, end key, partial slot or -1) and merges (sequence, kv head, first
+  // slot, pieces), 4 int32 each; warp w runs pieces dec_warp_off[w] ..
+  // dec_warp_off[w + 1] - 1; dec_rows = G * max qo_len rows per partial slot;
+  // dec_steps = the most key steps a warp takes
   bool decode = false;
-  int32_t dec_chunk = 0, dec_rows = 0;
+  int32_t dec_rows = 0, dec_warps = 0, dec_steps = 0;
   int64_t dec_parts = 0;
   std::vector<int32_t> dec_units;
   std::vector<int32_t> dec_merges;
+  std::vector<int32_t> dec_warp_off;
 };
 
 // Plans a decode (qo_len <= kDecodeMaxQo per sequence, G * qo_len <= 32).
 constexpr int kDecodeMaxQo = 8;
 constexpr int kDecodeMaxRows = 32;
+// Decode work split: keys go in steps of kDecodeStep (one warp-wide copy of
+// raw rows); a warp takes at least kDecodeMinSteps steps unless the batch has
+// fewer, and at most as many warps run as the decode kernels keep resident per
+// SM for the plan's rows (their launch bounds and shared memory: 4 CTAs of 4
+// warps up to 8 rows, 3 up to 16, 2 above).
+constexpr int kDecodeStep = 32;
+constexpr int kDecodeMinSteps = 8;
+constexpr int decode_warps_per_sm(int rows) { return rows <= 8 ? 16 : rows <= 16 ? 12 : 8; }
 fi_status plan_decode_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t batch,
                            int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
                            int32_t page_size, float sm_scale, int32_t num_sms, HostPlan* out);
@@ -101,6 +112,7 @@ struct DecodeArgs {
   const int32_t* kv_indptr_dev;
   const int32_t* units_dev;
   const int32_t* merges_dev;
+  const int32_t* warp_off_dev;
   float* part;
   const int32_t* page_table;
   int32_t page_table_stride;

@@ -280,45 +280,64 @@ fi_status plan_decode_host(const int32_t* qo_indptr, const int32_t* kv_indptr, i
   I.ctas_per_unit = 1;
   I.kv_bytes = I.total_kv_len * num_kv_heads * 2 * (head_dim / 2 + head_dim / 16);
   P.dec_rows = std::max(1, P.group * max_qo);
-  auto count_units = [&](int64_t chunk) {
-    int64_t n = 0;
-    for (int32_t b = 0; b < batch; ++b) {
-      const int32_t qo = qo_indptr[b + 1] - qo_indptr[b];
-      const int32_t kv = kv_indptr[b + 1] - kv_indptr[b];
-      if (qo > 0) n += (kv + chunk - 1) / chunk;
-    }
-    return n * num_kv_heads;
-  };
-  int64_t chunk = 256;
-  const int64_t cap = 32 * static_cast<int64_t>(std::max(num_sms, 1));
-  while (chunk < 16384 && count_units(chunk) > cap) chunk *= 2;
-  P.dec_chunk = static_cast<int32_t>(chunk);
-  int64_t slots = 0;
+  // Balanced split: the keys of every (sequence, KV head) pair with queries,
+  // in steps of kDecodeStep keys, laid end to end in (sequence, head) order
+  // and cut into W runs of equal length (to one step), one per warp.  A run
+  // that crosses pairs becomes one piece per pair; a pair cut into several
+  // pieces gets one partial slot per piece (consecutive) and one merge item.
+  if (static_cast<int64_t>(batch) * num_kv_heads > 0x7FFFFFFF) return FI_ERR_UNSUPPORTED;
+  int64_t total = 0;
+  for (int32_t b = 0; b < batch; ++b) {
+    const int32_t qo = qo_indptr[b + 1] - qo_indptr[b];
+    const int32_t kv = kv_indptr[b + 1] - kv_indptr[b];
+    if (qo > 0)
+      total += static_cast<int64_t>(num_kv_heads) * ((kv + kDecodeStep - 1) / kDecodeStep);
+  }
+  const int64_t resident = static_cast<int64_t>(num_sms) * decode_warps_per_sm(P.dec_rows);
+  const int64_t W =
+      total == 0 ? 0
+                 : std::max<int64_t>(1, std::min(resident, (total + kDecodeMinSteps - 1) /
+                                                                kDecodeMinSteps));
+  auto first_step = [&](int64_t w) { return w * total / W; };  // warp w's first step
+  P.dec_warp_off.assign(static_cast<size_t>(W) + 1, 0);
+  int64_t s0 = 0, w = 0, slots = 0, pieces = 0;
   for (int32_t b = 0; b < batch; ++b) {
     const int32_t qo = qo_indptr[b + 1] - qo_indptr[b];
     const int32_t kv = kv_indptr[b + 1] - kv_indptr[b];
     if (qo == 0) continue;
-    const int32_t n = static_cast<int32_t>((kv + chunk - 1) / chunk);
+    const int64_t n = (kv + kDecodeStep - 1) / kDecodeStep;  // >= 1: kv >= qo > 0
     for (int32_t hk = 0; hk < num_kv_heads; ++hk) {
-      for (int32_t c = 0; c < n; ++c) {
-        P.dec_units.push_back(b);
-        P.dec_units.push_back(hk);
-        P.dec_units.push_back(c);
-        P.dec_units.push_back(n > 1 ? static_cast<int32_t>(slots + c) : -1);
+      const int64_t pe = s0 + n;
+      int64_t wl = w;  // the warp that takes the pair's last step
+      while (first_step(wl + 1) <= pe - 1) ++wl;
+      const bool split = wl > w;
+      const int64_t first_slot = slots;
+      for (int64_t st = s0; st < pe;) {
+        const int64_t end = std::min(pe, first_step(w + 1));
+        P.dec_units.push_back(b * num_kv_heads + hk);
+        P.dec_units.push_back(static_cast<int32_t>((st - s0) * kDecodeStep));
+        P.dec_units.push_back(
+            static_cast<int32_t>(std::min<int64_t>((end - s0) * kDecodeStep, kv)));
+        P.dec_units.push_back(split ? static_cast<int32_t>(slots++) : -1);
+        ++pieces;
+        if (end == first_step(w + 1)) P.dec_warp_off[++w] = static_cast<int32_t>(pieces);
+        st = end;
       }
-      if (n > 1) {
+      if (split) {
         P.dec_merges.push_back(b);
         P.dec_merges.push_back(hk);
-        P.dec_merges.push_back(static_cast<int32_t>(slots));
-        P.dec_merges.push_back(n);
-        slots += n;
+        P.dec_merges.push_back(static_cast<int32_t>(first_slot));
+        P.dec_merges.push_back(static_cast<int32_t>(slots - first_slot));
       }
+      s0 = pe;
     }
   }
-  if (slots > 0x7FFFFFFF) return FI_ERR_UNSUPPORTED;
+  if (slots > 0x7FFFFFFF || pieces > 0x7FFFFFFF) return FI_ERR_UNSUPPORTED;
   P.dec_parts = slots;
-  I.num_units = static_cast<int64_t>(P.dec_units.size() / 4);
-  I.num_ctas = static_cast<int32_t>(std::min<int64_t>((I.num_units + 3) / 4, 0x7FFFFFFF));
+  P.dec_warps = static_cast<int32_t>(W);
+  P.dec_steps = W > 0 ? static_cast<int32_t>((total + W - 1) / W) : 0;
+  I.num_units = pieces;
+  I.num_ctas = static_cast<int32_t>((W + 3) / 4);
   return FI_OK;
 }
 
@@ -328,19 +347,21 @@ extern "C" fi_status fi_decode_plan_host(const int32_t* qo_indptr_host,
                                          const int32_t* kv_indptr_host, int32_t batch,
                                          int32_t num_qo_heads, int32_t num_kv_heads,
                                          int32_t head_dim, int32_t page_size, int32_t num_sms,
-                                         fi_plan_info* info, int32_t* chunk_out,
+                                         fi_plan_info* info, int32_t* num_warps_out,
                                          int64_t* num_merges_out, int32_t* units_out,
                                          int64_t unit_capacity, int32_t* merges_out,
-                                         int64_t merge_capacity) {
-  if (!info || !chunk_out || !num_merges_out || num_sms <= 0 ||
-      (units_out && unit_capacity < 0) || (merges_out && merge_capacity < 0))
+                                         int64_t merge_capacity, int32_t* warp_off_out,
+                                         int64_t warp_off_capacity) {
+  if (!info || !num_warps_out || !num_merges_out || num_sms <= 0 ||
+      (units_out && unit_capacity < 0) || (merges_out && merge_capacity < 0) ||
+      (warp_off_out && warp_off_capacity < 0))
     return FI_ERR_INVALID_ARGUMENT;
   fi::HostPlan P;
   const fi_status st = fi::plan_decode_host(qo_indptr_host, kv_indptr_host, batch, num_qo_heads,
                                             num_kv_heads, head_dim, page_size, 0.0f, num_sms, &P);
   if (st != FI_OK) return st;
   *info = P.info;
-  *chunk_out = P.dec_chunk;
+  *num_warps_out = P.dec_warps;
   const int64_t merges = static_cast<int64_t>(P.dec_merges.size() / 4);
   *num_merges_out = merges;
   if (units_out) {
@@ -350,6 +371,10 @@ extern "C" fi_status fi_decode_plan_host(const int32_t* qo_indptr_host,
   if (merges_out) {
     const int64_t n = std::min<int64_t>(merge_capacity, merges);
     std::memcpy(merges_out, P.dec_merges.data(), static_cast<size_t>(n) * 4 * sizeof(int32_t));
+  }
+  if (warp_off_out) {
+    const int64_t n = std::min<int64_t>(warp_off_capacity, P.dec_warps + 1);
+    std::memcpy(warp_off_out, P.dec_warp_off.data(), static_cast<size_t>(n) * sizeof(int32_t));
   }
   return FI_OK;
 }

@@ -1,7 +1,8 @@
 """Decode through the C ABI vs the oracle: the newest 1..8 tokens of each
 sequence attend to its whole NVFP4 cache (query row t sees keys
-j <= t + kv_len - qo_len), split into KV chunks and merged, within the same
-tolerances as the prefill."""
+j <= t + kv_len - qo_len), the keys split evenly over the kernel's warps and
+pairs cut into several pieces merged, within the same tolerances as the
+prefill."""
 import numpy as np
 import pytest
 import torch
@@ -39,7 +40,7 @@ def _run_decode(d):
 
 
 @pytest.mark.parametrize("name", ["decode_small", "decode_spec_small", "decode_d64", "decode_g8",
-                                  "decode_g6_d64"])
+                                  "decode_g6_d64", "decode_mixed"])
 def test_decode_matches_oracle(name):
     d = device_inputs(name)
     out, lse, c, status, info = _run_decode(d)
@@ -53,14 +54,14 @@ def test_decode_matches_oracle(name):
     assert_within_tolerance(res)
 
 
-def test_decode_splits_long_sequences_into_merged_chunks():
-    """decode_small has a 5000-key sequence: several chunks, merged; its rows
-    must agree with the oracle like the single-chunk ones."""
+def test_decode_splits_long_sequences_into_merged_pieces():
+    """decode_small has a 5000-key sequence: cut into pieces over several
+    warps, merged; its rows must agree with the oracle like the others."""
     d = device_inputs("decode_small")
     out, lse, _, status, info = _run_decode(d)
     assert status == 0
     sp = d["spec"]
-    # units = sum over sequences of ceil(kv_len / chunk) per kv head, chunk >= 256
+    # 404 steps of 32 keys over 51 warps: more pieces than (sequence, head) pairs
     assert info["num_units"] > sp.num_kv_heads * len(sp.seq_lens)
     host = oracle_cache(d)
     ref_out, ref_lse = oracle_attention(d, host)

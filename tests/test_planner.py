@@ -5,6 +5,8 @@ Mirrors the pages' plan tests: FlashInfer PR #5043 analysis page ("plan() 함수
 uint32 and several batch and page sizes; and the scheduling rules of the PR
 #3575 page (O(1) uniform decode, global reverse-Q-tile order, L2 gate).
 """
+import itertools
+
 import numpy as np
 import pytest
 
@@ -210,73 +212,98 @@ def test_balanced_ragged_plan_bounds():
 
 # ---------------------------------------------------------------- decode plans
 # The decode plan of the PR #5043 page (max_kv_len from one reduction over the
-# lengths) with this library's split: units (sequence, KV head, chunk of keys),
-# the chunk the smallest power of two from 256 to 16384 that keeps at most 32
-# units per SM, one partial slot per chunk and one merge per multi-chunk
-# (sequence, KV head).
+# lengths) with this library's split: the keys of all (sequence, KV head)
+# pairs in 32-key steps, laid end to end and cut evenly over W warps (the warps
+# the kernel keeps resident: 16 per SM up to 8 rows, 12 up to 16, 8 above; at
+# least 8 steps a warp); one piece per pair a warp touches, consecutive partial
+# slots and one merge for a pair cut into several pieces.
 
 def _decode_plan(qo_lens, kv_lens, hq, hk, num_sms=148, d=128, ps=16):
     return fi.fi_decode_plan_host(fi.indptr_from_lens(qo_lens), fi.indptr_from_lens(kv_lens),
                                   hq, hk, d, ps, num_sms=num_sms)
 
 
-def _check_decode_cover(qo_lens, kv_lens, hk, chunk, units, merges):
-    """Every (sequence, KV head) with queries is split into ceil(kv / chunk) units
-    that cover its keys once; multi-chunk ones own consecutive partial slots and
-    one merge item, single-chunk ones write directly (slot -1)."""
-    expect = [(b, h) for b in range(len(kv_lens)) if qo_lens[b] > 0 for h in range(hk)]
-    seen = {}
-    for b, h, c, slot in units.tolist():
-        seen.setdefault((b, h), []).append((c, slot))
-    assert sorted(seen) == expect
-    merge_of = {(b, h): (first, n) for b, h, first, n in merges.tolist()}
-    next_slot = 0
-    for (b, h) in expect:                       # units and merges in (sequence, head) order
-        n = -(-kv_lens[b] // chunk)
-        got = seen[(b, h)]
-        assert [c for c, _ in got] == list(range(n))
-        if n == 1:
-            assert got[0][1] == -1 and (b, h) not in merge_of
-        else:
-            assert merge_of[(b, h)] == (next_slot, n)
-            assert [s for _, s in got] == list(range(next_slot, next_slot + n))
-            next_slot += n
+def _expected_split(qo_lens, kv_lens, hk, warps_per_sm, num_sms):
+    """The split by brute force: the owner warp of every step, then the pieces
+    as maximal runs of one owner within a pair."""
+    pairs = [(b, h, -(-kv_lens[b] // 32)) for b in range(len(kv_lens)) if qo_lens[b] > 0
+             for h in range(hk)]
+    total = sum(n for _, _, n in pairs)
+    warps = 0 if total == 0 else max(1, min(num_sms * warps_per_sm, -(-total // 8)))
+    owner = [w for w in range(warps) for _ in range(w * total // warps, (w + 1) * total // warps)]
+    assert len(owner) == total
+    pieces, merges, slot, s = [], [], 0, 0
+    for b, h, n in pairs:
+        runs = [(w, [i for i, _ in grp]) for w, grp in
+                itertools.groupby(enumerate(owner[s:s + n]), key=lambda x: x[1])]
+        first = slot
+        for w, steps in runs:
+            pslot = -1
+            if len(runs) > 1:
+                pslot, slot = slot, slot + 1
+            pieces.append((w, [b * hk + h, steps[0] * 32, min((steps[-1] + 1) * 32, kv_lens[b]),
+                               pslot]))
+        if len(runs) > 1:
+            merges.append([b, h, first, len(runs)])
+        s += n
+    return warps, pieces, merges
+
+
+def _check_decode_split(qo_lens, kv_lens, hk, warps_per_sm, num_sms, plan):
+    info, warps, units, merges, off = plan
+    want_warps, pieces, want_merges = _expected_split(qo_lens, kv_lens, hk, warps_per_sm, num_sms)
+    assert warps == want_warps and info["num_ctas"] == -(-warps // 4)
+    assert units.tolist() == [p for _, p in pieces]
+    assert merges.tolist() == want_merges
+    assert off.tolist() == [sum(1 for w, _ in pieces if w < k) for k in range(warps + 1)]
 
 
 def test_decode_plan_of_the_decode_workload():
     import workloads as W
     sp = W.spec("decode")
-    info, chunk, units, merges = _decode_plan(sp.qo_lens, sp.seq_lens, 32, 8)
-    # 128 x 8 (sequence, head) pairs of 4096 keys on 148 SMs: 32 units per SM
-    # allow 4736 units, so chunks of 1024 keys (4096 units); 512 would give 8192.
-    assert chunk == 1024 and info["num_units"] == 4096 and merges.shape == (1024, 4)
+    plan = _decode_plan(sp.qo_lens, sp.seq_lens, 32, 8)
+    info, warps, units, merges, off = plan
+    # 128 x 8 pairs of 128 steps = 131072 steps over 148 SMs x 16 warps: 55 or
+    # 56 steps a warp; every pair is cut into 3 or 4 pieces and merged
+    assert warps == 2368 and merges.shape == (1024, 4)
+    steps = [sum(-(-(u[2] - u[1]) // 32) for u in units[off[w]:off[w + 1]]) for w in range(warps)]
+    assert min(steps) == 55 and max(steps) == 56
+    assert set(merges[:, 3].tolist()) <= {3, 4}
     assert info["max_qo_len"] == 1 and info["max_kv_len"] == 4096 and info["is_uniform"] == 1
-    _check_decode_cover(sp.qo_lens, sp.seq_lens, 8, chunk, units, merges)
+    _check_decode_split(sp.qo_lens, sp.seq_lens, 8, 16, 148, plan)
 
 
-@pytest.mark.parametrize("num_sms,want_chunk", [(148, 256), (1, 512), (200000, 256)])
-def test_decode_chunk_is_the_smallest_power_of_two_that_fits(num_sms, want_chunk):
+@pytest.mark.parametrize("num_sms,want_warps", [(148, 43), (1, 16), (200000, 43)])
+def test_decode_warps_are_resident_and_take_at_least_8_steps(num_sms, want_warps):
+    # G = 4, 2 query tokens: 8 rows, 16 warps per SM; (4 + 10 + 157) x 2 = 342 steps
     qo, kv = [1, 1, 2], [100, 300, 5000]
-    info, chunk, units, merges = _decode_plan(qo, kv, 8, 2, num_sms=num_sms)
-    assert chunk == want_chunk
-    # 256 keys: (1 + 2 + 20) chunks x 2 heads = 46 units, above 32 for one SM;
-    # 512 keys: (1 + 1 + 10) x 2 = 24
-    assert info["num_units"] == {256: 46, 512: 24}[chunk]
-    _check_decode_cover(qo, kv, 2, chunk, units, merges)
+    plan = _decode_plan(qo, kv, 8, 2, num_sms=num_sms)
+    assert plan[1] == want_warps
+    _check_decode_split(qo, kv, 2, 16, num_sms, plan)
 
 
-def test_decode_chunk_stops_at_16384():
-    # one SM cannot hold 1024 units whatever the chunk: the chunk stops at 16384
-    info, chunk, units, merges = _decode_plan([1] * 128, [4096] * 128, 32, 8, num_sms=1)
-    assert chunk == 16384 and info["num_units"] == 1024 and merges.shape[0] == 0
-    assert (units[:, 3] == -1).all()
+@pytest.mark.parametrize("hq,qo_len,warps_per_sm", [(12, 2, 12), (16, 3, 8), (8, 1, 16)])
+def test_decode_warps_per_sm_follow_the_rows(hq, qo_len, warps_per_sm):
+    # rows G * qo_len with 2 KV heads: 6 * 2 = 12, 8 * 3 = 24, 4 * 1 = 4
+    qo, kv = [qo_len] * 64, [3000] * 64
+    plan = _decode_plan(qo, kv, hq, 2, num_sms=2)
+    assert plan[1] == 2 * warps_per_sm
+    _check_decode_split(qo, kv, 2, warps_per_sm, 2, plan)
+
+
+def test_decode_plan_of_one_short_sequence():
+    # one step: one warp, one piece written directly, nothing to merge
+    plan = _decode_plan([1], [5], 8, 1)
+    info, warps, units, merges, off = plan
+    assert warps == 1 and units.tolist() == [[0, 0, 5, -1]] and merges.shape[0] == 0
+    assert off.tolist() == [0, 1]
 
 
 def test_decode_plan_skips_sequences_without_queries():
     qo, kv = [0, 2, 0, 1], [50, 700, 9, 3000]
-    info, chunk, units, merges = _decode_plan(qo, kv, 4, 2)
-    assert set(units[:, 0].tolist()) == {1, 3}
-    _check_decode_cover(qo, kv, 2, chunk, units, merges)
+    plan = _decode_plan(qo, kv, 4, 2)
+    assert set((plan[2][:, 0] // 2).tolist()) == {1, 3}
+    _check_decode_split(qo, kv, 2, 16, 148, plan)
 
 
 @pytest.mark.parametrize("args,code", [

@@ -115,6 +115,13 @@ def spec(name: str) -> Spec:
     if name == "decode_g6_d64":
         return Spec("decode_g6_d64", 13200, num_kv_heads=2, head_dim=64, page_size=64,
                     num_qo_heads=12, seq_lens=[1, 2049, 400], qo_lens=[1, 2, 2], attn="decode")
+    # Many short sequences and one long one: warps that run several pieces of
+    # different sequences, and pairs cut across warps.
+    if name == "decode_mixed":
+        return Spec("decode_mixed", 13300, num_kv_heads=2, head_dim=128, page_size=16,
+                    num_qo_heads=8, seq_lens=[3, 17, 33, 64, 5, 100, 31, 32, 2, 700, 9, 12, 40,
+                                              1, 250, 48] * 2 + [3000], qo_lens=[1] * 33,
+                    attn="decode")
     if name == "uniform_small":
         return Spec("uniform_small", 7000, num_kv_heads=2, head_dim=128, page_size=16,
                     num_qo_heads=8, seq_lens=[384] * 6)
