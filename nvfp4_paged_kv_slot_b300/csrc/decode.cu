@@ -49,7 +49,8 @@ struct DecodeParams {
   float* part;         // partial slots: [slot][rows][D + 2] = O, then m, l
   const int32_t* warp_off;  // warp w runs pieces warp_off[w] .. warp_off[w + 1] - 1
   int32_t num_warps, num_merges, num_qo_heads, num_kv_heads, group, page_size, num_pages;
-  int32_t rows;  // partial rows per slot (G * max qo_len)
+  int32_t rows;      // partial rows per slot (G * max qo_len)
+  int32_t ps_shift;  // log2 of page_size (a power of two)
   float sm_scale;
   int32_t* status;
 };
@@ -196,7 +197,7 @@ __global__ void __launch_bounds__(32 * kDecWarps, MT == 1 ? 3 : 2)
     // Raw rows of key kbs + lane into ring stage st (one commit group per call,
     // empty past the chunk).  The page id comes from the previous call, so the
     // page-table read is one step ahead of the copies that need it.
-    auto page_of = [&](int key) { return key < k1 ? __ldg(pt + key / p.page_size) : 0; };
+    auto page_of = [&](int key) { return key < k1 ? __ldg(pt + (key >> p.ps_shift)) : 0; };
     int page_next = page_of(k0 + lane);
     auto issue = [&](int kbs, int st) {
       const int key = kbs + lane;
@@ -208,7 +209,8 @@ __global__ void __launch_bounds__(32 * kDecWarps, MT == 1 ? 3 : 2)
           page = 0;
         }
         const int64_t row =
-            (static_cast<int64_t>(page) * p.num_kv_heads + hk) * p.page_size + key % p.page_size;
+            (static_cast<int64_t>(page) * p.num_kv_heads + hk) * p.page_size +
+            (key & (p.page_size - 1));
         uint8_t* dst = raw + (st * 32 + lane) * kLR;
         const uint8_t* kg = p.k_data + row * (D / 2);
         const uint8_t* vg = p.v_data + row * (D / 2);
@@ -560,29 +562,43 @@ __global__ void __launch_bounds__(32 * kTWarps, NT == 1 ? 4 : 3)
         for (int e = 0; e < 4; ++e) o[i][nt][e] = 0.0f;
     }
 
-    // Raw rows of key kbs + lane into stage st (one commit group per call).  A
-    // key past the chunk gets zero V scales, so its stale V codes weigh 0.
-    auto page_of = [&](int key) { return key < k1 ? __ldg(pt + key / p.page_size) : 0; };
+    // Raw rows of keys kbs .. kbs+31 into stage st (one commit group per
+    // call).  Lane l owns key kbs + l: its page id (read one step ahead) and
+    // its two scale rows.  The code rows are copied by the whole warp, so that
+    // each instruction reads 512 contiguous bytes of one page (8 rows of 64
+    // bytes or 16 of 32): instruction i copies rows kRpi*i .. kRpi*i + kRpi-1
+    // in 16-byte chunks, each row's page id taken from the lane that owns it.
+    // A key past the piece gets zero V scales, so its stale V codes weigh 0.
+    constexpr int kChunks = D / 32;      // 16-byte chunks per code row
+    constexpr int kRpi = 32 / kChunks;   // code rows per warp instruction
+    const int ps_mask = p.page_size - 1;
+    auto page_of = [&](int key) { return key < k1 ? __ldg(pt + (key >> p.ps_shift)) : 0; };
     int page_next = page_of(k0 + lane);
+    auto row_of = [&](int page, int key) {
+      return (static_cast<int64_t>(page) * p.num_kv_heads + hk) * p.page_size + (key & ps_mask);
+    };
     auto issue = [&](int kbs, int st) {
       const int key = kbs + lane;
       int page = page_next;
       page_next = page_of(key + 32);
       uint8_t* s = ring + st * kStage;
-      if (key < k1) {
-        if (page < 0 || page >= p.num_pages) {
-          atomicOr(p.status, FI_DEV_PAGE_OOB);
-          page = 0;
-        }
-        const int64_t row =
-            (static_cast<int64_t>(page) * p.num_kv_heads + hk) * p.page_size + key % p.page_size;
-        const uint8_t* kg = p.k_data + row * (D / 2);
-        const uint8_t* vg = p.v_data + row * (D / 2);
+      if (key < k1 && (page < 0 || page >= p.num_pages)) {
+        atomicOr(p.status, FI_DEV_PAGE_OOB);
+        page = 0;
+      }
 #pragma unroll
-        for (int i = 0; i < D / 32; ++i) {
-          cp_async16(s + lane * (D / 2) + 16 * i, kg + 16 * i);
-          cp_async16(s + kV + lane * kVR + 16 * i, vg + 16 * i);
+      for (int i = 0; i < kChunks; ++i) {
+        const int kr = kRpi * i + lane / kChunks;  // the step's row this lane copies
+        const int ch = lane % kChunks;
+        const int pg = __shfl_sync(0xFFFFFFFFu, page, kr);
+        if (kbs + kr < k1) {
+          const int64_t row = row_of(pg, kbs + kr);
+          cp_async16(s + kr * (D / 2) + 16 * ch, p.k_data + row * (D / 2) + 16 * ch);
+          cp_async16(s + kV + kr * kVR + 16 * ch, p.v_data + row * (D / 2) + 16 * ch);
         }
+      }
+      if (key < k1) {
+        const int64_t row = row_of(page, key);
         if constexpr (D == 128) {
           cp_async8(s + kKsf + lane * 8, p.k_sf + row * 8);
           cp_async8(s + kV + lane * kVR + 64, p.v_sf + row * 8);
@@ -927,6 +943,8 @@ fi_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.num_kv_heads = P.num_kv_heads;
   p.group = P.group;
   p.page_size = P.page_size;
+  p.ps_shift = 0;
+  while ((1 << p.ps_shift) < P.page_size) ++p.ps_shift;
   p.num_pages = a.cache.num_pages;
   p.warp_off = a.warp_off_dev;
   p.num_warps = P.dec_warps;
