@@ -567,8 +567,8 @@ __global__ void __launch_bounds__(32 * kTWarps, NT == 1 ? 4 : 3)
     // its two scale rows.  The code rows are copied by the whole warp, so that
     // each instruction reads 512 contiguous bytes of one page (8 rows of 64
     // bytes or 16 of 32): instruction i copies rows kRpi*i .. kRpi*i + kRpi-1
-    // in 16-byte chunks, each row's page id taken from the lane that owns it.
-    // A key past the piece gets zero V scales, so its stale V codes weigh 0.
+    // in 16-byte chunks.  A key past the piece gets zero V scales, so its
+    // stale V codes weigh 0.
     constexpr int kChunks = D / 32;      // 16-byte chunks per code row
     constexpr int kRpi = 32 / kChunks;   // code rows per warp instruction
     const int ps_mask = p.page_size - 1;
@@ -586,19 +586,22 @@ __global__ void __launch_bounds__(32 * kTWarps, NT == 1 ? 4 : 3)
         atomicOr(p.status, FI_DEV_PAGE_OOB);
         page = 0;
       }
+      // each half step (16 keys, 16-aligned) lies in one page: the cache row
+      // of its first key, from the page id of the lane that owns that key
+      const int64_t row_h0 = row_of(__shfl_sync(0xFFFFFFFFu, page, 0), kbs);
+      const int64_t row_h1 = row_of(__shfl_sync(0xFFFFFFFFu, page, 16), kbs + 16);
 #pragma unroll
       for (int i = 0; i < kChunks; ++i) {
         const int kr = kRpi * i + lane / kChunks;  // the step's row this lane copies
         const int ch = lane % kChunks;
-        const int pg = __shfl_sync(0xFFFFFFFFu, page, kr);
         if (kbs + kr < k1) {
-          const int64_t row = row_of(pg, kbs + kr);
+          const int64_t row = (kr < 16 ? row_h0 : row_h1) + (kr & 15);
           cp_async16(s + kr * (D / 2) + 16 * ch, p.k_data + row * (D / 2) + 16 * ch);
           cp_async16(s + kV + kr * kVR + 16 * ch, p.v_data + row * (D / 2) + 16 * ch);
         }
       }
       if (key < k1) {
-        const int64_t row = row_of(page, key);
+        const int64_t row = (lane < 16 ? row_h0 : row_h1) + (lane & 15);
         if constexpr (D == 128) {
           cp_async8(s + kKsf + lane * 8, p.k_sf + row * 8);
           cp_async8(s + kV + lane * kVR + 64, p.v_sf + row * 8);
@@ -680,6 +683,11 @@ __global__ void __launch_bounds__(32 * kTWarps, NT == 1 ? 4 : 3)
       // 32 keys every row sees (row 0 sees the fewest) takes no mask; rows past
       // R then run on zero logits, finite and never written out.
       const bool full = kb + 31 <= min(k1 - 1, delta);
+      // This lane's maximum of each row over its four keys; the row maximum
+      // (three shuffles) is taken only when some lane's exceeds the running
+      // maximum by more than 8, which the lazy rescale needs to move it.
+      float mxl[NT][2];
+      bool grow = false;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -702,19 +710,36 @@ __global__ void __launch_bounds__(32 * kTWarps, NT == 1 ? 4 : 3)
                 mx = fmaxf(mx, x);
               }
           }
-          mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
-          mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
-          mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
-          if (mx > mrun[nt][e] + 8.0f) {
-            const float alpha = ex2_approx(mrun[nt][e] - mx);  // 0 while mrun is -inf
-            lrun[nt][e] *= alpha;
+          mxl[nt][e] = mx;
+          grow |= mx > mrun[nt][e] + 8.0f;
+        }
+      }
+      if (__any_sync(0xFFFFFFFFu, grow)) {
 #pragma unroll
-            for (int i = 0; i < D / 16; ++i) {
-              o[i][nt][e] *= alpha;
-              o[i][nt][2 + e] *= alpha;
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float mx = mxl[nt][e];
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
+            if (mx > mrun[nt][e] + 8.0f) {
+              const float alpha = ex2_approx(mrun[nt][e] - mx);  // 0 while mrun is -inf
+              lrun[nt][e] *= alpha;
+#pragma unroll
+              for (int i = 0; i < D / 16; ++i) {
+                o[i][nt][e] *= alpha;
+                o[i][nt][2 + e] *= alpha;
+              }
+              mrun[nt][e] = mx;
             }
-            mrun[nt][e] = mx;
           }
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
           const float m = mrun[nt][e];
           float psum = 0.0f;
 #pragma unroll
