@@ -581,8 +581,9 @@ def measure(fi, name, device, steps, warmup, dist_on, kv_format="nvfp4", seqs=0)
                             "append_ms_b2b": app_ms, "attn_ms_b2b": att_ms}
 
 
-def attention_entry(runner, t, peaks):
-    """Per-launch numbers of the attention kernel of a measured workload."""
+def attention_entry(runner, t, peaks, traffic_key=None):
+    """Per-launch numbers of the attention kernel of a measured workload;
+    `traffic_key` names its recorded DRAM traffic (full-size workloads only)."""
     app_name, attn_name = kernel_names(runner)
     ms = t["attn_ms"]
     e = {"kernel": attn_name, "ms_per_launch": ms, "ms_per_launch_back_to_back": t["attn_ms_b2b"],
@@ -593,7 +594,8 @@ def attention_entry(runner, t, peaks):
     if runner.decode:
         gbs = runner.decode_bytes / (ms * 1e-3) / 1e9
         e.update({"bound": "hbm", "gbs": gbs, "algorithmic_bytes": runner.decode_bytes,
-                  "frac": gbs / peaks["hbm_gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s"})
+                  "frac": gbs / peaks["hbm_gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                  "traffic": recorded_traffic(traffic_key) if traffic_key else None})
     else:
         e.update({"bound": "tensor", "frac": e["tflops"] / peaks["bf16_tflops"],
                   "frac_of_sustained": e["tflops"] / peaks["bf16_tflops_sustained"],
@@ -662,12 +664,14 @@ def main():
     clk = clocks.stop()
     step_ms = max_over_ranks(t["step_ms"], dist_on, device)
     value = aggregate_value(runner.flops, step_ms, world)
-    head = attention_entry(runner, t, peaks)
+    head = attention_entry(runner, t, peaks,
+                           "decode_128x4096" if args.workload == "decode" and not args.seqs
+                           else None)
     full_uniform = args.workload == "uniform" and not args.seqs and not runner.fp8
     traffic = recorded_traffic("prefill_uniform") if full_uniform else None
     if runner.decode:
         roofline = {"bound": "hbm", "achieved": head["gbs"], "peak": peaks["hbm_gbs"],
-                    "unit": "GB/s", "frac": head["frac"], "traffic": None,
+                    "unit": "GB/s", "frac": head["frac"], "traffic": head["traffic"],
                     "kernel": head["kernel"], "algorithmic_bytes": runner.decode_bytes,
                     "ms_per_launch": head["ms_per_launch"],
                     "ms_per_launch_back_to_back": head["ms_per_launch_back_to_back"],
@@ -705,7 +709,8 @@ def main():
             c2.start()
             r2, s2, t2 = measure(fi, name, device, args.extra_steps, 3, dist_on, kv_format=fmt)
             ck = c2.stop()
-            e = attention_entry(r2, t2, peaks)
+            e = attention_entry(r2, t2, peaks,
+                                "decode_128x4096" if name == "decode" else None)
             e["workload"] = WORKLOAD_DESC[name] + (" [FP8 (E4M3) paged KV]" if fmt == "fp8" else "")
             e["steps"] = args.extra_steps
             e["clocks"] = {"sm_mhz": ck["sm_mhz"], "reasons": ck["reasons"]}

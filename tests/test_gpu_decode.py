@@ -72,6 +72,30 @@ def test_decode_splits_long_sequences_into_merged_pieces():
     assert_within_tolerance(res)
 
 
+def test_decode_repeated_runs_merge_every_time():
+    """Three runs of one plan with split pairs (output cleared in between, the
+    partial slots reused) must each match the oracle."""
+    m = fi()
+    d = device_inputs("decode_small")
+    sp = d["spec"]
+    ctx = m.fi_context_create()
+    c = gpu_cache(d)
+    m.fi_nvfp4_append(ctx, d["k"], d["v"], c.k_scale, c.v_scale, d["slot_mapping"], c)
+    plan = m.fi_plan_create(ctx)
+    m.fi_decode_plan(plan, d["host"]["qo_indptr"], d["host"]["kv_indptr"], d["page_table"],
+                     sp.num_qo_heads, sp.num_kv_heads, sp.head_dim, sp.page_size,
+                     sm_scale=d["sm_scale"])
+    ref_out, ref_lse = oracle_attention(d, oracle_cache(d))
+    for _ in range(3):
+        out = torch.full_like(d["q"], float("nan"))
+        lse = torch.full(d["q"].shape[:2], float("nan"), dtype=torch.float32, device="cuda")
+        m.fi_decode_run(plan, d["q"], c, out, lse)
+        assert m.fi_device_status(ctx) == 0
+        assert_within_tolerance(compare_attention(out, lse, ref_out, ref_lse))
+    m.fi_plan_destroy(plan)
+    m.fi_context_destroy(ctx)
+
+
 def test_decode_plan_limits_and_plan_kinds():
     m = fi()
     d = device_inputs("decode_small")
