@@ -194,31 +194,44 @@ __global__ void __launch_bounds__(32 * kDecWarps, MT == 1 ? 3 : 2)
         for (int e = 0; e < 4; ++e) o[mt][nd][e] = 0.0f;
     }
 
-    // Raw rows of key kbs + lane into ring stage st (one commit group per call,
-    // empty past the chunk).  The page id comes from the previous call, so the
-    // page-table read is one step ahead of the copies that need it.
+    // Raw rows of keys kbs .. kbs+31 into ring stage st (one commit group per
+    // call, empty past the piece).  Lane l owns key kbs + l: its page id (read
+    // one step before the copies that need it) and its scale rows; the code
+    // rows are copied by the whole warp, each instruction reading 512
+    // contiguous bytes of one page (as in the transposed form below).
+    constexpr int kChunks = D / 32;     // 16-byte chunks per code row
+    constexpr int kRpi = 32 / kChunks;  // code rows per warp instruction
     auto page_of = [&](int key) { return key < k1 ? __ldg(pt + (key >> p.ps_shift)) : 0; };
+    auto row_of = [&](int page, int key) {
+      return (static_cast<int64_t>(page) * p.num_kv_heads + hk) * p.page_size +
+             (key & (p.page_size - 1));
+    };
     int page_next = page_of(k0 + lane);
     auto issue = [&](int kbs, int st) {
       const int key = kbs + lane;
       int page = page_next;
       page_next = page_of(key + 32);
-      if (key < k1) {
-        if (page < 0 || page >= p.num_pages) {
-          atomicOr(p.status, FI_DEV_PAGE_OOB);
-          page = 0;
-        }
-        const int64_t row =
-            (static_cast<int64_t>(page) * p.num_kv_heads + hk) * p.page_size +
-            (key & (p.page_size - 1));
-        uint8_t* dst = raw + (st * 32 + lane) * kLR;
-        const uint8_t* kg = p.k_data + row * (D / 2);
-        const uint8_t* vg = p.v_data + row * (D / 2);
+      if (key < k1 && (page < 0 || page >= p.num_pages)) {
+        atomicOr(p.status, FI_DEV_PAGE_OOB);
+        page = 0;
+      }
+      // each half step (16 keys, 16-aligned) lies in one page
+      const int64_t row_h0 = row_of(__shfl_sync(0xFFFFFFFFu, page, 0), kbs);
+      const int64_t row_h1 = row_of(__shfl_sync(0xFFFFFFFFu, page, 16), kbs + 16);
 #pragma unroll
-        for (int i = 0; i < D / 32; ++i) {
-          cp_async16(dst + 16 * i, kg + 16 * i);
-          cp_async16(dst + D / 2 + 16 * i, vg + 16 * i);
+      for (int i = 0; i < kChunks; ++i) {
+        const int kr = kRpi * i + lane / kChunks;  // the step's row this lane copies
+        const int ch = lane % kChunks;
+        if (kbs + kr < k1) {
+          const int64_t row = (kr < 16 ? row_h0 : row_h1) + (kr & 15);
+          uint8_t* dst = raw + (st * 32 + kr) * kLR + 16 * ch;
+          cp_async16(dst, p.k_data + row * (D / 2) + 16 * ch);
+          cp_async16(dst + D / 2, p.v_data + row * (D / 2) + 16 * ch);
         }
+      }
+      if (key < k1) {
+        const int64_t row = (lane < 16 ? row_h0 : row_h1) + (lane & 15);
+        uint8_t* dst = raw + (st * 32 + lane) * kLR;
         if constexpr (D == 128) {
           cp_async8(dst + D, p.k_sf + row * (D / 16));
           cp_async8(dst + D + D / 16, p.v_sf + row * (D / 16));

@@ -122,6 +122,11 @@ def spec(name: str) -> Spec:
                     num_qo_heads=8, seq_lens=[3, 17, 33, 64, 5, 100, 31, 32, 2, 700, 9, 12, 40,
                                               1, 250, 48] * 2 + [3000], qo_lens=[1] * 33,
                     attn="decode")
+    # Pages of 128 tokens (one page holds four 32-key steps).
+    if name == "decode_ps128":
+        return Spec("decode_ps128", 13400, num_kv_heads=2, head_dim=128, page_size=128,
+                    num_qo_heads=8, seq_lens=[1, 129, 1000, 4100], qo_lens=[1, 1, 1, 1],
+                    attn="decode")
     if name == "uniform_small":
         return Spec("uniform_small", 7000, num_kv_heads=2, head_dim=128, page_size=16,
                     num_qo_heads=8, seq_lens=[384] * 6)
