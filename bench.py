@@ -2,7 +2,8 @@
 causal prefill, through the C ABI of libfi_nvfp4.so.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload uniform|single|ragged|decode] [--kv-format nvfp4|fp8]
+                    [--workload uniform|single|ragged|decode|decode_spec]
+                    [--kv-format nvfp4|fp8]
                     [--no-e2e] [--no-cpu-baseline] [--no-extra]
 
 One step is one pass of the whole path over one batch: fi_prefill_plan of the
@@ -16,8 +17,9 @@ prefill FLOPs of a step divided by the measured step time (TFLOP/s), timed over
 K steps with no event between the kernels; a second pass of K steps with
 events around each kernel gives the per-kernel times of `roofline` and
 `append_in_step`.  The same run also measures, each in its own timed passes,
-the single 2048 x 2048 prefill, the ragged batch, the 128 x 4096 decode and the
-FP8 (E4M3) variant of the uniform batch (`workloads`), and the 8192-token
+the single 2048 x 2048 prefill, the ragged batch, the 128 x 4096 decode (1 and
+8 query tokens per sequence) and the FP8 (E4M3) variant of the uniform batch
+(`workloads`), and the 8192-token
 append with cold L2 (`append_bench`: 24 rotating buffer sets captured in one
 CUDA graph).
 
@@ -61,6 +63,9 @@ WORKLOAD_DESC = {
               "H_kv=8, head_dim=128, page_size=16, append + plan + causal prefill",
     "decode": "decode batch: 128 sequences x kv_len 4096, qo_len 1, H_q=32, H_kv=8, "
               "head_dim=128, page_size=16, decode plan + append of the newest token + decode",
+    "decode_spec": "speculative decode batch: 128 sequences x kv_len 4096, qo_len 8 (32 rows "
+                   "per KV head), H_q=32, H_kv=8, head_dim=128, page_size=16, decode plan + "
+                   "append of the newest 8 tokens + decode",
 }
 
 # Oracle sample (both arms): sequences of the workload drawn with a fixed seed
@@ -544,12 +549,7 @@ def kernel_names(runner):
     else:
         # the library's switch to the staged kernel
         app = "nvfp4_append_staged_kernel" if runner.tokens >= 65536 else "nvfp4_append_kernel"
-    if runner.decode:
-        # the library's choice: the transposed form up to 16 rows per KV head
-        rows = runner.sp.num_qo_heads // runner.sp.num_kv_heads * max(runner.sp.qo_lens)
-        attn = "nvfp4_decode_t_kernel" if rows <= 16 else "nvfp4_decode_kernel"
-    else:
-        attn = "nvfp4_prefill_kernel"
+    attn = "nvfp4_decode_t_kernel" if runner.decode else "nvfp4_prefill_kernel"
     return app, attn
 
 
@@ -608,7 +608,8 @@ def attention_entry(runner, t, peaks, traffic_key=None):
 
 
 EXTRA = [("single", "single", "nvfp4"), ("ragged", "ragged", "nvfp4"),
-         ("decode", "decode", "nvfp4"), ("fp8_uniform", "uniform", "fp8")]
+         ("decode", "decode", "nvfp4"), ("decode_spec", "decode_spec", "nvfp4"),
+         ("fp8_uniform", "uniform", "fp8")]
 
 
 def main():
@@ -625,7 +626,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-append-bench", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
-                    help="skip the other workloads (single, ragged, decode, fp8)")
+                    help="skip the other workloads (single, ragged, decode, decode_spec, fp8)")
     ap.add_argument("--extra-steps", type=int, default=10)
     ap.add_argument("--seqs", type=int, default=0,
                     help="use only the first N sequences of the workload (profiling cases)")

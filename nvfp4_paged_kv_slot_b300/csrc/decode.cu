@@ -7,17 +7,17 @@
 // j <= t + kv_len - qo_len).
 //
 // Decode rows are few (G * qo_len per KV head) and every key is read once, so
-// the work is HBM-bound.  One warp owns one unit = (sequence, KV head, chunk
-// of keys) and takes its keys 32 at a time: each lane copies its own key's
-// raw K and V rows (codes and block scales) into a two-step ring in shared
-// memory two steps ahead (cp.async) and dequantizes its V row into an exact
-// fp16 row (E2M1 x E4M3 fits fp16); the warp computes S = Q K^T with K's MMA
-// fragments converted straight from the raw codes in the ring, and O += P V
-// from the staged V rows, with m16n8k16 warp-level MMAs (fp16 in, fp32
-// accumulators; Q in registers, scaled by a power of two into fp16 range),
-// the online softmax running on the accumulator fragments.  A sequence whose keys span several chunks writes
-// unnormalized partial results (row max, row sum, O) that a merge kernel
-// combines.
+// the work is HBM-bound and runs on warp-level m16n8k16 MMAs (fp16 in, fp32
+// accumulators) fed straight from the raw NVFP4 rows, with the rows on the
+// MMA's n side (below).  The keys of all (sequence, KV head) pairs are split
+// evenly over the resident warps in steps of 32; a warp runs its pieces one
+// after another, copying each step's raw K and V rows (codes and block
+// scales) into a two-stage ring in shared memory one step ahead (cp.async),
+// converting its MMA fragments from the raw codes (E2M1 x E4M3 is exact in
+// fp16) and running the online softmax on the accumulator fragments.  A pair
+// split over several warps writes unnormalized partials (O, row max, row
+// sum) per piece, which a second kernel merges.
+
 #include <algorithm>
 
 #include "internal.h"
@@ -26,9 +26,6 @@
 namespace fi {
 
 namespace {
-
-constexpr int kDecWarps = 4;   // warps per CTA
-constexpr int kDecStages = 2;  // raw rows in flight per warp: this step's and the next
 
 struct DecodeParams {
   const __nv_bfloat16* q;
@@ -62,8 +59,7 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 // m16n8k16 MMA with fp16 inputs and fp32 accumulators (the warp-level tensor
-// core path: decode is HBM-bound, so its rate is ample), and the 8x8
-// shared-memory matrix loads that feed it.
+// core path: decode is HBM-bound, so its rate is ample).
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
   asm volatile(
@@ -72,375 +68,18 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
 __device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Bytes of one staged V row (fp16), padded so that the eight rows of an 8x8
-// matrix load fall on distinct banks.
-template <int D>
-constexpr int kRowStride = D * 2 + 16;
-// Bytes of one lane's raw rows in the ring: K codes, V codes, K scales, V
-// scales (D/2, D/2, D/16, D/16), padded to a multiple of 16.
-template <int D>
-constexpr int kLaneRaw = (D + D / 8 + 15) / 16 * 16;
-template <int D>
-constexpr int decode_smem_bytes() {
-  return kDecWarps * (32 * kRowStride<D> + kDecStages * 32 * kLaneRaw<D>);
-}
-
-// MT: 16-row MMA tiles per unit (rows G * qo_len <= 16 MT).
-template <int D, int MT>
-__global__ void __launch_bounds__(32 * kDecWarps, MT == 1 ? 3 : 2)
-    nvfp4_decode_kernel(const DecodeParams p) {
-  constexpr int kS = kRowStride<D>;
-  constexpr int kLR = kLaneRaw<D>;
-  extern __shared__ __align__(16) uint8_t dsm[];
-  grid_dep_wait();  // Q and the cache may come from the previous grid
-  grid_dep_launch();
-  const int warp = threadIdx.x / 32;
-  const int lane = threadIdx.x % 32;
-  const int wid = blockIdx.x * kDecWarps + warp;
-  if (wid >= p.num_warps) return;  // no block-wide barrier below
-  const int u_end = __ldg(p.warp_off + wid + 1);
-  for (int u = __ldg(p.warp_off + wid); u < u_end; ++u) {
-    __syncwarp();  // every lane is done with the previous piece's ring
-    const int4 w = __ldg(p.units + u);
-    const int b = w.x / p.num_kv_heads, hk = w.x - b * p.num_kv_heads, slot = w.w;
-    const int qo_start = __ldg(p.qo_indptr + b);
-    const int qo_len = __ldg(p.qo_indptr + b + 1) - qo_start;
-    const int kv_len = __ldg(p.kv_indptr + b + 1) - __ldg(p.kv_indptr + b);
-    const int G = p.group;
-    const int R = G * qo_len;  // <= 16 MT (the planner guarantees it)
-    const int delta = kv_len - qo_len;
-    const int k0 = w.y;  // the piece's keys: k0 .. k1 - 1
-    const int k1 = w.z;
-    const float ks = __ldg(p.k_scale), vs = __ldg(p.v_scale);
-    uint8_t* sv = dsm + warp * 32 * kS;  // this warp's 32 staged V rows
-    const uint32_t sv_addr = smem_u32(sv);
-    // this warp's raw ring: stage st, key (lane) l at (st * 32 + l) * kLR
-    uint8_t* raw = dsm + kDecWarps * 32 * kS + warp * kDecStages * 32 * kLR;
-    const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.pt_stride;
-    auto q_ptr = [&](int r) {  // row r = token r / G, head hk * G + r % G
-      return p.q + (static_cast<int64_t>(qo_start + r / G) * p.num_qo_heads + hk * G + r % G) * D;
-    };
-
-    // Q as fp16 A fragments: Q * sm_scale * k_scale * log2 e * 2^-e with e
-    // chosen so that every |value| < 2^14 (a power of two: exact); the logits
-    // are multiplied back by 2^e.
-    const float qs = p.sm_scale * ks * 1.4426950408889634f;
-    float qmax = 0.0f;
-    for (int i = lane; i < R * (D / 8); i += 32) {
-      float x[8];
-      bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(q_ptr(i / (D / 8)) + (i % (D / 8)) * 8)), x);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) qmax = fmaxf(qmax, fabsf(x[e]));
-    }
-    qmax = warp_max(qmax) * qs;
-    const int qe = qmax > 0.0f ? ilogbf(qmax) - 13 : 0;
-    const float qsc = ldexpf(qs, -qe);
-    const float ssc = ldexpf(1.0f, qe);
-    uint32_t qa[MT][D / 16][4];
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      const int r0 = 16 * mt + lane / 4, r1 = r0 + 8;
-#pragma unroll
-      for (int s = 0; s < D / 16; ++s) {
-        const int d0 = 16 * s + 2 * (lane % 4);
-        float v[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) v[k] = 0.0f;
-        if (r0 < R) {
-          const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(q_ptr(r0) + d0);
-          const __nv_bfloat162 bb = *reinterpret_cast<const __nv_bfloat162*>(q_ptr(r0) + d0 + 8);
-          v[0] = __low2float(a) * qsc;
-          v[1] = __high2float(a) * qsc;
-          v[4] = __low2float(bb) * qsc;
-          v[5] = __high2float(bb) * qsc;
-        }
-        if (r1 < R) {
-          const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(q_ptr(r1) + d0);
-          const __nv_bfloat162 bb = *reinterpret_cast<const __nv_bfloat162*>(q_ptr(r1) + d0 + 8);
-          v[2] = __low2float(a) * qsc;
-          v[3] = __high2float(a) * qsc;
-          v[6] = __low2float(bb) * qsc;
-          v[7] = __high2float(bb) * qsc;
-        }
-        qa[mt][s][0] = f16x2_of(v[0], v[1]);
-        qa[mt][s][1] = f16x2_of(v[2], v[3]);
-        qa[mt][s][2] = f16x2_of(v[4], v[5]);
-        qa[mt][s][3] = f16x2_of(v[6], v[7]);
-      }
-    }
-
-    float o[MT][D / 8][4];
-    float mrow[MT][2], lrow[MT][2];
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        mrow[mt][h] = -INFINITY;
-        lrow[mt][h] = 0.0f;
-      }
-#pragma unroll
-      for (int nd = 0; nd < D / 8; ++nd)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o[mt][nd][e] = 0.0f;
-    }
-
-    // Raw rows of keys kbs .. kbs+31 into ring stage st (one commit group per
-    // call, empty past the piece).  Lane l owns key kbs + l: its page id (read
-    // one step before the copies that need it) and its scale rows; the code
-    // rows are copied by the whole warp, each instruction reading 512
-    // contiguous bytes of one page (as in the transposed form below).
-    constexpr int kChunks = D / 32;     // 16-byte chunks per code row
-    constexpr int kRpi = 32 / kChunks;  // code rows per warp instruction
-    auto page_of = [&](int key) { return key < k1 ? __ldg(pt + (key >> p.ps_shift)) : 0; };
-    auto row_of = [&](int page, int key) {
-      return (static_cast<int64_t>(page) * p.num_kv_heads + hk) * p.page_size +
-             (key & (p.page_size - 1));
-    };
-    int page_next = page_of(k0 + lane);
-    auto issue = [&](int kbs, int st) {
-      const int key = kbs + lane;
-      int page = page_next;
-      page_next = page_of(key + 32);
-      if (key < k1 && (page < 0 || page >= p.num_pages)) {
-        atomicOr(p.status, FI_DEV_PAGE_OOB);
-        page = 0;
-      }
-      // each half step (16 keys, 16-aligned) lies in one page
-      const int64_t row_h0 = row_of(__shfl_sync(0xFFFFFFFFu, page, 0), kbs);
-      const int64_t row_h1 = row_of(__shfl_sync(0xFFFFFFFFu, page, 16), kbs + 16);
-#pragma unroll
-      for (int i = 0; i < kChunks; ++i) {
-        const int kr = kRpi * i + lane / kChunks;  // the step's row this lane copies
-        const int ch = lane % kChunks;
-        if (kbs + kr < k1) {
-          const int64_t row = (kr < 16 ? row_h0 : row_h1) + (kr & 15);
-          uint8_t* dst = raw + (st * 32 + kr) * kLR + 16 * ch;
-          cp_async16(dst, p.k_data + row * (D / 2) + 16 * ch);
-          cp_async16(dst + D / 2, p.v_data + row * (D / 2) + 16 * ch);
-        }
-      }
-      if (key < k1) {
-        const int64_t row = (lane < 16 ? row_h0 : row_h1) + (lane & 15);
-        uint8_t* dst = raw + (st * 32 + lane) * kLR;
-        if constexpr (D == 128) {
-          cp_async8(dst + D, p.k_sf + row * (D / 16));
-          cp_async8(dst + D + D / 16, p.v_sf + row * (D / 16));
-        } else {
-          cp_async4(dst + D, p.k_sf + row * (D / 16));
-          cp_async4(dst + D + D / 16, p.v_sf + row * (D / 16));
-        }
-      }
-      cp_async_commit();
-    };
-    issue(k0, 0);
-    issue(k0 + 32, 1);
-
-    int st = 0;
-    for (int kb = k0; kb < k1; kb += 32, st ^= 1) {
-      // ---- stage this lane's key: its V row as exact fp16 (zeros past k1)
-      cp_async_wait<1>();  // this lane's raw rows of this step have landed
-      __syncwarp();        // ... and every lane's; the previous batch's V rows have been read
-      {
-        uint4* dv = reinterpret_cast<uint4*>(sv + lane * kS);
-        const int key = kb + lane;
-        if (key < k1) {
-          const uint8_t* src = raw + (st * 32 + lane) * kLR;
-          uint4 vc4[D / 32];
-          uint32_t vsf4[D / 64];
-#pragma unroll
-          for (int i = 0; i < D / 32; ++i) vc4[i] = reinterpret_cast<const uint4*>(src + D / 2)[i];
-#pragma unroll
-          for (int i = 0; i < D / 64; ++i)
-            vsf4[i] = reinterpret_cast<const uint32_t*>(src + D + D / 16)[i];
-          const uint32_t* vc = reinterpret_cast<const uint32_t*>(vc4);
-#pragma unroll
-          for (int blk = 0; blk < D / 16; ++blk) {
-            const uint32_t s8v = (vsf4[blk / 4] >> (8 * (blk % 4))) & 0xFFu;
-            dv[2 * blk] = dequant8_f16(vc[2 * blk], s8v);
-            dv[2 * blk + 1] = dequant8_f16(vc[2 * blk + 1], s8v);
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < D / 8; ++i) dv[i] = make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
-
-      // ---- S = Q K^T for the 32 keys (4 n-tiles of 8 keys, D/16 k-steps).  The
-      // B fragment of n-tile j, k-step t (dims 16t .. 16t+15 = scale block t)
-      // holds, in lane l, key 8j + l/4 at dims 16t + 2(l%4) + {0, 1} and
-      // {8, 9} more: byte l%4 of code words 4(t/2) + 2(t%2) and the word after
-      // it of that key's raw row, times the block's scale.  Keys past k1 read
-      // stale ring bytes; their logits are replaced by -inf below.
-      float sacc[MT][4][4];
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) sacc[mt][j][e] = 0.0f;
-      const uint32_t bsel = static_cast<uint32_t>(lane % 4) | ((4u + static_cast<uint32_t>(lane % 4)) << 4);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint8_t* kr = raw + (st * 32 + 8 * j + lane / 4) * kLR;
-        uint32_t kw[D / 8];
-#pragma unroll
-        for (int i = 0; i < D / 32; ++i) {
-          const uint4 w4 = reinterpret_cast<const uint4*>(kr)[i];
-          kw[4 * i] = w4.x;
-          kw[4 * i + 1] = w4.y;
-          kw[4 * i + 2] = w4.z;
-          kw[4 * i + 3] = w4.w;
-        }
-        uint32_t ksf[D / 64];
-#pragma unroll
-        for (int i = 0; i < D / 64; ++i) ksf[i] = reinterpret_cast<const uint32_t*>(kr + D)[i];
-#pragma unroll
-        for (int s2 = 0; s2 < D / 32; ++s2) {
-          // bytes for k-steps 2 s2 (b0, b1) and 2 s2 + 1 (b0, b1), in that order
-          const uint32_t lo = __byte_perm(kw[4 * s2], kw[4 * s2 + 1], bsel);
-          const uint32_t hi = __byte_perm(kw[4 * s2 + 2], kw[4 * s2 + 3], bsel);
-          uint32_t h[4];
-          e2m1x8_to_f16x2(__byte_perm(lo, hi, 0x5410), h);
-          const uint32_t sa = e4m3_to_f16x2_dup(ksf[s2 / 2] >> (16 * (s2 % 2)));
-          const uint32_t sb = e4m3_to_f16x2_dup(ksf[s2 / 2] >> (16 * (s2 % 2) + 8));
-          const uint32_t b0a = hmul2_u32(h[0], sa), b1a = hmul2_u32(h[1], sa);
-          const uint32_t b0b = hmul2_u32(h[2], sb), b1b = hmul2_u32(h[3], sb);
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            mma16816(sacc[mt][j], qa[mt][2 * s2], b0a, b1a);
-            mma16816(sacc[mt][j], qa[mt][2 * s2 + 1], b0b, b1b);
-          }
-        }
-      }
-      __syncwarp();  // every lane has read this stage's raw rows; V rows are staged
-      // the raw stage just read takes the rows of the step after next
-      issue(kb + 64, st);
-
-      // ---- causal mask and online softmax; rows r0 = 16 mt + lane/4 (h = 0)
-      // and r0 + 8 (h = 1), keys kb + 8j + 2(lane%4) + e
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int r = 16 * mt + lane / 4 + 8 * h;
-          const int lim = r < R ? min(k1 - 1, delta + r / G) : -1;  // last visible key
-          float mx = -INFINITY;
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int key = kb + 8 * j + 2 * (lane % 4) + e;
-              const float x = key <= lim ? sacc[mt][j][2 * h + e] * ssc : -INFINITY;
-              sacc[mt][j][2 * h + e] = x;
-              mx = fmaxf(mx, x);
-            }
-          mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-          mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
-          const float m_new = fmaxf(mrow[mt][h], mx);
-          const float alpha = m_new == -INFINITY ? 1.0f : ex2_approx(mrow[mt][h] - m_new);
-          float psum = 0.0f;
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float x = sacc[mt][j][2 * h + e];
-              const float pv = x == -INFINITY ? 0.0f : ex2_approx(x - m_new);
-              sacc[mt][j][2 * h + e] = pv;
-              psum += pv;
-            }
-          lrow[mt][h] = lrow[mt][h] * alpha + psum;
-          mrow[mt][h] = m_new;
-#pragma unroll
-          for (int nd = 0; nd < D / 8; ++nd) {
-            o[mt][nd][2 * h] *= alpha;
-            o[mt][nd][2 * h + 1] *= alpha;
-          }
-        }
-      }
-
-      // ---- O += P V (k-steps of 16 keys, n-tiles of 8 columns)
-#pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        uint32_t pa[MT][4];
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          pa[mt][0] = f16x2_of(sacc[mt][2 * kk][0], sacc[mt][2 * kk][1]);
-          pa[mt][1] = f16x2_of(sacc[mt][2 * kk][2], sacc[mt][2 * kk][3]);
-          pa[mt][2] = f16x2_of(sacc[mt][2 * kk + 1][0], sacc[mt][2 * kk + 1][1]);
-          pa[mt][3] = f16x2_of(sacc[mt][2 * kk + 1][2], sacc[mt][2 * kk + 1][3]);
-        }
-#pragma unroll
-        for (int nd2 = 0; nd2 < D / 16; ++nd2) {
-          uint32_t bv[4];  // n-tiles 2 nd2 and 2 nd2 + 1, keys 16 kk .. 16 kk + 15
-          const int m = lane / 8;
-          ldsm_x4_t(sv_addr + (16 * kk + 8 * (m & 1) + lane % 8) * kS + (16 * nd2 + 8 * (m >> 1)) * 2,
-                    bv);
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            mma16816(o[mt][2 * nd2], pa[mt], bv[0], bv[1]);
-            mma16816(o[mt][2 * nd2 + 1], pa[mt], bv[2], bv[3]);
-          }
-        }
-      }
-    }
-
-    cp_async_wait<0>();  // (every copy was consumed; nothing is left in flight)
-
-    // ---- results: the whole sequence in this unit, or a partial slot
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float lsum = lrow[mt][h];
-        lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 1);
-        lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 2);
-        const int r = 16 * mt + lane / 4 + 8 * h;
-        if (r >= R) continue;
-        const int col = 2 * (lane % 4);
-        if (slot < 0) {
-          const int64_t orow =
-              static_cast<int64_t>(qo_start + r / G) * p.num_qo_heads + hk * G + r % G;
-          const float inv = vs / lsum;
-          __nv_bfloat16* dst = p.out + orow * D + col;
-#pragma unroll
-          for (int nd = 0; nd < D / 8; ++nd)
-            *reinterpret_cast<__nv_bfloat162*>(dst + 8 * nd) =
-                __floats2bfloat162_rn(o[mt][nd][2 * h] * inv, o[mt][nd][2 * h + 1] * inv);
-          if (p.lse && lane % 4 == 0)
-            p.lse[orow] = (mrow[mt][h] + log2f(lsum)) * 0.6931471805599453f;
-        } else {
-          float* dst = p.part + (static_cast<int64_t>(slot) * p.rows + r) * (D + 2);
-#pragma unroll
-          for (int nd = 0; nd < D / 8; ++nd) {
-            dst[8 * nd + col] = o[mt][nd][2 * h];
-            dst[8 * nd + col + 1] = o[mt][nd][2 * h + 1];
-          }
-          if (lane % 4 == 0) {
-            dst[D] = mrow[mt][h];
-            dst[D + 1] = lsum;
-          }
-        }
-      }
-    }
-  }
-}
-
-// ---- transposed form, for up to 16 rows per unit -------------------------
+// ---- the decode kernel: rows on the MMA's n side ------------------------
 // With few rows the row dimension is better placed on the MMA's n side (8
 // rows per n-tile) than on its 16-row m side: S^T = K Q^T takes keys as m,
-// O^T = V^T P^T takes head dimensions as m.  That halves the MMAs and the
-// accumulators of the form above, and both K and V fragments come straight
-// from the raw codes, so no dequantized copy of V is staged.
+// O^T = V^T P^T takes head dimensions as m.  With up to 8 rows that halves
+// the MMAs and the accumulators of the row-major form (S = Q K^T, O += P V),
+// and both K and V fragments come straight from the raw codes, so no
+// dequantized copy of V is staged.
 //
 // The contraction index of each MMA may be permuted freely as long as both
 // operands agree, and the m index of O^T may be permuted as long as the
@@ -465,19 +104,19 @@ __global__ void __launch_bounds__(32 * kDecWarps, MT == 1 ? 3 : 2)
 constexpr int kTWarps = 4;   // warps per CTA
 constexpr int kTStages = 2;  // raw stages per warp: this step's and the next
 
-// The planner sizes the warp count to what is resident per SM: 4 CTAs (up to
-// 8 rows) or 3 (up to 16) of this form, 2 of the form above (above 16 rows).
+// The planner sizes the warp count to what is resident per SM: 4 CTAs up to
+// 8 rows, 3 up to 16, 2 up to 32 (the launch bounds below).
 static_assert(kTWarps * 4 == decode_warps_per_sm(8) && kTWarps * 3 == decode_warps_per_sm(16) &&
-                  kDecWarps * 2 == decode_warps_per_sm(32),
+                  kTWarps * 2 == decode_warps_per_sm(32),
               "decode occupancy and plan disagree");
 
 template <int D>
 constexpr int kTVRow = D == 128 ? 80 : 48;
 template <int D>
 constexpr int kTStage = 32 * (D / 2 + D / 16 + kTVRow<D>);
-template <int D>
+template <int D, int NT>
 constexpr int decode_t_smem_bytes() {
-  return kTWarps * kTStages * kTStage<D>;
+  return kTWarps * (kTStages * kTStage<D> + (NT == 4 ? NT * (D / 16) * 32 * 8 : 0));
 }
 
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
@@ -488,7 +127,7 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
 
 // NT: 8-row n-tiles per unit (rows G * qo_len <= 8 NT).
 template <int D, int NT>
-__global__ void __launch_bounds__(32 * kTWarps, NT == 1 ? 4 : 3)
+__global__ void __launch_bounds__(32 * kTWarps, NT == 1 ? 4 : NT == 2 ? 3 : 2)
     nvfp4_decode_t_kernel(const DecodeParams p) {
   constexpr int kStage = kTStage<D>;
   constexpr int kVR = kTVRow<D>;
@@ -496,6 +135,7 @@ __global__ void __launch_bounds__(32 * kTWarps, NT == 1 ? 4 : 3)
   constexpr int kV = 32 * (D / 2 + D / 16);  // V rows within a stage
   constexpr int kKW = D / 32;                // code words of a key a lane converts for S^T
   constexpr int kVW = D / 64;                // code words of a key a lane converts for O^T
+  constexpr bool kQs = NT == 4;              // Q^T fragments in shared memory
   extern __shared__ __align__(16) uint8_t dsm[];
   grid_dep_wait();  // Q and the cache may come from the previous grid
   grid_dep_launch();
@@ -519,18 +159,22 @@ __global__ void __launch_bounds__(32 * kTWarps, NT == 1 ? 4 : 3)
     const int k1 = w.z;
     const float ks = __ldg(p.k_scale), vs = __ldg(p.v_scale);
     uint8_t* ring = dsm + warp * kTStages * kStage;
+    uint2* qsm = reinterpret_cast<uint2*>(dsm + kTWarps * kTStages * kStage) +
+                 warp * (kQs ? NT * (D / 16) * 32 : 0);
     const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.pt_stride;
     auto q_ptr = [&](int r) {  // row r = token r / G, head hk * G + r % G
       return p.q + (static_cast<int64_t>(qo_start + r / G) * p.num_qo_heads + hk * G + r % G) * D;
     };
 
-    // Q^T as fp16 B fragments, scaled as in the form above (a power of two
-    // brings every |value| below 2^14; the logits are multiplied back).
+    // Q^T as fp16 B fragments: Q * sm_scale * k_scale * log2 e * 2^-e with e
+    // chosen so that every |value| < 2^14 (a power of two: exact); the logits
+    // are multiplied back by 2^e.
     const float qs = p.sm_scale * ks * 1.4426950408889634f;
     float qmax = 0.0f;
     for (int i = lane; i < R * (D / 8); i += 32) {
       float x[8];
-      bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(q_ptr(i / (D / 8)) + (i % (D / 8)) * 8)), x);
+      bf16x8_to_f32(
+          __ldg(reinterpret_cast<const uint4*>(q_ptr(i / (D / 8)) + (i % (D / 8)) * 8)), x);
 #pragma unroll
       for (int e = 0; e < 8; ++e) qmax = fmaxf(qmax, fabsf(x[e]));
     }
@@ -538,6 +182,9 @@ __global__ void __launch_bounds__(32 * kTWarps, NT == 1 ? 4 : 3)
     const int qe = qmax > 0.0f ? ilogbf(qmax) - 13 : 0;
     const float qsc = ldexpf(qs, -qe);
     const float ssc = ldexpf(1.0f, qe);
+    // With 4 n-tiles the fragments live in shared memory (this warp's slice,
+    // fragment (nt, k-step s) of lane l at [nt][s][l]: conflict-free 8-byte
+    // reads), which keeps the kernel within its registers; else in registers.
     uint32_t qb[NT][D / 16][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -549,12 +196,28 @@ __global__ void __launch_bounds__(32 * kTWarps, NT == 1 ? 4 : 3)
         for (int e = 0; e < 8; ++e) x[e] = 0.0f;
         if (r < R)
           bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(q_ptr(r) + t * (D / 4)) + i), x);
-        qb[nt][2 * i][0] = f16x2_of(x[0] * qsc, x[1] * qsc);
-        qb[nt][2 * i][1] = f16x2_of(x[2] * qsc, x[3] * qsc);
-        qb[nt][2 * i + 1][0] = f16x2_of(x[4] * qsc, x[5] * qsc);
-        qb[nt][2 * i + 1][1] = f16x2_of(x[6] * qsc, x[7] * qsc);
+        const uint2 f0 =
+            make_uint2(f16x2_of(x[0] * qsc, x[1] * qsc), f16x2_of(x[2] * qsc, x[3] * qsc));
+        const uint2 f1 =
+            make_uint2(f16x2_of(x[4] * qsc, x[5] * qsc), f16x2_of(x[6] * qsc, x[7] * qsc));
+        if constexpr (kQs) {
+          qsm[(nt * (D / 16) + 2 * i) * 32 + lane] = f0;
+          qsm[(nt * (D / 16) + 2 * i + 1) * 32 + lane] = f1;
+        } else {
+          qb[nt][2 * i][0] = f0.x;
+          qb[nt][2 * i][1] = f0.y;
+          qb[nt][2 * i + 1][0] = f1.x;
+          qb[nt][2 * i + 1][1] = f1.y;
+        }
       }
     }
+    if constexpr (kQs) __syncwarp();  // every lane's fragments are stored
+    auto qfrag = [&](int nt, int ks) {
+      if constexpr (kQs)
+        return qsm[(nt * (D / 16) + ks) * 32 + lane];
+      else
+        return make_uint2(qb[nt][ks][0], qb[nt][ks][1]);
+    };
 
     // O^T accumulators (m-tile i, n-tile nt), and per lane the running max and
     // sum of rows 8 nt + 2t + e.  The max is raised lazily: only when a step's
@@ -642,51 +305,98 @@ __global__ void __launch_bounds__(32 * kTWarps, NT == 1 ? 4 : 3)
       const uint8_t* sb = ring + st * kStage;
 
       // ---- S^T = K Q^T: m-tiles of keys 0-15 and 16-31.  Keys past k1 read
-      // stale bytes; their logits are replaced by -inf below.
+      // stale bytes; their logits are replaced by -inf below.  A lane converts
+      // its code words of keys g, g+8 (m-tile 0) and 16+g, 24+g (m-tile 1).
       float sacc[2][NT][4];
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
+      for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) sacc[mt][nt][e] = 0.0f;
-        const int ka = 16 * mt + g, kz = ka + 8;
-        uint32_t ca[kKW], cz[kKW];
-        uint32_t sfa, sfz;
+      // code words and scale bytes of key 16 mt + 8 z + g
+      auto load_k = [&](int mt, int z, uint32_t (&cw)[kKW], uint32_t& sf) {
+        const int key = 16 * mt + 8 * z + g;
         if constexpr (D == 128) {
-          const uint4 xa = *reinterpret_cast<const uint4*>(sb + ka * 64 + 16 * t);
-          const uint4 xz = *reinterpret_cast<const uint4*>(sb + kz * 64 + 16 * t);
-          ca[0] = xa.x; ca[1] = xa.y; ca[2] = xa.z; ca[3] = xa.w;
-          cz[0] = xz.x; cz[1] = xz.y; cz[2] = xz.z; cz[3] = xz.w;
-          sfa = *reinterpret_cast<const uint16_t*>(sb + kKsf + ka * 8 + 2 * t);
-          sfz = *reinterpret_cast<const uint16_t*>(sb + kKsf + kz * 8 + 2 * t);
+          const uint4 x = *reinterpret_cast<const uint4*>(sb + key * 64 + 16 * t);
+          cw[0] = x.x;
+          cw[1] = x.y;
+          cw[2] = x.z;
+          cw[3] = x.w;
+          sf = *reinterpret_cast<const uint16_t*>(sb + kKsf + key * 8 + 2 * t);
         } else {
-          const uint2 xa = *reinterpret_cast<const uint2*>(sb + ka * 32 + 8 * t);
-          const uint2 xz = *reinterpret_cast<const uint2*>(sb + kz * 32 + 8 * t);
-          ca[0] = xa.x; ca[1] = xa.y;
-          cz[0] = xz.x; cz[1] = xz.y;
-          sfa = sb[kKsf + ka * 4 + t];
-          sfz = sb[kKsf + kz * 4 + t];
+          const uint2 x = *reinterpret_cast<const uint2*>(sb + key * 32 + 8 * t);
+          cw[0] = x.x;
+          cw[1] = x.y;
+          sf = sb[kKsf + key * 4 + t];
         }
+      };
+      // code word i holds bytes 4i .. 4i+3 of the lane's range = k-steps 2i and
+      // 2i+1; its scale block is the lane's first (bytes 0-7) or second (8-15)
+      auto kscale = [&](uint32_t sf, int i) {
+        return e4m3x2_to_f16x2(__byte_perm(sf, 0u, i / 2 ? 0x1111u : 0x0000u));
+      };
+      if constexpr (kQs) {
+        // Q fragments from shared memory: each is read once and used for both
+        // m-tiles, so the words of all four keys are converted together
+        uint32_t cw[2][2][kKW], sfb[2][2];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int z = 0; z < 2; ++z) load_k(mt, z, cw[mt][z], sfb[mt][z]);
 #pragma unroll
         for (int i = 0; i < kKW; ++i) {
-          // code word i: bytes 4i .. 4i+3 of the lane's range = k-steps 2i, 2i+1;
-          // its scale block is the lane's first (bytes 0-7) or second (8-15)
-          const uint32_t sa = e4m3x2_to_f16x2(__byte_perm(sfa, 0u, i / 2 ? 0x1111u : 0x0000u));
-          const uint32_t sz = e4m3x2_to_f16x2(__byte_perm(sfz, 0u, i / 2 ? 0x1111u : 0x0000u));
-          uint32_t ha[4], hz[4];
-          e2m1x8_to_f16x2(ca[i], ha);
-          e2m1x8_to_f16x2(cz[i], hz);
+          uint32_t hc[2][2][4], sc[2][2];
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int z = 0; z < 2; ++z) {
+              sc[mt][z] = kscale(sfb[mt][z], i);
+              e2m1x8_to_f16x2(cw[mt][z][i], hc[mt][z]);
+            }
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            uint32_t a[4];
-            a[0] = hmul2_u32(ha[2 * h], sa);
-            a[1] = hmul2_u32(hz[2 * h], sz);
-            a[2] = hmul2_u32(ha[2 * h + 1], sa);
-            a[3] = hmul2_u32(hz[2 * h + 1], sz);
+            uint32_t a[2][4];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-              mma16816(sacc[mt][nt], a, qb[nt][2 * i + h][0], qb[nt][2 * i + h][1]);
+            for (int mt = 0; mt < 2; ++mt) {
+              a[mt][0] = hmul2_u32(hc[mt][0][2 * h], sc[mt][0]);
+              a[mt][1] = hmul2_u32(hc[mt][1][2 * h], sc[mt][1]);
+              a[mt][2] = hmul2_u32(hc[mt][0][2 * h + 1], sc[mt][0]);
+              a[mt][3] = hmul2_u32(hc[mt][1][2 * h + 1], sc[mt][1]);
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              const uint2 q = qfrag(nt, 2 * i + h);
+              mma16816(sacc[0][nt], a[0], q.x, q.y);
+              mma16816(sacc[1][nt], a[1], q.x, q.y);
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          uint32_t ca[kKW], cz[kKW], sfa, sfz;
+          load_k(mt, 0, ca, sfa);
+          load_k(mt, 1, cz, sfz);
+#pragma unroll
+          for (int i = 0; i < kKW; ++i) {
+            const uint32_t sa = kscale(sfa, i), sz = kscale(sfz, i);
+            uint32_t ha[4], hz[4];
+            e2m1x8_to_f16x2(ca[i], ha);
+            e2m1x8_to_f16x2(cz[i], hz);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint32_t a[4];
+              a[0] = hmul2_u32(ha[2 * h], sa);
+              a[1] = hmul2_u32(hz[2 * h], sz);
+              a[2] = hmul2_u32(ha[2 * h + 1], sa);
+              a[3] = hmul2_u32(hz[2 * h + 1], sz);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                const uint2 q = qfrag(nt, 2 * i + h);
+                mma16816(sacc[mt][nt], a, q.x, q.y);
+              }
+            }
           }
         }
       }
@@ -923,24 +633,9 @@ __global__ void __launch_bounds__(128) nvfp4_decode_merge_kernel(const DecodePar
   if (p.lse && lane == 0) p.lse[orow] = (M + log2f(L)) * 0.6931471805599453f;
 }
 
-template <int D, int MT>
-fi_status launch_decode_impl(const DecodeParams& p, cudaStream_t stream) {
-  const int smem = decode_smem_bytes<D>();
-  auto kern = nvfp4_decode_kernel<D, MT>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-      cudaSuccess)
-    return FI_ERR_CUDA;
-  const unsigned grid = static_cast<unsigned>((p.num_warps + kDecWarps - 1) / kDecWarps);
-  fi_status st = launch_pdl(kern, dim3(grid), dim3(32 * kDecWarps), smem, stream, p);
-  if (st != FI_OK || p.num_merges == 0) return st;
-  const int64_t warps = static_cast<int64_t>(p.num_merges) * p.rows;
-  const unsigned mgrid = static_cast<unsigned>((warps + 3) / 4);
-  return launch_pdl(nvfp4_decode_merge_kernel<D>, dim3(mgrid), dim3(128), 0, stream, p);
-}
-
 template <int D, int NT>
 fi_status launch_decode_t_impl(const DecodeParams& p, cudaStream_t stream) {
-  const int smem = decode_t_smem_bytes<D>();
+  const int smem = decode_t_smem_bytes<D, NT>();
   auto kern = nvfp4_decode_t_kernel<D, NT>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
@@ -996,7 +691,8 @@ fi_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (P.dec_rows <= 16)
     return D == 128 ? launch_decode_t_impl<128, 2>(p, stream)
                     : launch_decode_t_impl<64, 2>(p, stream);
-  return D == 128 ? launch_decode_impl<128, 2>(p, stream) : launch_decode_impl<64, 2>(p, stream);
+  return D == 128 ? launch_decode_t_impl<128, 4>(p, stream)
+                  : launch_decode_t_impl<64, 4>(p, stream);
 }
 
 }  // namespace fi

@@ -97,6 +97,9 @@ def spec(name: str) -> Spec:
     if name == "decode":
         return Spec("decode", 10000, num_kv_heads=8, head_dim=128, page_size=16,
                     num_qo_heads=32, seq_lens=[4096] * 128, qo_lens=[1] * 128, attn="decode")
+    if name == "decode_spec":
+        return Spec("decode_spec", 10500, num_kv_heads=8, head_dim=128, page_size=16,
+                    num_qo_heads=32, seq_lens=[4096] * 128, qo_lens=[8] * 128, attn="decode")
     if name == "decode_small":
         return Spec("decode_small", 11000, num_kv_heads=2, head_dim=128, page_size=16,
                     num_qo_heads=8, seq_lens=[1, 40, 300, 1000, 5000], qo_lens=[1] * 5, attn="decode")
