@@ -661,8 +661,11 @@ __global__ void __launch_bounds__(Layout<D, NQ, PAIR, KVF>::kThreads, 1)
         // 2^kLazyRescale (P stays below that power of two otherwise).  O holds
         // the PV products of tiles < j, all complete (the commit behind this
         // tile's s_full follows them); it is rescaled, 16 columns at a time,
-        // before any P of this tile is released.
-        if (m_new > m_ref + kLazyRescale) {
+        // before any P of this tile is released.  The tensor-memory accesses
+        // are warp-wide, so the decision is the warp's: when any of its rows
+        // grows past the threshold, every row of the warp moves its max to
+        // m_new (for the others an ordinary online-softmax step, alpha <= 1).
+        if (__any_sync(0xFFFFFFFFu, m_new > m_ref + kLazyRescale)) {
           const float alpha = ex2(m_ref - m_new);
           l *= alpha;
           m_ref = m_new;

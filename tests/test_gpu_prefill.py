@@ -68,6 +68,28 @@ def test_prefill_bottom_right_causal_matches_oracle(name, schedule, cta_pairs):
     assert_within_tolerance(res)
 
 
+@pytest.mark.parametrize("cta_pairs", [0, 1])
+def test_prefill_rescale_when_only_some_rows_of_a_warp_grow(cta_pairs):
+    """A key of large norm at position 200 of a 300-token sequence, aligned
+    with query row 210: in the second KV tile the running maximum of some rows
+    (those at or after the key, and aligned with it) grows past the lazy
+    rescale threshold while the other rows of their warps do not see the key
+    (causal mask) and keep theirs.  The rescale of O must still match the
+    oracle."""
+    sp = W.Spec("rescale_split", 19000, num_kv_heads=2, head_dim=128, page_size=16,
+                num_qo_heads=8, seq_lens=[300])
+    d = device_inputs(sp)
+    g = sp.num_qo_heads // sp.num_kv_heads
+    for h in range(sp.num_kv_heads):
+        big = 8.0 * torch.sign(d["host"]["q"][210, h * g].float())
+        d["host"]["k"][200, h] = big.to(torch.bfloat16)
+    d["k"] = d["host"]["k"].to("cuda")
+    out, lse, cache, status, info = run_path(d, cta_pairs=cta_pairs)
+    assert status == 0
+    ref_out, ref_lse = oracle_attention(d, oracle_cache(d))
+    assert_within_tolerance(compare_attention(out, lse, ref_out, ref_lse))
+
+
 def test_prefill_single_sequence_2048_sampled():
     d = device_inputs("single")
     out, lse, cache, status, info = run_path(d)
