@@ -114,8 +114,8 @@ struct Layout {
   // warpgroup gives registers up, each softmax warpgroup takes more (a whole
   // row of S), the load/MMA warpgroup keeps the launch's count.  The
   // launcher checks that the sum fits in what the CTA is launched with.
-  static constexpr int kRegRepack = 64;
-  static constexpr int kRegSoftmax = NQ == 2 ? 160 : 232;
+  static constexpr int kRegRepack = NQ == 2 ? 48 : 64;
+  static constexpr int kRegSoftmax = NQ == 2 ? 168 : 232;
   static_assert(kOffStg % 1024 == 0 && kStg % 1024 == 0, "swizzled tiles need 1 KB alignment");
   static_assert(kAlloc <= 232448, "at most 227 KB of shared memory per CTA");
   static_assert(kRaw % 16 == 0 && kOffRaw % 16 == 0, "bulk copies need 16 B alignment");
