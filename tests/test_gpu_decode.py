@@ -8,7 +8,7 @@ import pytest
 import torch
 
 from gpu_util import (assert_within_tolerance, compare_attention, device_inputs, fi, gpu_cache,
-                      oracle_attention, oracle_cache)
+                      oracle_attention, oracle_attention_subset, oracle_cache)
 
 pytestmark = pytest.mark.gpu
 
@@ -151,3 +151,30 @@ def test_decode_page_id_out_of_range_flagged():
     d["page_table"][4, 0] = -5
     _, _, _, status, _ = _run_decode(d)
     assert status & fi().FI_DEV_PAGE_OOB
+
+
+@pytest.mark.parametrize("name", ["decode", "decode_spec"])
+def test_decode_full_size_sampled(name):
+    """The bench's decode batches (128 x 4096 keys; 1 and 8 query tokens per
+    sequence) in the bench's launch configuration: every query row of six
+    sampled sequences against the oracle."""
+    d = device_inputs(name, gen_device="cuda")
+    out, lse, _, status, info = _run_decode(d)
+    assert status == 0
+    sp = d["spec"]
+    h = d["host"]
+    qo = h["qo_indptr"].cpu().numpy()
+    kv = h["kv_indptr"].cpu().numpy()
+    seqs = np.random.default_rng(11).choice(len(qo) - 1, size=6, replace=False)
+    mask = torch.zeros(int(kv[-1]), dtype=torch.bool)
+    for b in seqs:
+        mask[kv[b]:kv[b + 1]] = True
+    for k in ("k", "v", "slot_mapping"):
+        h[k] = h[k].cpu()
+    host_cache = oracle_cache(d, token_mask=mask)
+    rows = np.array([(t, hq) for b in sorted(seqs) for t in range(qo[b], qo[b + 1])
+                     for hq in range(sp.num_qo_heads)], np.int64)
+    ref_out, ref_lse = oracle_attention_subset(d, host_cache, seqs, rows)
+    res = compare_attention(out, lse, ref_out, ref_lse, rows=rows)
+    print(name, info["num_units"], res)
+    assert_within_tolerance(res)
