@@ -96,7 +96,7 @@ __device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
 //  * The keys of the PV k-step are the S^T m-tile's rows in order; P^T's B
 //    fragment is the S^T accumulator packed to fp16 and transposed 8x8 by
 //    movmatrix.
-// Raw stage of one warp (32 keys, key = lane of the copy): K codes (D/2
+// Raw stage of one warp (32 keys, row r = key kb + r): K codes (D/2
 // bytes a key, unpadded: a quarter-warp reads 128 contiguous bytes), K
 // scales (D/16 bytes a key), V rows (D/2 codes, D/16 scales, padded to 80
 // or 48 bytes so that the 8-byte or 4-byte reads of a half-warp or warp hit
@@ -125,7 +125,7 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   return r;
 }
 
-// NT: 8-row n-tiles per unit (rows G * qo_len <= 8 NT).
+// NT: 8-row n-tiles (rows G * qo_len <= 8 NT); one warp runs its pieces in turn.
 template <int D, int NT>
 __global__ void __launch_bounds__(32 * kTWarps, NT == 1 ? 4 : NT == 2 ? 3 : 2)
     nvfp4_decode_t_kernel(const DecodeParams p) {
