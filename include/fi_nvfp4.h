@@ -314,7 +314,9 @@ fi_status fi_decode_plan_host(const int32_t* qo_indptr_host, const int32_t* kv_i
  * copy, so they must stay unchanged until then.  The first call on a device
  * looks up the array's device address; make that first call before any stream
  * capture.  Ragged work units are taken in sequence order with the heaviest
- * q-tile of each sequence first. */
+ * q-tile of each sequence first (dealt round-robin to the CTAs: no balanced
+ * slot lists); groups of a multiple of 4 query heads run on CTA pairs, as
+ * fi_prefill_plan chooses by default. */
 fi_status fi_prefill_noalloc(const int32_t* qo_indptr_host, const int32_t* kv_indptr_host,
                              int32_t batch, const int32_t* page_table_dev,
                              int32_t page_table_stride, int32_t num_qo_heads,

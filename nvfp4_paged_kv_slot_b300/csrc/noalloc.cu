@@ -95,7 +95,11 @@ extern "C" fi_status fi_prefill_noalloc(const int32_t* qo_indptr_host,
   int64_t units_ragged = 0;
   fi_plan_info& I = P.info;
   I.heads_per_cta = (P.group % 2 == 0) ? 2 : 1;
-  P.units_per_kv_head = P.group / I.heads_per_cta;
+  // groups of a multiple of 4 query heads on CTA pairs, as fi_prefill_plan
+  // chooses by default
+  P.pair = P.group % 4 == 0;
+  I.ctas_per_unit = P.pair ? 2 : 1;
+  P.units_per_kv_head = P.group / (I.heads_per_cta * I.ctas_per_unit);
   I.head_units = num_kv_heads * P.units_per_kv_head;
   for (int32_t b = 0; b < batch; ++b) {
     const int32_t qo = qo_indptr_host[b + 1] - qo_indptr_host[b];
@@ -129,7 +133,9 @@ extern "C" fi_status fi_prefill_noalloc(const int32_t* qo_indptr_host,
   } else {
     I.num_units = units_ragged;
   }
-  I.num_ctas = static_cast<int32_t>(std::min<int64_t>(I.num_units, std::max(sms, 1)));
+  I.num_ctas = static_cast<int32_t>(
+      std::min<int64_t>(I.num_units * I.ctas_per_unit, std::max(sms, I.ctas_per_unit)));
+  if (P.pair) I.num_ctas &= ~1;
   if (batch > 0 && (!page_table_dev || page_table_stride <= 0 ||
                     (max_kv + page_size - 1) / page_size > page_table_stride))
     return FI_ERR_INVALID_ARGUMENT;

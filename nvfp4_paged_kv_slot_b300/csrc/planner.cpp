@@ -231,11 +231,9 @@ fi_status plan_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t 
 }
 
 // Decode plan ([#5043] decode.py: max_kv_len from one reduction over the
-// lengths).  Units are (sequence, kv head, chunk of keys); the chunk length
-// (a power of two, 256 .. 16384) is the smallest that keeps the units below
-// 32 per SM, so that short batches still fill the GPU and long ones do not
-// pay for many merges.  A sequence with several chunks gets one partial slot
-// per chunk and one merge.
+// lengths).  The keys of all (sequence, KV head) pairs are split evenly over
+// the warps the decode kernel keeps resident (below); a pair split over
+// several warps gets one partial slot per piece and one merge.
 fi_status plan_decode_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t batch,
                            int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
                            int32_t page_size, float sm_scale, int32_t num_sms, HostPlan* out) {
