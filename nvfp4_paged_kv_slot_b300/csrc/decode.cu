@@ -116,7 +116,7 @@ template <int D>
 constexpr int kTStage = 32 * (D / 2 + D / 16 + kTVRow<D>);
 template <int D, int NT>
 constexpr int decode_t_smem_bytes() {
-  return kTWarps * (kTStages * kTStage<D> + (NT == 4 ? NT * (D / 16) * 32 * 8 : 0));
+  return kTWarps * (kTStages * kTStage<D> + (NT >= 2 ? NT * (D / 16) * 32 * 8 : 0));
 }
 
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(32 * kTWarps, NT == 1 ? 4 : NT == 2 ? 3 : 2)
   constexpr int kV = 32 * (D / 2 + D / 16);  // V rows within a stage
   constexpr int kKW = D / 32;                // code words of a key a lane converts for S^T
   constexpr int kVW = D / 64;                // code words of a key a lane converts for O^T
-  constexpr bool kQs = NT == 4;              // Q^T fragments in shared memory
+  constexpr bool kQs = NT >= 2;              // Q^T fragments in shared memory
   extern __shared__ __align__(16) uint8_t dsm[];
   grid_dep_wait();  // Q and the cache may come from the previous grid
   grid_dep_launch();
@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(32 * kTWarps, NT == 1 ? 4 : NT == 2 ? 3 : 2)
     const int qe = qmax > 0.0f ? ilogbf(qmax) - 13 : 0;
     const float qsc = ldexpf(qs, -qe);
     const float ssc = ldexpf(1.0f, qe);
-    // With 4 n-tiles the fragments live in shared memory (this warp's slice,
+    // With 2 or 4 n-tiles the fragments live in shared memory (this warp's slice,
     // fragment (nt, k-step s) of lane l at [nt][s][l]: conflict-free 8-byte
     // reads), which keeps the kernel within its registers; else in registers.
     uint32_t qb[NT][D / 16][2];
