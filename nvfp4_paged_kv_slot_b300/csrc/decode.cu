@@ -19,6 +19,7 @@
 // sum) per piece, which a second kernel merges.
 
 #include <algorithm>
+#include <atomic>
 
 #include "internal.h"
 #include "nvfp4.cuh"
@@ -101,7 +102,8 @@ __device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
 // scales (D/16 bytes a key), V rows (D/2 codes, D/16 scales, padded to 80
 // or 48 bytes so that the 8-byte or 4-byte reads of a half-warp or warp hit
 // distinct banks).
-constexpr int kTWarps = 4;   // warps per CTA
+constexpr int kDecMaxDevices = 64;  // per-device launch attributes cached
+constexpr int kTWarps = 4;          // warps per CTA
 constexpr int kTStages = 2;  // raw stages per warp: this step's and the next
 
 // The planner sizes the warp count to what is resident per SM: 4 CTAs up to
@@ -637,9 +639,18 @@ template <int D, int NT>
 fi_status launch_decode_t_impl(const DecodeParams& p, cudaStream_t stream) {
   const int smem = decode_t_smem_bytes<D, NT>();
   auto kern = nvfp4_decode_t_kernel<D, NT>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-      cudaSuccess)
-    return FI_ERR_CUDA;
+  // the shared-memory attribute is set once per device (a race between host
+  // threads only sets it twice)
+  static std::atomic<int> attr_set[kDecMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FI_ERR_CUDA;
+  if (dev < 0 || dev >= kDecMaxDevices) return FI_ERR_UNSUPPORTED;
+  if (attr_set[dev].load(std::memory_order_relaxed) == 0) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return FI_ERR_CUDA;
+    attr_set[dev].store(1, std::memory_order_relaxed);
+  }
   const unsigned grid = static_cast<unsigned>((p.num_warps + kTWarps - 1) / kTWarps);
   fi_status st = launch_pdl(kern, dim3(grid), dim3(32 * kTWarps), smem, stream, p);
   if (st != FI_OK || p.num_merges == 0) return st;

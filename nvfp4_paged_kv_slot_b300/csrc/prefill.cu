@@ -779,15 +779,24 @@ fi_status launch_impl(const PrefillParams& p, int grid, cudaStream_t stream) {
   // at least ~116 KB so that a single CTA (and its 256-512 TMEM columns)
   // occupies each SM
   const int smem = L::kAlloc > 118784 ? L::kAlloc : 118784;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-      cudaSuccess)
-    return FI_ERR_CUDA;
-  // The warpgroup register reallocation must fit in what the launch gives the
-  // CTA, or a warpgroup's increase would never be granted.
-  cudaFuncAttributes attr;
-  if (cudaFuncGetAttributes(&attr, kern) != cudaSuccess) return FI_ERR_CUDA;
-  if (128 * (attr.numRegs + L::kRegRepack + NQ * L::kRegSoftmax) > attr.numRegs * L::kThreads)
-    return FI_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FI_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FI_ERR_UNSUPPORTED;
+  // The shared-memory attribute and the register check are done once per
+  // device (1 = done; a race between host threads only repeats them).
+  static std::atomic<int> checked[kMaxDevices];
+  if (checked[dev].load(std::memory_order_relaxed) == 0) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return FI_ERR_CUDA;
+    // The warpgroup register reallocation must fit in what the launch gives
+    // the CTA, or a warpgroup's increase would never be granted.
+    cudaFuncAttributes attr;
+    if (cudaFuncGetAttributes(&attr, kern) != cudaSuccess) return FI_ERR_CUDA;
+    if (128 * (attr.numRegs + L::kRegRepack + NQ * L::kRegSoftmax) > attr.numRegs * L::kThreads)
+      return FI_ERR_UNSUPPORTED;
+    checked[dev].store(1, std::memory_order_relaxed);
+  }
   if (!PAIR) return launch_pdl(kern, dim3(grid), dim3(L::kThreads), smem, stream, p);
   cudaLaunchAttribute cl[1];
   cl[0].id = cudaLaunchAttributeClusterDimension;
@@ -798,9 +807,6 @@ fi_status launch_impl(const PrefillParams& p, int grid, cudaStream_t stream) {
   // unit.  The occupancy query is cached per device (0 = not yet known); a
   // race between host threads only repeats the same query.
   static std::atomic<int> max_clusters[kMaxDevices];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FI_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return FI_ERR_UNSUPPORTED;
   int n_clusters = max_clusters[dev].load(std::memory_order_relaxed);
   if (n_clusters == 0) {
     int sms = 0;
