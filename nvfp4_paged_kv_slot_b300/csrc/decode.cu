@@ -98,13 +98,15 @@ __device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
 //    fragment is the S^T accumulator packed to fp16 and transposed 8x8 by
 //    movmatrix.
 // Raw stage of one warp (32 keys, row r = key kb + r): K codes (D/2
-// bytes a key, unpadded: a quarter-warp reads 128 contiguous bytes), K
-// scales (D/16 bytes a key), V rows (D/2 codes, D/16 scales, padded to 80
-// or 48 bytes so that the 8-byte or 4-byte reads of a half-warp or warp hit
-// distinct banks).
+// bytes a key: a quarter-warp reads 128 contiguous bytes), K scales (D/16
+// bytes a key), V codes (D/2 bytes a key), V scales (D/16).  Rows are
+// unpadded so that three stages fit with 16 warps per SM; the 8-byte reads
+// of V codes then meet two-way bank conflicts (padding the rows to 80 bytes
+// avoids them but leaves room for two stages only, which measured slower
+// with 9-16 rows and the same with fewer).
 constexpr int kDecMaxDevices = 64;  // per-device launch attributes cached
 constexpr int kTWarps = 4;          // warps per CTA
-constexpr int kTStages = 2;  // raw stages per warp: this step's and the next
+constexpr int kTStages = 3;  // raw stages per warp: this step's and the next two
 
 // The planner sizes the warp count to what is resident per SM: 4 CTAs up to
 // 8 rows, 3 up to 16, 2 up to 32 (the launch bounds below).
@@ -113,9 +115,9 @@ static_assert(kTWarps * 4 == decode_warps_per_sm(8) && kTWarps * 3 == decode_war
               "decode occupancy and plan disagree");
 
 template <int D>
-constexpr int kTVRow = D == 128 ? 80 : 48;
+constexpr int kTVRow = D / 2;  // V code rows unpadded; V scales in their own rows
 template <int D>
-constexpr int kTStage = 32 * (D / 2 + D / 16 + kTVRow<D>);
+constexpr int kTStage = 32 * (D + D / 8);
 template <int D, int NT>
 constexpr int decode_t_smem_bytes() {
   return kTWarps * (kTStages * kTStage<D> + (NT >= 2 ? NT * (D / 16) * 32 * 8 : 0));
@@ -135,6 +137,7 @@ __global__ void __launch_bounds__(32 * kTWarps, NT == 1 ? 4 : NT == 2 ? 3 : 2)
   constexpr int kVR = kTVRow<D>;
   constexpr int kKsf = 32 * (D / 2);         // K scales within a stage
   constexpr int kV = 32 * (D / 2 + D / 16);  // V rows within a stage
+  constexpr int kVsf = kV + 32 * (D / 2);    // V scales within a stage
   constexpr int kKW = D / 32;                // code words of a key a lane converts for S^T
   constexpr int kVW = D / 64;                // code words of a key a lane converts for O^T
   constexpr bool kQs = NT >= 2;              // Q^T fragments in shared memory
@@ -282,16 +285,16 @@ __global__ void __launch_bounds__(32 * kTWarps, NT == 1 ? 4 : NT == 2 ? 3 : 2)
         const int64_t row = (lane < 16 ? row_h0 : row_h1) + (lane & 15);
         if constexpr (D == 128) {
           cp_async8(s + kKsf + lane * 8, p.k_sf + row * 8);
-          cp_async8(s + kV + lane * kVR + 64, p.v_sf + row * 8);
+          cp_async8(s + kVsf + lane * 8, p.v_sf + row * 8);
         } else {
           cp_async4(s + kKsf + lane * 4, p.k_sf + row * 4);
-          cp_async4(s + kV + lane * kVR + 32, p.v_sf + row * 4);
+          cp_async4(s + kVsf + lane * 4, p.v_sf + row * 4);
         }
       } else {
         if constexpr (D == 128)
-          *reinterpret_cast<uint2*>(s + kV + lane * kVR + 64) = make_uint2(0u, 0u);
+          *reinterpret_cast<uint2*>(s + kVsf + lane * 8) = make_uint2(0u, 0u);
         else
-          *reinterpret_cast<uint32_t*>(s + kV + lane * kVR + 32) = 0u;
+          *reinterpret_cast<uint32_t*>(s + kVsf + lane * 4) = 0u;
       }
       cp_async_commit();
     };
@@ -504,15 +507,15 @@ __global__ void __launch_bounds__(32 * kTWarps, NT == 1 ? 4 : NT == 2 ? 3 : 2)
           const uint2 x3 = *reinterpret_cast<const uint2*>(vb + (kA + 9) * kVR + 8 * g);
           va[0] = x0.x; va[1] = x0.y; vb1[0] = x1.x; vb1[1] = x1.y;
           vc[0] = x2.x; vc[1] = x2.y; vd[0] = x3.x; vd[1] = x3.y;
-          sab = vb[kA * kVR + 64 + g] | (vb[(kA + 1) * kVR + 64 + g] << 8);
-          scd = vb[(kA + 8) * kVR + 64 + g] | (vb[(kA + 9) * kVR + 64 + g] << 8);
+          sab = sb[kVsf + kA * 8 + g] | (sb[kVsf + (kA + 1) * 8 + g] << 8);
+          scd = sb[kVsf + (kA + 8) * 8 + g] | (sb[kVsf + (kA + 9) * 8 + g] << 8);
         } else {
           va[0] = *reinterpret_cast<const uint32_t*>(vb + kA * kVR + 4 * g);
           vb1[0] = *reinterpret_cast<const uint32_t*>(vb + (kA + 1) * kVR + 4 * g);
           vc[0] = *reinterpret_cast<const uint32_t*>(vb + (kA + 8) * kVR + 4 * g);
           vd[0] = *reinterpret_cast<const uint32_t*>(vb + (kA + 9) * kVR + 4 * g);
-          sab = vb[kA * kVR + 32 + g / 2] | (vb[(kA + 1) * kVR + 32 + g / 2] << 8);
-          scd = vb[(kA + 8) * kVR + 32 + g / 2] | (vb[(kA + 9) * kVR + 32 + g / 2] << 8);
+          sab = sb[kVsf + kA * 4 + g / 2] | (sb[kVsf + (kA + 1) * 4 + g / 2] << 8);
+          scd = sb[kVsf + (kA + 8) * 4 + g / 2] | (sb[kVsf + (kA + 9) * 4 + g / 2] << 8);
         }
         const uint32_t s01 = e4m3x2_to_f16x2(sab), s89 = e4m3x2_to_f16x2(scd);
 #pragma unroll
