@@ -99,14 +99,12 @@ __device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
 //    movmatrix.
 // Raw stage of one warp (32 keys, row r = key kb + r): K codes (D/2
 // bytes a key: a quarter-warp reads 128 contiguous bytes), K scales (D/16
-// bytes a key), V codes (D/2 bytes a key), V scales (D/16).  Rows are
-// unpadded so that three stages fit with 16 warps per SM; the 8-byte reads
-// of V codes then meet two-way bank conflicts (padding the rows to 80 bytes
-// avoids them but leaves room for two stages only, which measured slower
-// with 9-16 rows and the same with fewer).
+// bytes a key), V codes and scales (D/2 and D/16 bytes a key).  V rows
+// padded to 80 or 48 bytes put the 8- or 4-byte reads of a half-warp or warp
+// on distinct banks; unpadded (two-way conflicts) they leave room for a
+// third stage, which pays with 2 n-tiles (12 warps per SM) only.
 constexpr int kDecMaxDevices = 64;  // per-device launch attributes cached
 constexpr int kTWarps = 4;          // warps per CTA
-constexpr int kTStages = 3;  // raw stages per warp: this step's and the next two
 
 // The planner sizes the warp count to what is resident per SM: 4 CTAs up to
 // 8 rows, 3 up to 16, 2 up to 32 (the launch bounds below).
@@ -114,13 +112,20 @@ static_assert(kTWarps * 4 == decode_warps_per_sm(8) && kTWarps * 3 == decode_war
                   kTWarps * 2 == decode_warps_per_sm(32),
               "decode occupancy and plan disagree");
 
-template <int D>
-constexpr int kTVRow = D / 2;  // V code rows unpadded; V scales in their own rows
-template <int D>
-constexpr int kTStage = 32 * (D + D / 8);
+// Raw stages per warp and their layout by n-tiles: with 2 n-tiles (3 CTAs
+// per SM) three stages in unpadded rows, V scales in their own rows; else
+// two stages with V rows (codes, then scales) padded to 80 or 48 bytes.
+template <int NT>
+constexpr int kTStagesOf = NT == 2 ? 3 : 2;
+template <int D, int NT>
+constexpr bool kTSepSf = NT == 2;
+template <int D, int NT>
+constexpr int kTVRowOf = kTSepSf<D, NT> ? D / 2 : (D == 128 ? 80 : 48);
+template <int D, int NT>
+constexpr int kTStageOf = 32 * (D / 2 + D / 16 + kTVRowOf<D, NT> + (kTSepSf<D, NT> ? D / 16 : 0));
 template <int D, int NT>
 constexpr int decode_t_smem_bytes() {
-  return kTWarps * (kTStages * kTStage<D> + (NT >= 2 ? NT * (D / 16) * 32 * 8 : 0));
+  return kTWarps * (kTStagesOf<NT> * kTStageOf<D, NT> + (NT >= 2 ? NT * (D / 16) * 32 * 8 : 0));
 }
 
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
@@ -133,11 +138,14 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
 template <int D, int NT>
 __global__ void __launch_bounds__(32 * kTWarps, NT == 1 ? 4 : NT == 2 ? 3 : 2)
     nvfp4_decode_t_kernel(const DecodeParams p) {
-  constexpr int kStage = kTStage<D>;
-  constexpr int kVR = kTVRow<D>;
+  constexpr int kTStages = kTStagesOf<NT>;
+  constexpr int kStage = kTStageOf<D, NT>;
+  constexpr int kVR = kTVRowOf<D, NT>;
   constexpr int kKsf = 32 * (D / 2);         // K scales within a stage
   constexpr int kV = 32 * (D / 2 + D / 16);  // V rows within a stage
-  constexpr int kVsf = kV + 32 * (D / 2);    // V scales within a stage
+  // V scale byte of block b of row r: kVsf + r * kVsfS + b
+  constexpr int kVsf = kTSepSf<D, NT> ? kV + 32 * kVR : kV + D / 2;
+  constexpr int kVsfS = kTSepSf<D, NT> ? D / 16 : kVR;
   constexpr int kKW = D / 32;                // code words of a key a lane converts for S^T
   constexpr int kVW = D / 64;                // code words of a key a lane converts for O^T
   constexpr bool kQs = NT >= 2;              // Q^T fragments in shared memory
@@ -285,16 +293,16 @@ __global__ void __launch_bounds__(32 * kTWarps, NT == 1 ? 4 : NT == 2 ? 3 : 2)
         const int64_t row = (lane < 16 ? row_h0 : row_h1) + (lane & 15);
         if constexpr (D == 128) {
           cp_async8(s + kKsf + lane * 8, p.k_sf + row * 8);
-          cp_async8(s + kVsf + lane * 8, p.v_sf + row * 8);
+          cp_async8(s + kVsf + lane * kVsfS, p.v_sf + row * 8);
         } else {
           cp_async4(s + kKsf + lane * 4, p.k_sf + row * 4);
-          cp_async4(s + kVsf + lane * 4, p.v_sf + row * 4);
+          cp_async4(s + kVsf + lane * kVsfS, p.v_sf + row * 4);
         }
       } else {
         if constexpr (D == 128)
-          *reinterpret_cast<uint2*>(s + kVsf + lane * 8) = make_uint2(0u, 0u);
+          *reinterpret_cast<uint2*>(s + kVsf + lane * kVsfS) = make_uint2(0u, 0u);
         else
-          *reinterpret_cast<uint32_t*>(s + kVsf + lane * 4) = 0u;
+          *reinterpret_cast<uint32_t*>(s + kVsf + lane * kVsfS) = 0u;
       }
       cp_async_commit();
     };
@@ -507,15 +515,15 @@ __global__ void __launch_bounds__(32 * kTWarps, NT == 1 ? 4 : NT == 2 ? 3 : 2)
           const uint2 x3 = *reinterpret_cast<const uint2*>(vb + (kA + 9) * kVR + 8 * g);
           va[0] = x0.x; va[1] = x0.y; vb1[0] = x1.x; vb1[1] = x1.y;
           vc[0] = x2.x; vc[1] = x2.y; vd[0] = x3.x; vd[1] = x3.y;
-          sab = sb[kVsf + kA * 8 + g] | (sb[kVsf + (kA + 1) * 8 + g] << 8);
-          scd = sb[kVsf + (kA + 8) * 8 + g] | (sb[kVsf + (kA + 9) * 8 + g] << 8);
+          sab = sb[kVsf + kA * kVsfS + g] | (sb[kVsf + (kA + 1) * kVsfS + g] << 8);
+          scd = sb[kVsf + (kA + 8) * kVsfS + g] | (sb[kVsf + (kA + 9) * kVsfS + g] << 8);
         } else {
           va[0] = *reinterpret_cast<const uint32_t*>(vb + kA * kVR + 4 * g);
           vb1[0] = *reinterpret_cast<const uint32_t*>(vb + (kA + 1) * kVR + 4 * g);
           vc[0] = *reinterpret_cast<const uint32_t*>(vb + (kA + 8) * kVR + 4 * g);
           vd[0] = *reinterpret_cast<const uint32_t*>(vb + (kA + 9) * kVR + 4 * g);
-          sab = sb[kVsf + kA * 4 + g / 2] | (sb[kVsf + (kA + 1) * 4 + g / 2] << 8);
-          scd = sb[kVsf + (kA + 8) * 4 + g / 2] | (sb[kVsf + (kA + 9) * 4 + g / 2] << 8);
+          sab = sb[kVsf + kA * kVsfS + g / 2] | (sb[kVsf + (kA + 1) * kVsfS + g / 2] << 8);
+          scd = sb[kVsf + (kA + 8) * kVsfS + g / 2] | (sb[kVsf + (kA + 9) * kVsfS + g / 2] << 8);
         }
         const uint32_t s01 = e4m3x2_to_f16x2(sab), s89 = e4m3x2_to_f16x2(scd);
 #pragma unroll
