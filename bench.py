@@ -368,27 +368,48 @@ def time_e2e(runner, stream, steps, warmup):
     """Same step through the public API with host inputs: pinned host K/V/Q,
     slot_mapping and page_table are copied to the device inside the timed
     region, and the attention output (and LSE) are read back to pinned host
-    memory at the end of every step."""
-    hk = runner.k.cpu().pin_memory()
-    hv = runner.v.cpu().pin_memory()
-    hq = runner.q.cpu().pin_memory()
-    hs = runner.slots.cpu().pin_memory()
-    hpt = runner.page_table.cpu().pin_memory()
+    memory at the end of every step.  Two device buffer sets alternate between
+    steps, as a serving loop double-buffers its transfers: step s's inputs are
+    copied on one copy stream while step s-1's kernels run, and step s-1's
+    results are read back on another while step s's kernels run.  Every step
+    still moves all of its inputs and results; the time per step is the whole
+    timed region (first copy in to last copy out) over the steps."""
+    names = ("k", "v", "q", "slots", "page_table")
+    host_in = {n: getattr(runner, n).cpu().pin_memory() for n in names}
     ho = torch.empty(runner.out.shape, dtype=runner.out.dtype, pin_memory=True)
     hl = torch.empty(runner.lse.shape, dtype=runner.lse.dtype, pin_memory=True)
-    h2d = sum(t.numel() * t.element_size() for t in (hk, hv, hq, hs, hpt))
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    own = {n: getattr(runner, n) for n in names + ("out", "lse")}
+    sets = [own, {n: torch.empty_like(t) for n, t in own.items()}]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    # per buffer set: inputs copied / kernels done / results read back
+    ev = [{k: torch.cuda.Event() for k in ("in", "run", "out")} for _ in sets]
+    for e in ev:
+        for x in e.values():
+            x.record(stream)
+    n_step = [0]
 
     def one():
-        with torch.cuda.stream(stream):
-            runner.k.copy_(hk, non_blocking=True)
-            runner.v.copy_(hv, non_blocking=True)
-            runner.q.copy_(hq, non_blocking=True)
-            runner.slots.copy_(hs, non_blocking=True)
-            runner.page_table.copy_(hpt, non_blocking=True)
-            runner.step(stream)
-            ho.copy_(runner.out, non_blocking=True)
-            hl.copy_(runner.lse, non_blocking=True)
+        b = sets[n_step[0] % 2]
+        e = ev[n_step[0] % 2]
+        n_step[0] += 1
+        s_in.wait_event(e["run"])            # the previous kernels of this set have read it
+        with torch.cuda.stream(s_in):
+            for n in names:
+                b[n].copy_(host_in[n], non_blocking=True)
+        e["in"].record(s_in)
+        stream.wait_event(e["in"])
+        stream.wait_event(e["out"])          # this set's previous results are read back
+        for n, t in b.items():
+            setattr(runner, n, t)
+        runner.step(stream)
+        e["run"].record(stream)
+        s_out.wait_event(e["run"])
+        with torch.cuda.stream(s_out):
+            ho.copy_(b["out"], non_blocking=True)
+            hl.copy_(b["lse"], non_blocking=True)
+        e["out"].record(s_out)
 
     for _ in range(warmup):
         one()
@@ -396,8 +417,11 @@ def time_e2e(runner, stream, steps, warmup):
     t0 = time.perf_counter()
     for _ in range(steps):
         one()
-    stream.synchronize()
+    torch.cuda.synchronize()
     dt = time.perf_counter() - t0
+    for n, t in own.items():
+        setattr(runner, n, t)
+    del sets
     return dt / steps, h2d, d2h
 
 
@@ -621,7 +645,7 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOAD_DESC), default="uniform")
     ap.add_argument("--kv-format", choices=["nvfp4", "fp8"], default="nvfp4",
                     help="fp8: the FP8 (E4M3) paged KV variant of the same path")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-append-bench", action="store_true")
