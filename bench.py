@@ -373,7 +373,9 @@ def time_e2e(runner, stream, steps, warmup):
     copied on one copy stream while step s-1's kernels run, and step s-1's
     results are read back on another while step s's kernels run.  Every step
     still moves all of its inputs and results; the time per step is the whole
-    timed region (first copy in to last copy out) over the steps."""
+    timed region (first copy in to last copy out) over the steps.  Returns
+    (seconds per step, bytes in per step, bytes out per step, the last step's
+    host O and LSE)."""
     names = ("k", "v", "q", "slots", "page_table")
     host_in = {n: getattr(runner, n).cpu().pin_memory() for n in names}
     ho = torch.empty(runner.out.shape, dtype=runner.out.dtype, pin_memory=True)
@@ -422,7 +424,7 @@ def time_e2e(runner, stream, steps, warmup):
     for n, t in own.items():
         setattr(runner, n, t)
     del sets
-    return dt / steps, h2d, d2h
+    return dt / steps, h2d, d2h, (ho, hl)
 
 
 def time_append_cold(fi, device, n_sets=24, reps=20):
@@ -715,7 +717,7 @@ def main():
 
     e2e = None
     if not args.no_e2e:
-        e2e_s, h2d, d2h = time_e2e(runner, stream, args.e2e_steps, 1)
+        e2e_s, h2d, d2h, _ = time_e2e(runner, stream, args.e2e_steps, 1)
         e2e_s = max_over_ranks(e2e_s, dist_on, device)
         e2e = {"value": aggregate_value(runner.flops, e2e_s * 1e3, world), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
