@@ -90,6 +90,28 @@ def test_prefill_rescale_when_only_some_rows_of_a_warp_grow(cta_pairs):
     assert_within_tolerance(compare_attention(out, lse, ref_out, ref_lse))
 
 
+@pytest.mark.parametrize("page_size", [32, 64, 128])
+@pytest.mark.parametrize("head_dim", [64, 128])
+@pytest.mark.parametrize("cta_pairs", [0, 1])
+def test_prefill_page_sizes(page_size, head_dim, cta_pairs):
+    """Pages of 32, 64 and 128 tokens: a 128-key tile spans 4, 2 or 1 pages.
+    On CTA pairs each CTA copies the pages of its 64 rows of a tile (two of 32
+    tokens, one of 64, or half of a 128-token page); the single-CTA kernel
+    copies whole pages.  Ragged lengths with partial last pages, a length that
+    fills its pages exactly, and queries over a longer cache."""
+    sp = W.Spec(f"pages{page_size}_d{head_dim}", 20000 + page_size + head_dim, num_kv_heads=2,
+                head_dim=head_dim, page_size=page_size, num_qo_heads=8,
+                seq_lens=[1, 70, 256, 333, 129], qo_lens=[1, 70, 200, 333, 5])
+    d = device_inputs(sp)
+    out, lse, cache, status, info = run_path(d, cta_pairs=cta_pairs)
+    assert status == 0
+    assert info["ctas_per_unit"] == (1 if cta_pairs else 2)
+    ref_out, ref_lse = oracle_attention(d, oracle_cache(d))
+    res = compare_attention(out, lse, ref_out, ref_lse)
+    print(page_size, head_dim, cta_pairs, info, res)
+    assert_within_tolerance(res)
+
+
 def test_prefill_single_sequence_2048_sampled():
     d = device_inputs("single")
     out, lse, cache, status, info = run_path(d)
