@@ -29,7 +29,8 @@ def _assert_cache_equal(gpu_c, host_c):
         assert diff.size == 0, f"{name}: {len(diff)} bytes differ, first at {diff[:4].tolist()}"
 
 
-@pytest.mark.parametrize("name", ["tiny", "append", "ragged_small", "ragged_small_d64", "mha_small_d64"])
+@pytest.mark.parametrize("name", ["tiny", "append", "ragged_small", "ragged_small_d64", "mha_small_d64",
+                                  "decode_ps128"])
 @pytest.mark.parametrize("host_scale", [False, True])
 def test_append_bit_exact(name, host_scale):
     m = fi()

@@ -94,11 +94,20 @@ def test_fp8_append_extreme_magnitudes(oracle, H, D, N, gk, gv):
     assert_fp8_cache_equal(c, host)
 
 
+def _pages_spec(page_size, num_qo_heads):
+    """Ragged lengths with partial last pages and queries over a longer cache,
+    on pages of `page_size` tokens (GQA 4: CTA pairs; GQA 1: one CTA)."""
+    return W.Spec(f"fp8_pages{page_size}_h{num_qo_heads}", 21000 + page_size + num_qo_heads,
+                  num_kv_heads=2, head_dim=128, page_size=page_size, num_qo_heads=num_qo_heads,
+                  seq_lens=[1, 70, 256, 333, 129], qo_lens=[1, 70, 200, 333, 5])
+
+
 @pytest.mark.parametrize("name", ["tiny", "ragged_small", "ragged_small_d64", "uniform_small",
-                                  "gqa3_small", "mha_small_d64"])
+                                  "gqa3_small", "mha_small_d64", (32, 8), (64, 8), (128, 8),
+                                  (128, 2)])
 def test_fp8_prefill_matches_oracle(name):
     m = fi()
-    d = device_inputs(name)
+    d = device_inputs(_pages_spec(*name) if isinstance(name, tuple) else name)
     sp = d["spec"]
     ks, vs = fp8_scales(d)
     c = gpu_fp8_cache(d, ks, vs)
