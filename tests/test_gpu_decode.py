@@ -40,7 +40,8 @@ def _run_decode(d):
 
 
 @pytest.mark.parametrize("name", ["decode_small", "decode_spec_small", "decode_d64", "decode_g8",
-                                  "decode_g6_d64", "decode_mixed", "decode_ps128"])
+                                  "decode_g6_d64", "decode_mixed", "decode_ps128",
+                                  "decode_spec_d64"])
 def test_decode_matches_oracle(name):
     d = device_inputs(name)
     out, lse, c, status, info = _run_decode(d)

@@ -125,6 +125,11 @@ def spec(name: str) -> Spec:
                     num_qo_heads=8, seq_lens=[3, 17, 33, 64, 5, 100, 31, 32, 2, 700, 9, 12, 40,
                                               1, 250, 48] * 2 + [3000], qo_lens=[1] * 33,
                     attn="decode")
+    # 17..32 rows per KV head at head_dim 64 (GQA 4 with up to 8-token steps).
+    if name == "decode_spec_d64":
+        return Spec("decode_spec_d64", 13500, num_kv_heads=2, head_dim=64, page_size=32,
+                    num_qo_heads=8, seq_lens=[9, 300, 1200, 64], qo_lens=[8, 5, 8, 1],
+                    attn="decode")
     # Pages of 128 tokens (one page holds four 32-key steps).
     if name == "decode_ps128":
         return Spec("decode_ps128", 13400, num_kv_heads=2, head_dim=128, page_size=128,
