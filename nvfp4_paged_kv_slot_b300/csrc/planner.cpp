@@ -173,28 +173,49 @@ fi_status plan_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t 
       }
     }
   } else {
-    // Ragged: enumerate (sequence, head unit, q-tile) with its cost in KV tiles.
-    struct Item {
-      int32_t b, hu, qt, cost;
-    };
-    std::vector<Item> items;
+    // Ragged: one unit per (sequence, head unit, q-tile) with its cost in KV
+    // tiles, written straight into the list in the kernel's order.
     int64_t n = 0;
     for (int32_t b = 0; b < batch; ++b)
       n += static_cast<int64_t>((qo_indptr[b + 1] - qo_indptr[b] + kTileQ - 1) / kTileQ) * HU;
-    items.reserve(static_cast<size_t>(n));
+    I.num_units = n;
+    P.work.resize(static_cast<size_t>(n) * 4);
+    int32_t* w = P.work.data();
+    auto put = [](int32_t* e, int32_t b, int32_t hu, int32_t qt, int32_t cost) {
+      e[0] = b;
+      e[1] = hu;
+      e[2] = qt;
+      e[3] = cost;
+    };
     if (I.global_reverse) {
+      // Heaviest tiles of all sequences and heads first; ties keep the
+      // head-then-sequence order of the page's global mapping.  The costs are
+      // small integers, so a stable counting sort by cost (descending) puts
+      // every unit in place in two passes.
+      const int32_t max_cost = max_kv / kTileKV + 1;
+      std::vector<int64_t> pos(static_cast<size_t>(max_cost) + 2, 0);
+      for (int32_t b = 0; b < batch; ++b) {
+        const int32_t qo = qo_indptr[b + 1] - qo_indptr[b];
+        const int32_t kv = kv_indptr[b + 1] - kv_indptr[b];
+        const int32_t tiles = (qo + kTileQ - 1) / kTileQ;
+        for (int32_t qt = 0; qt < tiles; ++qt) pos[n_kv_tiles(qt, qo, kv)] += HU;
+      }
+      int64_t acc = 0;  // first position of each cost, highest cost first
+      for (int32_t c = max_cost + 1; c >= 0; --c) {
+        const int64_t cnt = pos[c];
+        pos[c] = acc;
+        acc += cnt;
+      }
       for (int32_t b = 0; b < batch; ++b) {
         const int32_t qo = qo_indptr[b + 1] - qo_indptr[b];
         const int32_t kv = kv_indptr[b + 1] - kv_indptr[b];
         const int32_t tiles = (qo + kTileQ - 1) / kTileQ;
         for (int32_t hu = 0; hu < HU; ++hu)
-          for (int32_t qt = 0; qt < tiles; ++qt)
-            items.push_back({b, hu, qt, n_kv_tiles(qt, qo, kv)});
+          for (int32_t qt = 0; qt < tiles; ++qt) {
+            const int32_t cost = n_kv_tiles(qt, qo, kv);
+            put(w + 4 * pos[cost]++, b, hu, qt, cost);
+          }
       }
-      // heaviest tiles of all sequences and heads first (stable: ties keep the
-      // head-then-sequence order of the page's global mapping)
-      std::stable_sort(items.begin(), items.end(),
-                       [](const Item& x, const Item& y) { return x.cost > y.cost; });
     } else {
       // per (sequence, head unit) groups, reversed q-tiles inside each group;
       // groups ordered longest first so the longest chains start early
@@ -208,17 +229,8 @@ fi_status plan_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t 
         const int32_t kv = kv_indptr[b + 1] - kv_indptr[b];
         const int32_t tiles = (qo + kTileQ - 1) / kTileQ;
         for (int32_t hu = 0; hu < HU; ++hu)
-          for (int32_t qt = tiles - 1; qt >= 0; --qt)
-            items.push_back({b, hu, qt, n_kv_tiles(qt, qo, kv)});
+          for (int32_t qt = tiles - 1; qt >= 0; --qt, w += 4) put(w, b, hu, qt, n_kv_tiles(qt, qo, kv));
       }
-    }
-    I.num_units = static_cast<int64_t>(items.size());
-    P.work.resize(items.size() * 4);
-    for (size_t t = 0; t < items.size(); ++t) {
-      P.work[4 * t + 0] = items[t].b;
-      P.work[4 * t + 1] = items[t].hu;
-      P.work[4 * t + 2] = items[t].qt;
-      P.work[4 * t + 3] = items[t].cost;
     }
   }
   I.num_ctas = static_cast<int32_t>(std::min<int64_t>(I.num_units * I.ctas_per_unit,
