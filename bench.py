@@ -491,6 +491,40 @@ def time_append_cold(fi, device, n_sets=24, reps=20):
 
 
 # ----------------------------------------------------------------- oracle legs
+def time_plan_host(fi, device, reps=20):
+    """Host time of one fi_prefill_plan / fi_decode_plan call (the call a user
+    makes: host planning, the list copied into pinned staging, its upload
+    enqueued), median over `reps` calls with the stream idle before each (a
+    plan waits only when a third plan would reuse a staging buffer whose upload
+    the stream has not reached).  Batches of 64, 256 and 1024 sequences, H_q=32,
+    H_kv=8, D=128, page_size=16: uniform (1024 tokens each) and ragged (the
+    ragged workload's length distribution, log-uniform in [128, 16384])."""
+    ctx = fi.fi_context_create()
+    plan = fi.fi_plan_create(ctx)
+    out = {}
+    for B in (64, 256, 1024):
+        pt = torch.zeros((B, 16384 // 16), dtype=torch.int32, device=device)
+        for kind in ("uniform", "ragged"):
+            lens = np.full(B, 1024, np.int32) if kind == "uniform" else \
+                np.array(W.ragged_lengths(B, 128, 16384, 4000), np.int32)
+            ind = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+            calls = (("prefill", lambda: fi.fi_prefill_plan(plan, ind, ind, pt, 32, 8, 128, 16)),
+                     ("decode", lambda: fi.fi_decode_plan(plan, np.arange(B + 1, dtype=np.int32),
+                                                          ind, pt, 32, 8, 128, 16)))
+            for what, call in calls:
+                ts = []
+                for _ in range(reps + 2):
+                    torch.cuda.synchronize()
+                    t0 = time.perf_counter()
+                    call()
+                    ts.append(time.perf_counter() - t0)
+                out[f"{what}_{kind}_b{B}"] = float(np.median(ts[2:]) * 1e6)
+    torch.cuda.synchronize()
+    fi.fi_plan_destroy(plan)
+    fi.fi_context_destroy(ctx)
+    return out
+
+
 def oracle_sample(name, seed=0):
     """Times the CPU oracle on a fixed sample of workload `name`: sequences
     drawn with `seed` (same per-sequence shapes, freshly drawn seeded inputs)
@@ -746,6 +780,13 @@ def main():
             del r2, s2
             torch.cuda.empty_cache()
 
+    plan_us = None
+    if not args.no_extra and rank == 0:
+        plan_us = {"unit": "us per call", "what": "fi_prefill_plan / fi_decode_plan through the "
+                   "Python binding, stream idle (H_q=32, H_kv=8, D=128, ps=16; uniform: "
+                   "1024 tokens per sequence; ragged: log-uniform lengths in [128, 16384])",
+                   **time_plan_host(fi, device)}
+
     app = None
     if not args.no_append_bench and rank == 0:
         a = time_append_cold(fi, device)
@@ -787,6 +828,7 @@ def main():
         "append_in_step": append_in_step,
         "workloads": extra or None,
         "append_bench": app,
+        "plan_host_us": plan_us,
         "clocks": clk,
         "e2e": e2e,
         "gpu_launches": launches,

@@ -344,9 +344,9 @@ fi_status fi_decode_plan(fi_plan* plan, const int32_t* qo_indptr_host,
   plan->page_table_stride = page_table_stride;
   // the pieces, merges and warp offsets travel in the work-list, slot-unit
   // and slot-begin regions
-  P.work = P.dec_units;
-  P.slot_units = P.dec_merges;
-  P.slot_begin = P.dec_warp_off;
+  P.work.assign(P.dec_units.begin(), P.dec_units.end());
+  P.slot_units.assign(P.dec_merges.begin(), P.dec_merges.end());
+  P.slot_begin.assign(P.dec_warp_off.begin(), P.dec_warp_off.end());
   const size_t need = static_cast<size_t>(P.dec_parts) * P.dec_rows * (head_dim + 2);
   if (need > plan->part_floats) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -34,6 +34,24 @@ inline int32_t n_kv_tiles(int32_t qt, int32_t qo_len, int32_t kv_len) {
   return last_key / kTileKV + 1;
 }
 
+// Resets a plan for re-planning but keeps the capacity of its lists: a plan
+// object re-planned every step then allocates (and faults in) no memory once
+// its lists have reached their size.
+void reset_plan(HostPlan& P) {
+  std::vector<int32_t> keep[6] = {std::move(P.work),       std::move(P.slot_units),
+                                  std::move(P.slot_begin), std::move(P.dec_units),
+                                  std::move(P.dec_merges), std::move(P.dec_warp_off)};
+  P = HostPlan{};
+  std::vector<int32_t>* dst[6] = {&P.work,      &P.slot_units, &P.slot_begin,
+                                  &P.dec_units, &P.dec_merges, &P.dec_warp_off};
+  for (int i = 0; i < 6; ++i) {
+    // the work list keeps its contents: every plan resizes it and writes all
+    // of its entries, or clears it (no zero fill of a list about to be written)
+    if (i > 0) keep[i].clear();
+    *dst[i] = std::move(keep[i]);
+  }
+}
+
 // Plans with fewer units than this per slot are balanced.
 constexpr int64_t kBalanceUnitsPerSlot = 16;
 
@@ -94,7 +112,7 @@ fi_status plan_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t 
   if (batch > 0 && (qo_indptr[0] != 0 || kv_indptr[0] != 0)) return FI_ERR_INVALID_ARGUMENT;
 
   HostPlan& P = *out;
-  P = HostPlan{};
+  reset_plan(P);
   P.num_qo_heads = num_qo_heads;
   P.num_kv_heads = num_kv_heads;
   P.head_dim = head_dim;
@@ -150,6 +168,7 @@ fi_status plan_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t 
     P.uniform_kv_len = max_kv;
     I.num_units = static_cast<int64_t>(batch) * HU * I.q_tiles;
     const int64_t slots = std::max(ctas, I.ctas_per_unit) / I.ctas_per_unit;
+    P.work.clear();
     if (want_list || I.num_units < kBalanceUnitsPerSlot * slots) {
       P.work.resize(static_cast<size_t>(I.num_units) * 4);
       const int64_t BH = static_cast<int64_t>(batch) * HU;
@@ -258,7 +277,7 @@ fi_status plan_decode_host(const int32_t* qo_indptr, const int32_t* kv_indptr, i
     return FI_ERR_UNSUPPORTED;
   if (batch > 0 && (qo_indptr[0] != 0 || kv_indptr[0] != 0)) return FI_ERR_INVALID_ARGUMENT;
   HostPlan& P = *out;
-  P = HostPlan{};
+  reset_plan(P);
   P.decode = true;
   P.num_qo_heads = num_qo_heads;
   P.num_kv_heads = num_kv_heads;
@@ -308,8 +327,25 @@ fi_status plan_decode_host(const int32_t* qo_indptr, const int32_t* kv_indptr, i
       total == 0 ? 0
                  : std::max<int64_t>(1, std::min(resident, (total + kDecodeMinSteps - 1) /
                                                                 kDecodeMinSteps));
-  auto first_step = [&](int64_t w) { return w * total / W; };  // warp w's first step
+  // warp w's first step is floor(w * total / W): the W + 1 boundaries, by
+  // exact integer steps without a division per warp
+  std::vector<int64_t> bnd(static_cast<size_t>(W) + 2, total);
+  {
+    const int64_t q = W > 0 ? total / W : 0, r = W > 0 ? total % W : 0;
+    int64_t f = 0, rem = 0;
+    for (int64_t k = 0; k <= W; ++k) {
+      bnd[k] = f;
+      f += q;
+      rem += r;
+      if (rem >= W) {
+        ++f;
+        rem -= W;
+      }
+    }
+  }
+  auto first_step = [&](int64_t w) { return bnd[static_cast<size_t>(w)]; };
   P.dec_warp_off.assign(static_cast<size_t>(W) + 1, 0);
+  P.dec_units.reserve(static_cast<size_t>(4 * (W + static_cast<int64_t>(batch) * num_kv_heads)));
   int64_t s0 = 0, w = 0, slots = 0, pieces = 0;
   for (int32_t b = 0; b < batch; ++b) {
     const int32_t qo = qo_indptr[b + 1] - qo_indptr[b];

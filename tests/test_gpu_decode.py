@@ -179,3 +179,34 @@ def test_decode_full_size_sampled(name):
     res = compare_attention(out, lse, ref_out, ref_lse, rows=rows)
     print(name, info["num_units"], res)
     assert_within_tolerance(res)
+
+
+def test_one_plan_object_replanned_across_kinds():
+    """One plan object planned in turn for a ragged prefill, a decode, a
+    uniform prefill (no work list), a balanced prefill and the decode again:
+    every plan keeps only its own lists (the plan reuses their memory), and
+    every run matches the oracle."""
+    m = fi()
+    ctx = m.fi_context_create()
+    plan = m.fi_plan_create(ctx)
+    # tiny: one 64-token sequence, a balanced plan (slot lists)
+    for name in ["ragged_small", "decode_small", "uniform_small", "tiny", "decode_mixed"]:
+        d = device_inputs(name)
+        sp = d["spec"]
+        c = gpu_cache(d)
+        m.fi_nvfp4_append(ctx, d["k"], d["v"], c.k_scale, c.v_scale, d["slot_mapping"], c)
+        args = (plan, d["host"]["qo_indptr"], d["host"]["kv_indptr"], d["page_table"],
+                sp.num_qo_heads, sp.num_kv_heads, sp.head_dim, sp.page_size)
+        out = torch.empty_like(d["q"])
+        lse = torch.empty(d["q"].shape[:2], dtype=torch.float32, device="cuda")
+        if sp.attn == "decode":
+            m.fi_decode_plan(*args, sm_scale=d["sm_scale"])
+            m.fi_decode_run(plan, d["q"], c, out, lse)
+        else:
+            m.fi_prefill_plan(*args, sm_scale=d["sm_scale"])
+            m.fi_prefill_run(plan, d["q"], c, out, lse)
+        assert m.fi_device_status(ctx) == 0, name
+        ref_out, ref_lse = oracle_attention(d, oracle_cache(d))
+        assert_within_tolerance(compare_attention(out, lse, ref_out, ref_lse))
+    m.fi_plan_destroy(plan)
+    m.fi_context_destroy(ctx)
