@@ -97,6 +97,50 @@ def test_decode_repeated_runs_merge_every_time():
     m.fi_context_destroy(ctx)
 
 
+def test_decode_step_captured_in_a_cuda_graph():
+    """The append of the newest tokens, the decode and its merge captured in
+    one CUDA graph on a side stream: two replays give the bytes of the eager
+    calls, and the oracle's result."""
+    m = fi()
+    d = device_inputs("decode_mixed")
+    sp = d["spec"]
+    ctx = m.fi_context_create()
+    c = gpu_cache(d)
+    plan = m.fi_plan_create(ctx)
+    m.fi_decode_plan(plan, d["host"]["qo_indptr"], d["host"]["kv_indptr"], d["page_table"],
+                     sp.num_qo_heads, sp.num_kv_heads, sp.head_dim, sp.page_size,
+                     sm_scale=d["sm_scale"])
+    assert m.fi_plan_get_info(plan)["num_units"] > sp.batch * sp.num_kv_heads  # pairs merged
+
+    def step(stream=None):
+        m.fi_nvfp4_append(ctx, d["k"], d["v"], c.k_scale, c.v_scale, d["slot_mapping"], c,
+                          stream=stream)
+        m.fi_decode_run(plan, d["q"], c, out, lse, stream=stream)
+
+    out = torch.empty_like(d["q"])
+    lse = torch.empty(d["q"].shape[:2], dtype=torch.float32, device="cuda")
+    step()
+    torch.cuda.synchronize()
+    eager_out, eager_lse = out.clone(), lse.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            step(stream=s)
+    for _ in range(2):
+        out.fill_(float("nan"))
+        lse.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager_out) and torch.equal(lse, eager_lse)
+    assert m.fi_device_status(ctx) == 0
+    ref_out, ref_lse = oracle_attention(d, oracle_cache(d))
+    assert_within_tolerance(compare_attention(out, lse, ref_out, ref_lse))
+    m.fi_plan_destroy(plan)
+    m.fi_context_destroy(ctx)
+
+
 def test_decode_plan_limits_and_plan_kinds():
     m = fi()
     d = device_inputs("decode_small")
