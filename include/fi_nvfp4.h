@@ -257,9 +257,11 @@ fi_status fi_prefill_run_fp8(const fi_plan* plan, const void* q_dev, const fi_fp
 
 /* Host-only planning, for inspection and tests: fills `info` and, if
  * `work_out` is non-NULL, up to `work_capacity` work units as 4 int32 each
- * (sequence, head unit, q-tile, 0) in the order the kernel takes them
- * (uniform batches are decoded arithmetically and need no list).  Makes no
- * CUDA call.  `l2_bytes` is the L2 size for the gate. */
+ * (sequence, head unit, q-tile, KV tiles the unit reads) in the order the
+ * kernel numbers them.  (The device plan of a ragged batch holds one entry
+ * per (sequence, q-tile), whose head units are consecutive units; uniform
+ * batches are decoded arithmetically and need no list.)  Makes no CUDA call.
+ * `l2_bytes` is the L2 size for the gate. */
 fi_status fi_prefill_plan_host(const int32_t* qo_indptr_host, const int32_t* kv_indptr_host,
                                int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
                                int32_t head_dim, int32_t page_size, int64_t l2_bytes,
@@ -303,9 +305,10 @@ fi_status fi_decode_plan_host(const int32_t* qo_indptr_host, const int32_t* kv_i
  * Scratch: the indptr copies and, for ragged batches, the work-unit list are
  * kept in one fixed device array of 2 MiB (524288 int32 words) inside the
  * library, held by every GPU that loads it until the process exits.  A call
- * needs 4 + 2 (batch + 1) words, plus 4 per work unit for ragged batches
- * (units = sum over sequences of ceil(qo_len / 128) times the head units);
- * larger calls return FI_ERR_SCRATCH_TOO_SMALL and enqueue nothing.  Every
+ * needs 4 + 2 (batch + 1) words, plus 4 per (sequence, q-tile) for ragged
+ * batches (sum over sequences of ceil(qo_len / 128) entries, each standing for
+ * all head units of its q-tile); larger calls return FI_ERR_SCRATCH_TOO_SMALL
+ * and enqueue nothing.  Every
  * call shares the array: calls that overlap on the GPU (on different streams)
  * race; calls on one stream are ordered by the stream (each call's copies into
  * the array run after the previous call's kernel).  The indptr arrays are
@@ -314,7 +317,8 @@ fi_status fi_decode_plan_host(const int32_t* qo_indptr_host, const int32_t* kv_i
  * copy, so they must stay unchanged until then.  The first call on a device
  * looks up the array's device address; make that first call before any stream
  * capture.  Ragged work units are taken in sequence order with the heaviest
- * q-tile of each sequence first (dealt round-robin to the CTAs: no balanced
+ * q-tile of each sequence first, the head units of a q-tile together (dealt
+ * round-robin to the CTAs: no balanced
  * slot lists); groups of a multiple of 4 query heads run on CTA pairs, as
  * fi_prefill_plan chooses by default. */
 fi_status fi_prefill_noalloc(const int32_t* qo_indptr_host, const int32_t* kv_indptr_host,

@@ -311,7 +311,7 @@ fi_status fi_prefill_plan(fi_plan* plan, const int32_t* qo_indptr_host,
   const fi_context* ctx = plan->ctx;
   const int64_t l2 = (opts && opts->l2_bytes > 0) ? opts->l2_bytes : ctx->l2_bytes;
   fi_status st = fi::plan_host(qo_indptr_host, kv_indptr_host, batch, num_qo_heads, num_kv_heads,
-                               head_dim, page_size, sm_scale, l2, ctx->num_sms, opts, false,
+                               head_dim, page_size, sm_scale, l2, ctx->num_sms, opts,
                                &plan->host);
   if (st != FI_OK) return st;
   // page table rows must cover every sequence's pages

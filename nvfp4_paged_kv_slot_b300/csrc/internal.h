@@ -72,7 +72,11 @@ struct HostPlan {
   bool pair = false;              // units run on 2-CTA clusters sharing KV staging
   int32_t kv_format = 0;          // 0 NVFP4, 1 FP8
   float sm_scale = 0.0f;
-  std::vector<int32_t> work;      // 4 int32 per unit (ragged batches, and balanced plans)
+  // Ragged batches: one item per (sequence, q-tile) with queries, 4 int32
+  // each (sequence, q-tile, KV tiles, 0), in the kernel's order; unit u is
+  // head unit u % head_units of item u / head_units.  Empty for uniform
+  // batches, whose units the kernel decodes arithmetically.
+  std::vector<int32_t> work;
   // Balanced plans (few units per CTA slot): the work-list indices of each
   // slot's units, heaviest first; slot s runs slot_units[slot_begin[s] ..
   // slot_begin[s + 1]).  Empty otherwise (units are dealt round-robin).
@@ -125,11 +129,10 @@ struct DecodeArgs {
 fi_status launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
 // Validates the arguments and plans on the host only (no CUDA calls).
-// `want_list`: also fill the ordered work list for uniform batches.
 fi_status plan_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t batch,
                     int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
                     int32_t page_size, float sm_scale, int64_t l2_bytes, int32_t default_ctas,
-                    const fi_plan_options* opts, bool want_list, HostPlan* out);
+                    const fi_plan_options* opts, HostPlan* out);
 
 // ---- prefill -----------------------------------------------------------------
 struct PrefillArgs {

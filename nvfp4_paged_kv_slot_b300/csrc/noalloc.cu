@@ -26,7 +26,7 @@ namespace {
 constexpr int64_t kScratchWords = 1 << 19;
 constexpr int64_t kStatusWords = 4;
 constexpr int kMaxDevices = 64;
-constexpr int kChunkUnits = 1024;  // work units staged on the host stack per copy
+constexpr int kChunkItems = 1024;  // work-list items staged on the host stack per copy
 
 static __device__ __align__(256) int32_t g_prefill_scratch[kScratchWords];
 
@@ -148,7 +148,7 @@ extern "C" fi_status fi_prefill_noalloc(const int32_t* qo_indptr_host,
   const int64_t off_qo = kStatusWords;
   const int64_t off_kv = off_qo + nb;
   const int64_t off_work = (off_kv + nb + 3) & ~static_cast<int64_t>(3);
-  const int64_t words = off_work + (I.is_uniform ? 0 : 4 * I.num_units);
+  const int64_t words = off_work + (I.is_uniform ? 0 : 4 * (I.num_units / I.head_units));
   if (words > kScratchWords) return FI_ERR_SCRATCH_TOO_SMALL;
 
   int32_t* scratch = nullptr;
@@ -170,29 +170,28 @@ extern "C" fi_status fi_prefill_noalloc(const int32_t* qo_indptr_host,
                       cudaMemcpyHostToDevice, s) != cudaSuccess)
     return FI_ERR_CUDA;
   if (!I.is_uniform) {
-    // Ragged: units in sequence order, head units in order, q-tiles from the
-    // last (heaviest) to the first, staged through a fixed host buffer.
-    int32_t chunk[4 * kChunkUnits];
+    // Ragged: one item per (sequence, q-tile), sequences in order, q-tiles
+    // from the last (heaviest) to the first (the head units of an item are
+    // consecutive units), staged through a fixed host buffer.
+    int32_t chunk[4 * kChunkItems];
     int64_t done = 0;
     int n = 0;
     for (int32_t b = 0; b < batch; ++b) {
       const int32_t qo = qo_indptr_host[b + 1] - qo_indptr_host[b];
       const int32_t kv = kv_indptr_host[b + 1] - kv_indptr_host[b];
       const int32_t tiles = (qo + kTileQ - 1) / kTileQ;
-      for (int32_t hu = 0; hu < I.head_units; ++hu) {
-        for (int32_t qt = tiles - 1; qt >= 0; --qt) {
-          chunk[4 * n + 0] = b;
-          chunk[4 * n + 1] = hu;
-          chunk[4 * n + 2] = qt;
-          chunk[4 * n + 3] = kv_tiles_of(qt, qo, kv);
-          if (++n == kChunkUnits) {
-            if (cudaMemcpyAsync(scratch + off_work + 4 * done, chunk,
-                                static_cast<size_t>(n) * 4 * sizeof(int32_t),
-                                cudaMemcpyHostToDevice, s) != cudaSuccess)
-              return FI_ERR_CUDA;
-            done += n;
-            n = 0;
-          }
+      for (int32_t qt = tiles - 1; qt >= 0; --qt) {
+        chunk[4 * n + 0] = b;
+        chunk[4 * n + 1] = qt;
+        chunk[4 * n + 2] = kv_tiles_of(qt, qo, kv);
+        chunk[4 * n + 3] = 0;
+        if (++n == kChunkItems) {
+          if (cudaMemcpyAsync(scratch + off_work + 4 * done, chunk,
+                              static_cast<size_t>(n) * 4 * sizeof(int32_t),
+                              cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return FI_ERR_CUDA;
+          done += n;
+          n = 0;
         }
       }
     }

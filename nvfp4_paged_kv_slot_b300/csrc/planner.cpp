@@ -55,15 +55,47 @@ void reset_plan(HostPlan& P) {
 // Plans with fewer units than this per slot are balanced.
 constexpr int64_t kBalanceUnitsPerSlot = 16;
 
-// Longest-processing-time-first assignment of the work list's units to
-// `slots` slots; a unit costs its KV tiles plus one for its Q load and
-// epilogue.
-void balance(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t slots, HostPlan& P) {
-  const int64_t n = static_cast<int64_t>(P.work.size() / 4);
+// (sequence, head unit, q-tile, KV tiles) of unit t: the arithmetic decoding
+// of uniform batches ([#3575] §1, §2), or item t / head_units of the list.
+void unit_entry(const HostPlan& P, int64_t t, int32_t* e) {
+  const fi_plan_info& I = P.info;
+  const int64_t HU = I.head_units;
+  if (I.is_uniform) {
+    const int64_t B = I.batch;
+    int64_t b, hu, qt;
+    if (I.global_reverse) {
+      qt = I.q_tiles - 1 - t / (B * HU);
+      const int64_t r = t % (B * HU);
+      hu = r / B;
+      b = r % B;
+    } else {
+      b = t / (HU * I.q_tiles);
+      const int64_t r = t % (HU * I.q_tiles);
+      hu = r / I.q_tiles;
+      qt = I.q_tiles - 1 - r % I.q_tiles;
+    }
+    e[0] = static_cast<int32_t>(b);
+    e[1] = static_cast<int32_t>(hu);
+    e[2] = static_cast<int32_t>(qt);
+    e[3] = n_kv_tiles(static_cast<int32_t>(qt), P.uniform_qo_len, P.uniform_kv_len);
+  } else {
+    const int32_t* item = P.work.data() + 4 * (t / HU);
+    e[0] = item[0];
+    e[1] = static_cast<int32_t>(t % HU);
+    e[2] = item[1];
+    e[3] = item[2];
+  }
+}
+
+// Longest-processing-time-first assignment of the plan's units to `slots`
+// slots; a unit costs its KV tiles plus one for its Q load and epilogue.
+void balance(int32_t slots, HostPlan& P) {
+  const int64_t n = P.info.num_units;
   std::vector<int32_t> cost(static_cast<size_t>(n));
   for (int64_t t = 0; t < n; ++t) {
-    const int32_t b = P.work[4 * t + 0], qt = P.work[4 * t + 2];
-    cost[t] = n_kv_tiles(qt, qo_indptr[b + 1] - qo_indptr[b], kv_indptr[b + 1] - kv_indptr[b]) + 1;
+    int32_t e[4];
+    unit_entry(P, t, e);
+    cost[t] = e[3] + 1;
   }
   std::vector<int32_t> order(static_cast<size_t>(n));
   std::iota(order.begin(), order.end(), 0);
@@ -96,7 +128,7 @@ void balance(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t slots, 
 fi_status plan_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t batch,
                     int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
                     int32_t page_size, float sm_scale, int64_t l2_bytes, int32_t default_ctas,
-                    const fi_plan_options* opts, bool want_list, HostPlan* out) {
+                    const fi_plan_options* opts, HostPlan* out) {
   if (!out || batch < 0 || (batch > 0 && (!qo_indptr || !kv_indptr)))
     return FI_ERR_INVALID_ARGUMENT;
   if (num_kv_heads <= 0 || num_qo_heads <= 0 || num_qo_heads % num_kv_heads != 0)
@@ -164,60 +196,38 @@ fi_status plan_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t 
   const int32_t HU = I.head_units;
   const int32_t ctas = (opts && opts->num_ctas > 0) ? opts->num_ctas : default_ctas;
   if (I.is_uniform) {
+    // no list: the kernel decodes uniform units arithmetically
     P.uniform_qo_len = max_qo;
     P.uniform_kv_len = max_kv;
     I.num_units = static_cast<int64_t>(batch) * HU * I.q_tiles;
-    const int64_t slots = std::max(ctas, I.ctas_per_unit) / I.ctas_per_unit;
     P.work.clear();
-    if (want_list || I.num_units < kBalanceUnitsPerSlot * slots) {
-      P.work.resize(static_cast<size_t>(I.num_units) * 4);
-      const int64_t BH = static_cast<int64_t>(batch) * HU;
-      for (int64_t t = 0; t < I.num_units; ++t) {
-        int64_t b, hu, qt;
-        if (I.global_reverse) {
-          qt = I.q_tiles - 1 - t / BH;
-          const int64_t r = t % BH;
-          hu = r / batch;
-          b = r % batch;
-        } else {
-          b = t / (static_cast<int64_t>(HU) * I.q_tiles);
-          const int64_t r = t % (static_cast<int64_t>(HU) * I.q_tiles);
-          hu = r / I.q_tiles;
-          qt = I.q_tiles - 1 - r % I.q_tiles;
-        }
-        P.work[4 * t + 0] = static_cast<int32_t>(b);
-        P.work[4 * t + 1] = static_cast<int32_t>(hu);
-        P.work[4 * t + 2] = static_cast<int32_t>(qt);
-        P.work[4 * t + 3] = 0;
-      }
-    }
   } else {
-    // Ragged: one unit per (sequence, head unit, q-tile) with its cost in KV
-    // tiles, written straight into the list in the kernel's order.
-    int64_t n = 0;
+    // Ragged: one item per (sequence, q-tile) with its cost in KV tiles,
+    // written straight into the list in the kernel's order; the head units of
+    // an item are consecutive units.
+    int64_t items = 0;
     for (int32_t b = 0; b < batch; ++b)
-      n += static_cast<int64_t>((qo_indptr[b + 1] - qo_indptr[b] + kTileQ - 1) / kTileQ) * HU;
-    I.num_units = n;
-    P.work.resize(static_cast<size_t>(n) * 4);
+      items += (qo_indptr[b + 1] - qo_indptr[b] + kTileQ - 1) / kTileQ;
+    I.num_units = items * HU;
+    P.work.resize(static_cast<size_t>(items) * 4);
     int32_t* w = P.work.data();
-    auto put = [](int32_t* e, int32_t b, int32_t hu, int32_t qt, int32_t cost) {
+    auto put = [](int32_t* e, int32_t b, int32_t qt, int32_t cost) {
       e[0] = b;
-      e[1] = hu;
-      e[2] = qt;
-      e[3] = cost;
+      e[1] = qt;
+      e[2] = cost;
+      e[3] = 0;
     };
     if (I.global_reverse) {
-      // Heaviest tiles of all sequences and heads first; ties keep the
-      // head-then-sequence order of the page's global mapping.  The costs are
-      // small integers, so a stable counting sort by cost (descending) puts
-      // every unit in place in two passes.
+      // Heaviest q-tiles of all sequences first (ties in sequence, then
+      // q-tile order).  The costs are small integers, so a stable counting
+      // sort by cost (descending) puts every item in place in two passes.
       const int32_t max_cost = max_kv / kTileKV + 1;
       std::vector<int64_t> pos(static_cast<size_t>(max_cost) + 2, 0);
       for (int32_t b = 0; b < batch; ++b) {
         const int32_t qo = qo_indptr[b + 1] - qo_indptr[b];
         const int32_t kv = kv_indptr[b + 1] - kv_indptr[b];
         const int32_t tiles = (qo + kTileQ - 1) / kTileQ;
-        for (int32_t qt = 0; qt < tiles; ++qt) pos[n_kv_tiles(qt, qo, kv)] += HU;
+        for (int32_t qt = 0; qt < tiles; ++qt) ++pos[n_kv_tiles(qt, qo, kv)];
       }
       int64_t acc = 0;  // first position of each cost, highest cost first
       for (int32_t c = max_cost + 1; c >= 0; --c) {
@@ -229,15 +239,15 @@ fi_status plan_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t 
         const int32_t qo = qo_indptr[b + 1] - qo_indptr[b];
         const int32_t kv = kv_indptr[b + 1] - kv_indptr[b];
         const int32_t tiles = (qo + kTileQ - 1) / kTileQ;
-        for (int32_t hu = 0; hu < HU; ++hu)
-          for (int32_t qt = 0; qt < tiles; ++qt) {
-            const int32_t cost = n_kv_tiles(qt, qo, kv);
-            put(w + 4 * pos[cost]++, b, hu, qt, cost);
-          }
+        for (int32_t qt = 0; qt < tiles; ++qt) {
+          const int32_t cost = n_kv_tiles(qt, qo, kv);
+          put(w + 4 * pos[cost]++, b, qt, cost);
+        }
       }
     } else {
-      // per (sequence, head unit) groups, reversed q-tiles inside each group;
-      // groups ordered longest first so the longest chains start early
+      // per sequence, q-tiles from the last (heaviest) to the first, all head
+      // units of a q-tile together; sequences longest first so the longest
+      // chains start early
       std::vector<int32_t> order(batch);
       std::iota(order.begin(), order.end(), 0);
       std::stable_sort(order.begin(), order.end(), [&](int32_t x, int32_t y) {
@@ -247,8 +257,7 @@ fi_status plan_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t 
         const int32_t qo = qo_indptr[b + 1] - qo_indptr[b];
         const int32_t kv = kv_indptr[b + 1] - kv_indptr[b];
         const int32_t tiles = (qo + kTileQ - 1) / kTileQ;
-        for (int32_t hu = 0; hu < HU; ++hu)
-          for (int32_t qt = tiles - 1; qt >= 0; --qt, w += 4) put(w, b, hu, qt, n_kv_tiles(qt, qo, kv));
+        for (int32_t qt = tiles - 1; qt >= 0; --qt, w += 4) put(w, b, qt, n_kv_tiles(qt, qo, kv));
       }
     }
   }
@@ -256,8 +265,8 @@ fi_status plan_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t 
                                                       std::max(ctas, I.ctas_per_unit)));
   if (P.pair) I.num_ctas &= ~1;
   const int32_t slots = I.num_ctas / I.ctas_per_unit;
-  if (slots > 0 && !P.work.empty() && I.num_units < kBalanceUnitsPerSlot * slots)
-    balance(qo_indptr, kv_indptr, slots, P);
+  if (slots > 0 && I.num_units > 0 && I.num_units < kBalanceUnitsPerSlot * slots)
+    balance(slots, P);
   return FI_OK;
 }
 
@@ -435,12 +444,12 @@ extern "C" fi_status fi_prefill_plan_host(const int32_t* qo_indptr_host,
   fi::HostPlan P;
   const fi_status st = fi::plan_host(qo_indptr_host, kv_indptr_host, batch, num_qo_heads,
                                      num_kv_heads, head_dim, page_size, 0.0f, l2_bytes, 148,
-                                     opts, work_out != nullptr, &P);
+                                     opts, &P);
   if (st != FI_OK) return st;
   *info = P.info;
   if (work_out) {
     const int64_t n = std::min<int64_t>(work_capacity, P.info.num_units);
-    std::memcpy(work_out, P.work.data(), static_cast<size_t>(n) * 4 * sizeof(int32_t));
+    for (int64_t t = 0; t < n; ++t) fi::unit_entry(P, t, work_out + 4 * t);
   }
   return FI_OK;
 }

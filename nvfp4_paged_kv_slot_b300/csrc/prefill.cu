@@ -74,7 +74,28 @@ struct PrefillParams {
   int32_t num_units;
   float sm_scale;
   int32_t out_align32;  // `out` is 32-byte aligned: 32-byte stores in the epilogue
+  // unit -> work-list item: u / head_units by one multiply-high and shifts
+  uint32_t hu_magic, hu_sh1, hu_sh2;
 };
+
+// Division by a divisor fixed for the launch (Granlund and Montgomery,
+// "Division by Invariant Integers using Multiplication", 1994, the unsigned
+// method of their Figure 4.1): with l = ceil(log2 d) and
+// m = floor(2^32 (2^l - d) / d) + 1, n / d = (t + ((n - t) >> min(l, 1)))
+// >> max(l - 1, 0) where t = mulhi(m, n), exact for every 32-bit n.
+void divisor_magic(uint32_t d, uint32_t* m, uint32_t* sh1, uint32_t* sh2) {
+  uint32_t l = 0;
+  while ((uint64_t{1} << l) < d) ++l;
+  *m = static_cast<uint32_t>(((uint64_t{1} << 32) * ((uint64_t{1} << l) - d)) / d + 1);
+  *sh1 = l < 1 ? l : 1;
+  *sh2 = l > 1 ? l - 1 : 0;
+}
+
+__device__ __forceinline__ uint32_t div_by_magic(uint32_t n, uint32_t m, uint32_t sh1,
+                                                 uint32_t sh2) {
+  const uint32_t t = __umulhi(m, n);
+  return (t + ((n - t) >> sh1)) >> sh2;
+}
 
 // PAIR: a 2-CTA cluster shares its KV staging tiles; each CTA loads and
 // repacks half of every tile's rows (64 of 128) and writes them into both
@@ -151,10 +172,14 @@ __device__ __forceinline__ Unit decode_unit(const PrefillParams& p, int u, int h
     w.kv_len = p.uni_kv_len;
     w.qo_start = w.b * p.uni_qo_len;
   } else {
-    const int4 it = __ldg(p.work + u);
+    // the list holds one item per (sequence, q-tile); its head units are
+    // consecutive units
+    const int item = static_cast<int>(
+        div_by_magic(static_cast<uint32_t>(u), p.hu_magic, p.hu_sh1, p.hu_sh2));
+    hu = u - item * p.head_units;
+    const int4 it = __ldg(p.work + item);
     w.b = it.x;
-    hu = it.y;
-    w.qt = it.z;
+    w.qt = it.y;
     w.qo_start = __ldg(p.qo_indptr + w.b);
     w.qo_len = __ldg(p.qo_indptr + w.b + 1) - w.qo_start;
     w.kv_len = __ldg(p.kv_indptr + w.b + 1) - __ldg(p.kv_indptr + w.b);
@@ -879,6 +904,8 @@ fi_status launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.group = P.group;
   p.units_per_kv_head = P.units_per_kv_head;
   p.head_units = P.info.head_units;
+  divisor_magic(static_cast<uint32_t>(std::max(P.info.head_units, 1)), &p.hu_magic, &p.hu_sh1,
+                &p.hu_sh2);
   p.uniform = (P.info.is_uniform && !a.work_dev) ? 1 : 0;  // else: decode from the work list
   p.slot_units = a.slot_units_dev;
   p.slot_begin = a.slot_begin_dev;

@@ -123,16 +123,16 @@ def test_ragged_work_list(schedule):
     assert sorted(got) == sorted(want) and len(got) == len(want)
     for b, hu, qt, cost in work:
         assert cost == _n_kv(qt, qo[b], kv[b])
-    if schedule == 1:   # global: heaviest first
-        assert all(work[i, 3] >= work[i + 1, 3] for i in range(len(work) - 1))
-    else:               # per (sequence, head unit): contiguous, q-tiles reversed
-        seen = []
-        for b, hu, qt, _ in work:
-            if not seen or seen[-1][:2] != (b, hu):
-                seen.append((b, hu, qt))
-            else:
-                assert qt == seen[-1][2] - 1
-                seen[-1] = (b, hu, qt)
+    # the head units of one (sequence, q-tile) are consecutive units, in order
+    assert [int(w[1]) for w in work] == [t % HU for t in range(len(work))]
+    items = [(int(w[0]), int(w[2]), int(w[3])) for w in work[::HU]]
+    assert all(tuple(work[t, [0, 2, 3]]) == items[t // HU] for t in range(len(work)))
+    if schedule == 1:   # global: heaviest first, ties in (sequence, q-tile) order
+        assert items == sorted(items, key=lambda x: (-x[2], x[0], x[1]))
+    else:               # per sequence (longest first, stable), q-tiles reversed
+        order = sorted(range(len(qo)), key=lambda b: -kv[b])
+        assert items == [(b, qt, _n_kv(qt, qo[b], kv[b])) for b in order
+                         for qt in reversed(range((qo[b] + 127) // 128))]
 
 
 @pytest.mark.parametrize("args,code", [
