@@ -152,10 +152,10 @@ def spec(name: str) -> Spec:
     if name == "offset_uniform_small":
         return Spec("offset_uniform_small", 16000, num_kv_heads=2, head_dim=128, page_size=16,
                     num_qo_heads=8, seq_lens=[600] * 4, qo_lens=[200] * 4)
-    # Many ragged work units (more than a thousand q-tiles x head units).
+    # Many ragged work units (more than two thousand (sequence, q-tile) items).
     if name == "many_units":
         return Spec("many_units", 17000, num_kv_heads=2, head_dim=128, page_size=16,
-                    num_qo_heads=8, seq_lens=ragged_lengths(128, 1, 4000, 17000))
+                    num_qo_heads=8, seq_lens=ragged_lengths(512, 1, 4000, 17000))
     raise KeyError(name)
 
 
