@@ -48,6 +48,15 @@ constexpr int kRepackThreads = 128;
 // Devices whose cluster occupancy is cached by the launcher.
 constexpr int kMaxDevices = 64;
 
+// n / d and n % d for a divisor fixed for the launch (fast_div below).
+struct FastDiv {
+  uint32_t d, m, sh1, sh2;
+  __device__ __forceinline__ int div(int n) const {
+    const uint32_t t = __umulhi(m, static_cast<uint32_t>(n));
+    return static_cast<int>((t + ((static_cast<uint32_t>(n) - t) >> sh1)) >> sh2);
+  }
+};
+
 struct PrefillParams {
   CUtensorMap tmap_q;  // 3-D view of q: (head_dim, num_qo_heads, total_qo)
   const __nv_bfloat16* q;  // the same memory (L2 prefetch before the grid wait)
@@ -74,8 +83,10 @@ struct PrefillParams {
   int32_t num_units;
   float sm_scale;
   int32_t out_align32;  // `out` is 32-byte aligned: 32-byte stores in the epilogue
-  // unit -> work-list item: u / head_units by one multiply-high and shifts
-  uint32_t hu_magic, hu_sh1, hu_sh2;
+  // divisions of the tile decoding, by one multiply-high and shifts each:
+  // head units, batch * head units, batch, head units * q-tiles, q-tiles,
+  // head units per KV head
+  FastDiv div_hu, div_bh, div_b, div_per_b, div_qt, div_upk;
 };
 
 // Division by a divisor fixed for the launch (Granlund and Montgomery,
@@ -83,18 +94,15 @@ struct PrefillParams {
 // method of their Figure 4.1): with l = ceil(log2 d) and
 // m = floor(2^32 (2^l - d) / d) + 1, n / d = (t + ((n - t) >> min(l, 1)))
 // >> max(l - 1, 0) where t = mulhi(m, n), exact for every 32-bit n.
-void divisor_magic(uint32_t d, uint32_t* m, uint32_t* sh1, uint32_t* sh2) {
+FastDiv fast_div(uint32_t d) {
+  FastDiv f;
+  f.d = d < 1 ? 1 : d;
   uint32_t l = 0;
-  while ((uint64_t{1} << l) < d) ++l;
-  *m = static_cast<uint32_t>(((uint64_t{1} << 32) * ((uint64_t{1} << l) - d)) / d + 1);
-  *sh1 = l < 1 ? l : 1;
-  *sh2 = l > 1 ? l - 1 : 0;
-}
-
-__device__ __forceinline__ uint32_t div_by_magic(uint32_t n, uint32_t m, uint32_t sh1,
-                                                 uint32_t sh2) {
-  const uint32_t t = __umulhi(m, n);
-  return (t + ((n - t) >> sh1)) >> sh2;
+  while ((uint64_t{1} << l) < f.d) ++l;
+  f.m = static_cast<uint32_t>(((uint64_t{1} << 32) * ((uint64_t{1} << l) - f.d)) / f.d + 1);
+  f.sh1 = l < 1 ? l : 1;
+  f.sh2 = l > 1 ? l - 1 : 0;
+  return f;
 }
 
 // PAIR: a 2-CTA cluster shares its KV staging tiles; each CTA loads and
@@ -155,18 +163,17 @@ __device__ __forceinline__ Unit decode_unit(const PrefillParams& p, int u, int h
   Unit w;
   int hu;
   if (p.uniform) {
-    const int BH = p.batch * p.head_units;
     if (p.global_reverse) {
-      w.qt = p.q_tiles - 1 - u / BH;
-      const int r = u % BH;
-      hu = r / p.batch;
-      w.b = r % p.batch;
+      const int t = p.div_bh.div(u);  // u / (batch * head units)
+      w.qt = p.q_tiles - 1 - t;
+      const int r = u - t * static_cast<int>(p.div_bh.d);
+      hu = p.div_b.div(r);
+      w.b = r - hu * p.batch;
     } else {
-      const int per_b = p.head_units * p.q_tiles;
-      w.b = u / per_b;
-      const int r = u % per_b;
-      hu = r / p.q_tiles;
-      w.qt = p.q_tiles - 1 - r % p.q_tiles;
+      w.b = p.div_per_b.div(u);  // u / (head units * q-tiles)
+      const int r = u - w.b * static_cast<int>(p.div_per_b.d);
+      hu = p.div_qt.div(r);
+      w.qt = p.q_tiles - 1 - (r - hu * p.q_tiles);
     }
     w.qo_len = p.uni_qo_len;
     w.kv_len = p.uni_kv_len;
@@ -174,8 +181,7 @@ __device__ __forceinline__ Unit decode_unit(const PrefillParams& p, int u, int h
   } else {
     // the list holds one item per (sequence, q-tile); its head units are
     // consecutive units
-    const int item = static_cast<int>(
-        div_by_magic(static_cast<uint32_t>(u), p.hu_magic, p.hu_sh1, p.hu_sh2));
+    const int item = p.div_hu.div(u);
     hu = u - item * p.head_units;
     const int4 it = __ldg(p.work + item);
     w.b = it.x;
@@ -184,8 +190,8 @@ __device__ __forceinline__ Unit decode_unit(const PrefillParams& p, int u, int h
     w.qo_len = __ldg(p.qo_indptr + w.b + 1) - w.qo_start;
     w.kv_len = __ldg(p.kv_indptr + w.b + 1) - __ldg(p.kv_indptr + w.b);
   }
-  w.hk = hu / p.units_per_kv_head;
-  w.hq0 = w.hk * p.group + (hu % p.units_per_kv_head) * heads_per_unit + head_off;
+  w.hk = p.div_upk.div(hu);
+  w.hq0 = w.hk * p.group + (hu - w.hk * p.units_per_kv_head) * heads_per_unit + head_off;
   const int last_row = min(w.qo_len, (w.qt + 1) * kTileQ) - 1;
   w.n_kv = (last_row + w.kv_len - w.qo_len) / kTileKV + 1;
   return w;
@@ -904,8 +910,8 @@ fi_status launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.group = P.group;
   p.units_per_kv_head = P.units_per_kv_head;
   p.head_units = P.info.head_units;
-  divisor_magic(static_cast<uint32_t>(std::max(P.info.head_units, 1)), &p.hu_magic, &p.hu_sh1,
-                &p.hu_sh2);
+  p.div_hu = fast_div(static_cast<uint32_t>(P.info.head_units));
+  p.div_upk = fast_div(static_cast<uint32_t>(P.units_per_kv_head));
   p.uniform = (P.info.is_uniform && !a.work_dev) ? 1 : 0;  // else: decode from the work list
   p.slot_units = a.slot_units_dev;
   p.slot_begin = a.slot_begin_dev;
@@ -914,6 +920,11 @@ fi_status launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.uni_qo_len = P.uniform_qo_len;
   p.uni_kv_len = P.uniform_kv_len;
   p.q_tiles = P.info.q_tiles;
+  p.div_b = fast_div(static_cast<uint32_t>(P.info.batch));
+  p.div_qt = fast_div(static_cast<uint32_t>(P.info.q_tiles));
+  p.div_bh = fast_div(static_cast<uint32_t>(P.info.batch) * static_cast<uint32_t>(P.info.head_units));
+  p.div_per_b =
+      fast_div(static_cast<uint32_t>(P.info.head_units) * static_cast<uint32_t>(P.info.q_tiles));
   if (P.info.num_units > 0x7FFFFFFF) return FI_ERR_UNSUPPORTED;
   p.num_units = static_cast<int32_t>(P.info.num_units);
   p.sm_scale = P.sm_scale;
