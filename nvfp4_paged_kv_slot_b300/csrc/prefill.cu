@@ -48,7 +48,8 @@ constexpr int kRepackThreads = 128;
 // Devices whose cluster occupancy is cached by the launcher.
 constexpr int kMaxDevices = 64;
 
-// n / d and n % d for a divisor fixed for the launch (fast_div below).
+// n / d for a divisor d fixed for the launch and any n in [0, 2^31) (fast_div
+// below gives the constants; the remainder is n - (n / d) d).
 struct FastDiv {
   uint32_t d, m, sh1, sh2;
   __device__ __forceinline__ int div(int n) const {
