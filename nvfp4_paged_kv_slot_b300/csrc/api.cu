@@ -477,6 +477,6 @@ const char* fi_status_string(fi_status status) {
   }
 }
 
-int32_t fi_version(void) { return 200; }
+int32_t fi_version(void) { return 201; }
 
 }  // extern "C"
