@@ -150,17 +150,27 @@ __global__ void __launch_bounds__(32 * kTWarps, NT == 1 ? 4 : NT == 2 ? 3 : 2)
   constexpr int kVW = D / 64;                // code words of a key a lane converts for O^T
   constexpr bool kQs = NT >= 2;              // Q^T fragments in shared memory
   extern __shared__ __align__(16) uint8_t dsm[];
-  grid_dep_wait();  // Q and the cache may come from the previous grid
-  grid_dep_launch();
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int g = lane / 4, t = lane % 4;
   const int wid = blockIdx.x * kTWarps + warp;
+  // The plan's memory (the warp's pieces) is written by no kernel (its copy
+  // completed before the previous grid started): read it while the previous
+  // grid finishes.  Q and the cache may come from the previous grid: after
+  // the wait.
+  int u_begin = 0, u_end = 0;
+  int4 w_first = make_int4(0, 0, 0, 0);
+  if (wid < p.num_warps) {
+    u_begin = __ldg(p.warp_off + wid);
+    u_end = __ldg(p.warp_off + wid + 1);
+    if (u_begin < u_end) w_first = __ldg(p.units + u_begin);
+  }
+  grid_dep_wait();
+  grid_dep_launch();
   if (wid >= p.num_warps) return;  // no block-wide barrier below
-  const int u_end = __ldg(p.warp_off + wid + 1);
-  for (int u = __ldg(p.warp_off + wid); u < u_end; ++u) {
+  for (int u = u_begin; u < u_end; ++u) {
     __syncwarp();  // every lane is done with the previous piece's ring
-    const int4 w = __ldg(p.units + u);
+    const int4 w = u == u_begin ? w_first : __ldg(p.units + u);
     const int b = w.x / p.num_kv_heads, hk = w.x - b * p.num_kv_heads, slot = w.w;
     const int qo_start = __ldg(p.qo_indptr + b);
     const int qo_len = __ldg(p.qo_indptr + b + 1) - qo_start;
@@ -608,16 +618,22 @@ __global__ void __launch_bounds__(32 * kTWarps, NT == 1 ? 4 : NT == 2 ? 3 : 2)
 template <int D>
 __global__ void __launch_bounds__(128) nvfp4_decode_merge_kernel(const DecodeParams p) {
   constexpr int kDpl = D / 32;
-  grid_dep_wait();
-  grid_dep_launch();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
   const int lane = threadIdx.x % 32;
   const int item = warp / p.rows, r = warp % p.rows;
+  // the merge item and the lengths are plan memory (no kernel writes it):
+  // read while the decode kernel finishes; its partial results after the wait
+  int4 w = make_int4(0, 0, 0, 0);
+  int qo_start = 0, qo_len = 0;
+  if (item < p.num_merges) {
+    w = __ldg(p.merges + item);
+    qo_start = __ldg(p.qo_indptr + w.x);
+    qo_len = __ldg(p.qo_indptr + w.x + 1) - qo_start;
+  }
+  grid_dep_wait();
+  grid_dep_launch();
   if (item >= p.num_merges) return;
-  const int4 w = __ldg(p.merges + item);
   const int b = w.x, hk = w.y, first = w.z, n = w.w;
-  const int qo_start = __ldg(p.qo_indptr + b);
-  const int qo_len = __ldg(p.qo_indptr + b + 1) - qo_start;
   const int G = p.group;
   if (r >= G * qo_len) return;
   float M = -INFINITY;
