@@ -79,6 +79,17 @@ def spec(name: str) -> Spec:
     if name == "ragged":
         return Spec("ragged", 4000, num_kv_heads=8, head_dim=128, page_size=16,
                     num_qo_heads=32, seq_lens=ragged_lengths(256, 128, 16384, 4000))
+    # Other shapes of the uniform batch, for the measurements of head_dim 64,
+    # a GQA group of 8 and 64-token pages (first 256 sequences in the bench).
+    if name == "uniform_d64":
+        return Spec("uniform_d64", 3100, num_kv_heads=8, head_dim=64, page_size=16,
+                    num_qo_heads=32, seq_lens=[1024] * 1024)
+    if name == "uniform_g8":
+        return Spec("uniform_g8", 3200, num_kv_heads=8, head_dim=128, page_size=16,
+                    num_qo_heads=64, seq_lens=[1024] * 1024)
+    if name == "uniform_ps64":
+        return Spec("uniform_ps64", 3300, num_kv_heads=8, head_dim=128, page_size=64,
+                    num_qo_heads=32, seq_lens=[1024] * 1024)
     # Small cases for the parity tests: several tiles and ragged tails.
     if name == "ragged_small":
         return Spec("ragged_small", 5000, num_kv_heads=2, head_dim=128, page_size=16,
