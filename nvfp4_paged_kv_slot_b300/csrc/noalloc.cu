@@ -125,7 +125,7 @@ extern "C" fi_status fi_prefill_noalloc(const int32_t* qo_indptr_host,
       cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return FI_ERR_CUDA;
-  I.global_reverse = (2 * I.kv_bytes <= l2) ? 1 : 0;
+  I.global_reverse = (I.is_uniform || 2 * I.kv_bytes <= l2) ? 1 : 0;  // as fi_prefill_plan
   if (I.is_uniform) {
     P.uniform_qo_len = max_qo;
     P.uniform_kv_len = max_kv;

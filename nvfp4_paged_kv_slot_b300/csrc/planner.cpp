@@ -190,7 +190,16 @@ fi_status plan_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t 
   } else if (schedule == 2) {
     I.global_reverse = 0;
   } else {
-    I.global_reverse = (2 * I.kv_bytes <= l2_bytes) ? 1 : 0;
+    // [#3575] §3's gate (the global order only when the KV cache fits in half
+    // of L2) decides for ragged batches.  Uniform batches always take the
+    // global order: all units of a q-step cost the same, so the persistent
+    // CTAs run balanced waves, and the KV re-reads from HBM that the gate
+    // guards against are cheap for this kernel (a KV tile feeds 4 heads x 128
+    // rows of MMAs: even with every tile read from HBM the prefill needs under
+    // a tenth of the HBM bandwidth).  Measured on the 1024 x 1024 batch (1.2 GB
+    // of KV): 811 TFLOP/s in the global order against 757 in the per-(sequence,
+    // head) one; on the ragged batch the gate's choice wins (1086 against 1065).
+    I.global_reverse = (I.is_uniform || 2 * I.kv_bytes <= l2_bytes) ? 1 : 0;
   }
 
   const int32_t HU = I.head_units;

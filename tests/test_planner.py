@@ -93,15 +93,23 @@ def test_uniform_check_is_totals_based():
 
 
 def test_l2_gate():
+    """Ragged batches: the global order only while 2 * kv_bytes <= L2.  Uniform
+    batches take the global order at any size."""
     H_kv, D = 8, 128
     per_token = H_kv * 2 * (D // 2 + D // 16)        # NVFP4 K and V bytes per token
     fits = (L2 // 2) // per_token                    # 2 * kv_bytes <= L2
-    ind = fi.indptr_from_lens([fits])
+    ind = fi.indptr_from_lens([fits - 100, 100])
     info, _ = fi.fi_prefill_plan_host(ind, ind, 32, H_kv, D, 16, l2_bytes=L2, with_list=False)
+    assert info["is_uniform"] == 0
     assert info["kv_bytes"] == fits * per_token and info["global_reverse"] == 1
-    ind = fi.indptr_from_lens([fits + 1])
+    ind = fi.indptr_from_lens([fits - 99, 100])
     info, _ = fi.fi_prefill_plan_host(ind, ind, 32, H_kv, D, 16, l2_bytes=L2, with_list=False)
     assert info["global_reverse"] == 0
+    for lens in ([fits + 1], [1024] * 1024):
+        ind = fi.indptr_from_lens(lens)
+        info, _ = fi.fi_prefill_plan_host(ind, ind, 32, H_kv, D, 16, l2_bytes=L2, with_list=False)
+        assert info["is_uniform"] == 1 and 2 * info["kv_bytes"] > L2
+        assert info["global_reverse"] == 1
 
 
 def _n_kv(qt, qo, kv):
@@ -164,7 +172,8 @@ def test_workload_shapes():
     import workloads as W
     info, _ = fi.fi_prefill_plan_host(*([fi.indptr_from_lens(W.spec("uniform").seq_lens)] * 2),
                                       32, 8, 128, 16, with_list=False)
-    assert info["is_uniform"] == 1 and info["global_reverse"] == 0   # 1.2 GB KV > L2
+    # 1.2 GB of KV does not fit in L2, but a uniform batch takes the global order
+    assert info["is_uniform"] == 1 and info["global_reverse"] == 1
     # G = 4: one unit per (sequence, kv head, q-tile), on a CTA pair
     assert info["ctas_per_unit"] == 2 and info["num_units"] == 1024 * 8 * 8
     sp = W.spec("single")
@@ -173,6 +182,9 @@ def test_workload_shapes():
     assert info["global_reverse"] == 1                                 # 2.4 MB KV fits in L2
     sp = W.spec("ragged")
     assert len(sp.seq_lens) == 256 and min(sp.seq_lens) >= 128 and max(sp.seq_lens) <= 16384
+    ind = fi.indptr_from_lens(sp.seq_lens)
+    info, _ = fi.fi_prefill_plan_host(ind, ind, 32, 8, 128, 16, with_list=False)
+    assert info["is_uniform"] == 0 and info["global_reverse"] == 0    # ragged: the L2 gate
 
 
 def test_balanced_schedule_for_few_units():
@@ -323,11 +335,11 @@ def test_decode_plan_rejects(args, code):
 
 
 def test_fp8_plan_counts_one_byte_per_element_in_the_l2_gate():
-    # 20 sequences of 2000 tokens, H_kv = 8, D = 128: the NVFP4 K+V bytes
-    # (72 per token and head and tensor) fit the gate 2 kv_bytes <= L2, the FP8
-    # bytes (128) do not
-    ind = fi.indptr_from_lens([2000] * 20)
-    tokens = 40000
+    # a ragged batch of 20 sequences of about 2000 tokens, H_kv = 8, D = 128:
+    # the NVFP4 K+V bytes (72 per token and head and tensor) fit the gate
+    # 2 kv_bytes <= L2, the FP8 bytes (128) do not
+    ind = fi.indptr_from_lens([2000] * 19 + [2001])
+    tokens = 40001
     nv, _ = fi.fi_prefill_plan_host(ind, ind, 32, 8, 128, 16, l2_bytes=L2, with_list=False)
     f8, _ = fi.fi_prefill_plan_host(ind, ind, 32, 8, 128, 16, l2_bytes=L2, with_list=False,
                                     kv_format=1)
