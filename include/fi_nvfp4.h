@@ -122,7 +122,9 @@ fi_status fi_nvfp4_append_host_scale(fi_context* ctx, const void* k_dev, const v
 
 /* Plan options (all zero = defaults). */
 typedef struct {
-  int32_t schedule; /* 0: decided by the L2 gate; 1: global reverse-Q-tile order;
+  int32_t schedule; /* 0: default (uniform batches: global reverse-Q-tile order;
+                       ragged batches: decided by the L2 gate, global order iff
+                       2 * KV bytes <= L2); 1: global reverse-Q-tile order;
                        2: per-(sequence, head) reverse order */
   int32_t num_ctas; /* persistent CTAs; 0 = number of SMs */
   int64_t l2_bytes; /* L2 size for the gate; 0 = the device's */
